@@ -1,0 +1,237 @@
+"""CPU oracle for the DSA layer group with IndexShare (test infrastructure).
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg use
+this package; the product library never imports it.  It wraps the plain C
+restatement in ``oracle.c`` (fp64 arithmetic on the exact input values) with
+numpy marshalling, plus the group loop of the method:
+
+* an F layer computes indexer scores and keeps the top-K positions, writing
+  them into the group's index buffer;
+* every layer (F or S) runs sparse MLA over that buffer with its own cache
+  ("GLM-5.2 架构深度拆解" CH 2.2 and 2.4; "GLM-5 -> 5.1 -> 5.2" section 10).
+
+Functions whose results are pinned by tests against values fixed by the
+pages or by mathematics are listed in ``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+P_U8 = ctypes.POINTER(ctypes.c_uint8)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, OpenMP, no FP contraction)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB)
+            vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            L.oracle_e4m3_decode.restype = dbl
+            L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3_encode.restype = ctypes.c_uint8
+            L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            L.oracle_hadamard128_f64.argtypes = [vp, vp]
+            L.oracle_fwht128_f32.argtypes = [vp]
+            L.oracle_fp8_quantize_rows.argtypes = [vp, i64, vp, vp]
+            L.oracle_indexer_scores.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp,
+                                                vp, vp, vp, vp, vp, vp, ctypes.c_int, i64, vp]
+            L.oracle_topk.argtypes = [vp, i64, vp, ctypes.c_int, ctypes.c_int, vp]
+            L.oracle_sparse_mla.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                                            vp, vp, ctypes.c_int, vp, ctypes.c_int, dbl, vp, vp]
+            L.oracle_dense_mla.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                                           vp, vp, vp, ctypes.c_int, dbl, vp, vp]
+            L.oracle_num_threads.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+# ---------------------------------------------------------------- FP8 / Hadamard
+def e4m3_decode(codes) -> np.ndarray:
+    codes = np.asarray(codes, dtype=np.uint8)
+    f = lib().oracle_e4m3_decode
+    return np.array([f(int(c)) for c in codes.ravel()], dtype=np.float64).reshape(codes.shape)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float32)
+    f = lib().oracle_e4m3_encode
+    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint8).reshape(x.shape)
+
+
+def hadamard128_f64(v) -> np.ndarray:
+    v, pv = _c(v, np.float64)
+    assert v.shape == (128,)
+    out = np.empty(128, np.float64)
+    lib().oracle_hadamard128_f64(pv, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def fwht128_f32(v) -> np.ndarray:
+    v = np.array(v, dtype=np.float32, copy=True)
+    assert v.shape == (128,)
+    lib().oracle_fwht128_f32(v.ctypes.data_as(ctypes.c_void_p))
+    return v
+
+
+def fp8_quantize_rows(x_bf16_bits):
+    """Hadamard-rotate and FP8-quantise rows of 128 bf16 values.
+    Returns (codes uint8 [rows,128], scale float32 [rows])."""
+    x, px = _c(x_bf16_bits, np.uint16)
+    rows = x.size // 128
+    q = np.empty((rows, 128), np.uint8)
+    s = np.empty(rows, np.float32)
+    lib().oracle_fp8_quantize_rows(px, rows, q.ctypes.data_as(ctypes.c_void_p),
+                                   s.ctypes.data_as(ctypes.c_void_p))
+    return q, s
+
+
+# ---------------------------------------------------------------- batch helpers
+def row_metadata(q_start, q_pos, seq_row0, rows):
+    """Per listed query row: its absolute position and the cache row of its
+    sequence's position 0."""
+    q_start = np.asarray(q_start, np.int64)
+    rows = np.asarray(rows, np.int64)
+    seq = np.searchsorted(q_start, rows, side="right") - 1
+    row_pos = np.asarray(q_pos, np.int64)[rows].astype(np.int32)
+    row_key0 = np.asarray(seq_row0, np.int64)[seq]
+    return row_pos, row_key0
+
+
+# ---------------------------------------------------------------- the method
+def indexer_scores(q_idx, w, k_idx, rows, row_pos, row_key0, max_len, *, dtype=0,
+                   q_scale=None, k_scale=None, Hi=None, Di=None):
+    """Scores [len(rows), max_len] in fp64; -inf beyond each row's position.
+    dtype 0: q_idx/k_idx are bf16 bit patterns (uint16); dtype 1: E4M3 codes
+    (uint8) with q_scale [num_q, Hi] and k_scale [rows] (float32)."""
+    q_idx = np.asarray(q_idx)
+    Hi = q_idx.shape[-2] if Hi is None else Hi
+    Di = q_idx.shape[-1] if Di is None else Di
+    et = np.uint16 if dtype == 0 else np.uint8
+    q_idx, pq = _c(q_idx, et)
+    k_idx, pk = _c(k_idx, et)
+    w, pw = _c(w, np.float32)
+    qs, pqs = _c(q_scale if q_scale is not None else np.zeros(1), np.float32)
+    ks, pks = _c(k_scale if k_scale is not None else np.zeros(1), np.float32)
+    rows, pr = _c(rows, np.int32)
+    row_pos, pp = _c(row_pos, np.int32)
+    row_key0, p0 = _c(row_key0, np.int64)
+    out = np.empty((rows.size, int(max_len)), np.float64)
+    lib().oracle_indexer_scores(Hi, Di, dtype, pq, pqs, pw, pk, pks, pr, pp, p0, rows.size,
+                                int(max_len), out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def topk(scores, lens, K):
+    """Top-K positions per row (ties: lower position), ascending, -1 padded."""
+    scores, ps = _c(scores, np.float64)
+    lens, pl = _c(lens, np.int32)
+    n = lens.size
+    out = np.empty((n, K), np.int32)
+    lib().oracle_topk(ps, scores.shape[-1], pl, n, K, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def sparse_mla(q_lat, q_rope, kv, rows, row_key0, idx, scale):
+    """Sparse MLA for the listed rows: (out [n,H,Dl] fp64, lse [n,H] fp64)."""
+    q_lat = np.asarray(q_lat)
+    H, Dl = q_lat.shape[-2], q_lat.shape[-1]
+    Dr = np.asarray(q_rope).shape[-1]
+    q_lat, pql = _c(q_lat, np.uint16)
+    q_rope, pqr = _c(q_rope, np.uint16)
+    kv, pkv = _c(kv, np.uint16)
+    rows, pr = _c(rows, np.int32)
+    row_key0, p0 = _c(row_key0, np.int64)
+    idx, pi = _c(idx, np.int32)
+    n, K = idx.shape
+    out = np.empty((n, H, Dl), np.float64)
+    lse = np.empty((n, H), np.float64)
+    lib().oracle_sparse_mla(H, Dl, Dr, pql, pqr, pkv, pr, p0, n, pi, K, float(scale),
+                            out.ctypes.data_as(ctypes.c_void_p), lse.ctypes.data_as(ctypes.c_void_p))
+    return out, lse
+
+
+def dense_mla(q_lat, q_rope, kv, rows, row_pos, row_key0, scale):
+    q_lat = np.asarray(q_lat)
+    H, Dl = q_lat.shape[-2], q_lat.shape[-1]
+    Dr = np.asarray(q_rope).shape[-1]
+    q_lat, pql = _c(q_lat, np.uint16)
+    q_rope, pqr = _c(q_rope, np.uint16)
+    kv, pkv = _c(kv, np.uint16)
+    rows, pr = _c(rows, np.int32)
+    row_pos, pp = _c(row_pos, np.int32)
+    row_key0, p0 = _c(row_key0, np.int64)
+    n = rows.size
+    out = np.empty((n, H, Dl), np.float64)
+    lse = np.empty((n, H), np.float64)
+    lib().oracle_dense_mla(H, Dl, Dr, pql, pqr, pkv, pr, pp, p0, n, float(scale),
+                           out.ctypes.data_as(ctypes.c_void_p), lse.ctypes.data_as(ctypes.c_void_p))
+    return out, lse
+
+
+def parse_layer_types(layer_types: str):
+    """'F' = full layer (runs the indexer), 'S' = shared layer (reuses the
+    nearest preceding F layer's indices).  The first layer must be F."""
+    if not layer_types or any(c not in "FS" for c in layer_types) or layer_types[0] != "F":
+        raise ValueError(f"bad layer_types {layer_types!r}")
+    return [c == "F" for c in layer_types]
+
+
+def group_forward(layer_types, layers, rows, row_pos, row_key0, max_len, K, scale, *,
+                  idx_dtype=0, keep_scores=False):
+    """One layer group for the listed query rows.
+
+    layers[l] is a dict with q_lat, q_rope, kv and, on F layers, q_idx, w,
+    k_idx (plus q_scale, k_scale for the FP8 indexer).  Returns a dict with
+    per-layer outputs, lse, the index buffer each layer used, and the scores
+    of each F layer when keep_scores is set."""
+    full = parse_layer_types(layer_types)
+    lens = np.minimum(np.asarray(row_pos, np.int64) + 1, int(max_len)).astype(np.int32)
+    res = {"out": [], "lse": [], "idx": [], "scores": [], "kth": []}
+    idx = None
+    for l, is_full in enumerate(full):
+        L = layers[l]
+        if is_full:
+            sc = indexer_scores(L["q_idx"], L["w"], L["k_idx"], rows, row_pos, row_key0, max_len,
+                                dtype=idx_dtype, q_scale=L.get("q_scale"), k_scale=L.get("k_scale"))
+            idx = topk(sc, lens, K)
+            if keep_scores:
+                res["scores"].append(sc)
+        o, s = sparse_mla(L["q_lat"], L["q_rope"], L["kv"], rows, row_key0, idx, scale)
+        res["out"].append(o)
+        res["lse"].append(s)
+        res["idx"].append(idx)
+    return res
