@@ -1,0 +1,318 @@
+// C ABI of the library: argument validation, workspace layout, status
+// handling, tensor-map construction and the IndexShare group loop.  Every
+// compute step is one of the kernels in indexer.cu, topk.cu, sparse_mla.cu
+// and quant.cu; nothing here computes on the host.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+
+namespace dsa {
+
+namespace {
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches[kNumLaunchKinds];
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+dsa_status_t fail(dsa_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+dsa_status_t fail(dsa_status_t s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+dsa_status_t cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return DSA_OK;
+  return fail(DSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dsa_status_t check_batch(const dsa_batch_t* b) {
+  if (!b) return fail(DSA_ERR_INVALID_ARG, "batch is NULL");
+  if (b->num_seqs < 1 || b->num_q < 0 || b->max_q < 0 || b->max_len < 128 ||
+      b->max_len % 128 != 0)
+    return fail(DSA_ERR_INVALID_ARG,
+                "batch sizes: num_seqs=%d num_q=%d max_q=%d max_len=%d (max_len must be a "
+                "positive multiple of 128)",
+                b->num_seqs, b->num_q, b->max_q, b->max_len);
+  if (b->num_q > 0 && b->max_q < 1)
+    return fail(DSA_ERR_INVALID_ARG, "max_q must be >= 1 when num_q > 0");
+  if (b->max_q > b->num_q) return fail(DSA_ERR_INVALID_ARG, "max_q > num_q");
+  if (b->num_seqs > 65535) return fail(DSA_ERR_UNSUPPORTED, "num_seqs > 65535");
+  if (!b->q_start || !b->q_pos || !b->seq_row0)
+    return fail(DSA_ERR_INVALID_ARG, "batch arrays must be non-NULL device pointers");
+  return DSA_OK;
+}
+
+dsa_status_t check_ws(void* ws, size_t have, size_t need) {
+  if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return fail(DSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (have < need)
+    return fail(DSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", have, need);
+  return DSA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+dsa_status_t check_indexer_args(const void* q_idx, const float* q_scale, const float* w,
+                                const void* k_idx, const float* k_scale, int64_t k_rows,
+                                dsa_dtype_t dt) {
+  if (dt != DSA_BF16 && dt != DSA_FP8_E4M3) return fail(DSA_ERR_UNSUPPORTED, "indexer dtype %d", dt);
+  if (!q_idx || !w || !k_idx) return fail(DSA_ERR_INVALID_ARG, "q_idx, w and k_idx are required");
+  if (dt == DSA_FP8_E4M3 && (!q_scale || !k_scale))
+    return fail(DSA_ERR_INVALID_ARG, "FP8 indexer needs q_scale and k_scale");
+  if (!aligned16(q_idx) || !aligned16(k_idx))
+    return fail(DSA_ERR_INVALID_ARG, "q_idx and k_idx must be 16-byte aligned");
+  if (k_rows < 1) return fail(DSA_ERR_INVALID_ARG, "k_rows must be >= 1");
+  if (k_rows > (int64_t(1) << 31) - 1) return fail(DSA_ERR_UNSUPPORTED, "k_rows >= 2^31");
+  return DSA_OK;
+}
+
+dsa_status_t check_mla_args(const void* q_lat, const void* q_rope, const void* kv, int64_t kv_rows,
+                            const int32_t* idx, int32_t k, int32_t heads, float scale,
+                            const dsa_batch_t* b, const void* out) {
+  if (heads != 16 && heads != 64)
+    return fail(DSA_ERR_UNSUPPORTED, "heads=%d (supported: 16, 64)", heads);
+  if (k < 1 || k > 4096) return fail(DSA_ERR_UNSUPPORTED, "k=%d (supported: 1..4096)", k);
+  if (!q_lat || !q_rope || !kv || !idx || !out)
+    return fail(DSA_ERR_INVALID_ARG, "q_lat, q_rope, kv, idx and out are required");
+  if (!aligned16(q_lat) || !aligned16(q_rope) || !aligned16(kv) || !aligned16(out))
+    return fail(DSA_ERR_INVALID_ARG, "q_lat, q_rope, kv and out must be 16-byte aligned");
+  if (kv_rows < 1 || kv_rows > (int64_t(1) << 31) - 1)
+    return fail(DSA_ERR_INVALID_ARG, "kv_rows=%lld", static_cast<long long>(kv_rows));
+  if (!(scale == scale)) return fail(DSA_ERR_INVALID_ARG, "scale is NaN");
+  if (static_cast<int64_t>(b->num_q) * heads > (int64_t(1) << 31) - 1)
+    return fail(DSA_ERR_UNSUPPORTED, "num_q * heads >= 2^31");
+  return DSA_OK;
+}
+
+dsa_status_t launch_status(cudaError_t e, const char* where) { return cuda_status(e, where); }
+
+}  // namespace
+
+// ------------------------------------------------------------- host helpers
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
+                  uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      g_last_error = "cuTensorMapEncodeTiled unavailable";
+      return false;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu]", static_cast<int>(r),
+             static_cast<unsigned long long>(rows), static_cast<unsigned long long>(inner));
+    g_last_error = buf;
+    return false;
+  }
+  return true;
+}
+
+void count_launch(int which) { g_launches[which].fetch_add(1, std::memory_order_relaxed); }
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+const char* dsa_last_error_string(void) { return g_last_error.c_str(); }
+
+size_t dsa_status_bytes(void) { return kStatusBytes; }
+
+dsa_status_t dsa_workspace_init(void* d_ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (dsa_status_t s = check_ws(d_ws, ws_bytes, kStatusBytes)) return s;
+  return cuda_status(cudaMemsetAsync(d_ws, 0, kStatusBytes, stream), "cudaMemsetAsync");
+}
+
+dsa_status_t dsa_status_fetch(void* d_ws, dsa_stream_t stream, int32_t* raw_bits) {
+  if (!d_ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
+  int32_t bits = 0;
+  if (dsa_status_t s = cuda_status(cudaMemcpyAsync(&bits, d_ws, 4, cudaMemcpyDeviceToHost, stream),
+                                   "cudaMemcpyAsync"))
+    return s;
+  if (dsa_status_t s = cuda_status(cudaStreamSynchronize(stream), "cudaStreamSynchronize")) return s;
+  if (bits) {
+    if (dsa_status_t s = cuda_status(cudaMemsetAsync(d_ws, 0, 4, stream), "cudaMemsetAsync")) return s;
+  }
+  if (raw_bits) *raw_bits = bits;
+  if (bits & DSA_DEVERR_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a bounded wait in a kernel ran out");
+  if (bits & (DSA_DEVERR_INDEX | DSA_DEVERR_BATCH))
+    return fail(DSA_ERR_DEVICE_INDEX, "a kernel found an index or batch entry out of range (bits %d)", bits);
+  return DSA_OK;
+}
+
+int dsa_launch_counts(uint64_t* counts, int n) {
+  for (int i = 0; i < n && i < kNumLaunchKinds; ++i) counts[i] = g_launches[i].load();
+  return kNumLaunchKinds;
+}
+void dsa_launch_counts_reset(void) {
+  for (auto& c : g_launches) c.store(0);
+}
+
+void dsa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
+
+dsa_status_t dsa_selftest_wait_timeout(void* d_ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (dsa_status_t s = check_ws(d_ws, ws_bytes, kStatusBytes)) return s;
+  return launch_status(launch_selftest_wait(static_cast<int*>(d_ws), stream), "selftest launch");
+}
+
+// ------------------------------------------------------------- a1: scores
+size_t dsa_indexer_workspace_size(const dsa_batch_t*) { return kStatusBytes; }
+
+dsa_status_t dsa_indexer_scores(const void* q_idx, const float* q_scale, const float* w,
+                                const void* k_idx, const float* k_scale, int64_t k_rows,
+                                dsa_dtype_t dt, const dsa_batch_t* b, float* scores, void* ws,
+                                size_t ws_bytes, dsa_stream_t stream) {
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (dsa_status_t s = check_indexer_args(q_idx, q_scale, w, k_idx, k_scale, k_rows, dt)) return s;
+  if (!scores || !aligned16(scores)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
+  if (dsa_status_t s = check_ws(ws, ws_bytes, kStatusBytes)) return s;
+  return launch_status(launch_indexer(q_idx, q_scale, w, k_idx, k_scale, k_rows,
+                                      dt == DSA_FP8_E4M3, *b, scores, true,
+                                      static_cast<int*>(ws), stream),
+                       "indexer launch");
+}
+
+// ------------------------------------------------------------- a2: top-K
+size_t dsa_topk_workspace_size(const dsa_batch_t*, int32_t) { return kStatusBytes; }
+
+dsa_status_t dsa_topk(const float* scores, const dsa_batch_t* b, int32_t k, int32_t* idx, void* ws,
+                      size_t ws_bytes, dsa_stream_t stream) {
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (k < 1 || k > 4096) return fail(DSA_ERR_UNSUPPORTED, "k=%d (supported: 1..4096)", k);
+  if (!scores || !idx) return fail(DSA_ERR_INVALID_ARG, "scores and idx are required");
+  if (!aligned16(scores)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
+  if (dsa_status_t s = check_ws(ws, ws_bytes, kStatusBytes)) return s;
+  return launch_status(launch_topk(scores, *b, k, idx, static_cast<int*>(ws), stream), "top-K launch");
+}
+
+// ------------------------------------------------------------- a4-a5: sparse MLA
+size_t dsa_sparse_mla_workspace_size(const dsa_batch_t* b, int32_t heads, int32_t k) {
+  if (!b) return kStatusBytes;
+  return kStatusBytes + round256(mla_workspace_bytes(*b, heads, k));
+}
+
+dsa_status_t dsa_sparse_mla_attn(const void* q_lat, const void* q_rope, const void* kv,
+                                 int64_t kv_rows, const int32_t* idx, int32_t k, int32_t heads,
+                                 float scale, const dsa_batch_t* b, void* out, float* lse, void* ws,
+                                 size_t ws_bytes, dsa_stream_t stream) {
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (dsa_status_t s = check_mla_args(q_lat, q_rope, kv, kv_rows, idx, k, heads, scale, b, out)) return s;
+  const size_t need = dsa_sparse_mla_workspace_size(b, heads, k);
+  if (dsa_status_t s = check_ws(ws, ws_bytes, need)) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  return launch_status(launch_sparse_mla(q_lat, q_rope, kv, kv_rows, idx, k, heads, scale, *b, out,
+                                         lse, wsb + kStatusBytes, need - kStatusBytes,
+                                         static_cast<int*>(ws), stream),
+                       "sparse MLA launch");
+}
+
+// ------------------------------------------------------------- a6: group
+size_t dsa_group_workspace_size(const dsa_group_t* g, const dsa_batch_t* b) {
+  if (!g || !b) return kStatusBytes;
+  const size_t scores = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4);
+  const size_t mla = round256(mla_workspace_bytes(*b, g->heads, g->k));
+  return kStatusBytes + (scores > mla ? scores : mla);
+}
+
+dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b, int32_t* idx_buf,
+                                      void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (!g) return fail(DSA_ERR_INVALID_ARG, "group is NULL");
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (!g->layer_types || g->layer_types[0] != 'F')
+    return fail(DSA_ERR_INVALID_ARG, "layer_types must start with F");
+  const int nl = static_cast<int>(strlen(g->layer_types));
+  if (nl > 4096) return fail(DSA_ERR_INVALID_ARG, "layer_types too long");
+  for (int l = 0; l < nl; ++l)
+    if (g->layer_types[l] != 'F' && g->layer_types[l] != 'S')
+      return fail(DSA_ERR_INVALID_ARG, "layer_types[%d] = '%c' (want F or S)", l, g->layer_types[l]);
+  if (!g->q_lat || !g->q_rope || !g->kv || !g->out || !idx_buf)
+    return fail(DSA_ERR_INVALID_ARG, "q_lat, q_rope, kv, out arrays and idx_buf are required");
+  for (int l = 0; l < nl; ++l) {
+    if (dsa_status_t s = check_mla_args(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, idx_buf,
+                                        g->k, g->heads, g->scale, b, g->out[l]))
+      return s;
+    if (g->layer_types[l] == 'F') {
+      if (!g->q_idx || !g->w || !g->k_idx ||
+          (g->idx_dtype == DSA_FP8_E4M3 && (!g->q_scale || !g->k_scale)))
+        return fail(DSA_ERR_INVALID_ARG, "F layer %d: indexer arrays missing", l);
+      if (dsa_status_t s = check_indexer_args(g->q_idx[l], g->q_scale ? g->q_scale[l] : nullptr,
+                                              g->w[l], g->k_idx[l],
+                                              g->k_scale ? g->k_scale[l] : nullptr, g->k_rows,
+                                              g->idx_dtype))
+        return s;
+    }
+  }
+  const size_t need = dsa_group_workspace_size(g, b);
+  if (dsa_status_t s = check_ws(ws, ws_bytes, need)) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  int* status = static_cast<int*>(ws);
+  float* scores = reinterpret_cast<float*>(wsb + kStatusBytes);
+  const bool fp8 = g->idx_dtype == DSA_FP8_E4M3;
+  for (int l = 0; l < nl; ++l) {
+    if (g->layer_types[l] == 'F') {
+      // F layer: candidate scoring, then top-K into the shared index buffer
+      if (dsa_status_t s = launch_status(
+              launch_indexer(g->q_idx[l], fp8 ? g->q_scale[l] : nullptr, g->w[l], g->k_idx[l],
+                             fp8 ? g->k_scale[l] : nullptr, g->k_rows, fp8, *b, scores, false,
+                             status, stream),
+              "indexer launch"))
+        return s;
+      if (dsa_status_t s = launch_status(launch_topk(scores, *b, g->k, idx_buf, status, stream),
+                                         "top-K launch"))
+        return s;
+    }
+    // every layer: gather from its own cache + sparse attention over idx_buf
+    if (dsa_status_t s = launch_status(
+            launch_sparse_mla(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, idx_buf, g->k,
+                              g->heads, g->scale, *b, g->out[l], g->lse ? g->lse[l] : nullptr,
+                              wsb + kStatusBytes, need - kStatusBytes, status, stream),
+            "sparse MLA launch"))
+      return s;
+  }
+  return DSA_OK;
+}
+
+// ------------------------------------------------------------- a7: FP8 quantiser
+dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
+                              dsa_stream_t stream) {
+  if (rows < 0) return fail(DSA_ERR_INVALID_ARG, "rows < 0");
+  if (rows > 0 && (!x || !codes || !scale))
+    return fail(DSA_ERR_INVALID_ARG, "x, codes and scale are required");
+  if (rows > 0 && (!aligned16(x) || !aligned16(codes)))
+    return fail(DSA_ERR_INVALID_ARG, "x and codes must be 16-byte aligned");
+  if (rows > (int64_t(1) << 34)) return fail(DSA_ERR_UNSUPPORTED, "rows too large");
+  return launch_status(launch_quantize(x, rows, codes, scale, stream), "quantiser launch");
+}
+
+}  // extern "C"

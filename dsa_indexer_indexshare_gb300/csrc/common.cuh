@@ -1,0 +1,74 @@
+// Internal declarations shared by the kernels and the host launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/dsa.h"
+#include "ptx.cuh"
+
+namespace dsa {
+
+constexpr size_t kStatusBytes = 256;
+
+// Device view of dsa_batch_t (plain values, passed by value to kernels).
+struct BatchArgs {
+  int32_t num_seqs, num_q, max_q, max_len;
+  const int32_t* q_start;
+  const int32_t* q_pos;
+  const int64_t* seq_row0;
+};
+
+inline BatchArgs to_args(const dsa_batch_t& b) {
+  return BatchArgs{b.num_seqs, b.num_q, b.max_q, b.max_len, b.q_start, b.q_pos, b.seq_row0};
+}
+
+// Rows [qs, qe) of sequence `seq`, validated against the batch sizes.  On
+// inconsistency records DSA_DEVERR_BATCH and returns an empty range.
+__device__ __forceinline__ void seq_rows(const BatchArgs& b, int seq, int* status, int& qs,
+                                         int& qe) {
+  qs = b.q_start[seq];
+  qe = b.q_start[seq + 1];
+  if (qs < 0 || qe < qs || qe > b.num_q) {
+    if (threadIdx.x == 0) atomicOr(status, DSA_DEVERR_BATCH);
+    qs = qe = 0;
+  }
+}
+
+// Position of query t, or -1 (with DSA_DEVERR_BATCH) when outside [0, max_len).
+__device__ __forceinline__ int query_pos(const BatchArgs& b, int t, int* status) {
+  int p = b.q_pos[t];
+  if (p < 0 || p >= b.max_len) {
+    if (status) atomicOr(status, DSA_DEVERR_BATCH);
+    return -1;
+  }
+  return p;
+}
+
+// ------------------------------------------------------------- host helpers
+// Implemented in api.cu.
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
+                  uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows);
+void count_launch(int which);
+uint64_t wait_timeout_ns();
+
+enum LaunchKind { kLaunchIndexer = 0, kLaunchTopk, kLaunchMla, kLaunchCombine, kLaunchQuant,
+                  kLaunchOther, kNumLaunchKinds };
+
+// Launchers (return a CUDA error code; argument checks are done by api.cu).
+cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float* w,
+                           const void* k_idx, const float* k_scale, int64_t k_rows, bool fp8,
+                           const dsa_batch_t& b, float* scores, bool fill_tail, int* status,
+                           cudaStream_t stream);
+cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_t* idx,
+                        int* status, cudaStream_t stream);
+size_t mla_workspace_bytes(const dsa_batch_t& b, int heads, int k);
+cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void* kv,
+                              int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
+                              const dsa_batch_t& b, void* out, float* lse, void* ws_extra,
+                              size_t ws_extra_bytes, int* status, cudaStream_t stream);
+cudaError_t launch_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
+                            cudaStream_t stream);
+cudaError_t launch_selftest_wait(int* status, cudaStream_t stream);
+
+}  // namespace dsa

@@ -1,0 +1,327 @@
+// Lightning-indexer scoring on the tcgen05 tensor cores.
+//
+//   scores[t, s] = sum_{j<32} w[t,j] * ReLU(q_idx[t,j,:] . k_idx[s,:])
+//
+// ("GLM-5.2 / 总览" config table: 32 heads x 128 dims; sub-doc index row 02:
+// ReLU, FP8 per-block + Hadamard variant; "GLM-5.2 架构深度拆解" CH 2.2.)
+//
+// The contraction runs with the KEYS on the MMA M dimension (128 keys per
+// tile) and the (token, head) pairs of a block of NTOK queries on N, so that
+// TMEM lane i holds every head's dot product for key i.  The epilogue then
+// reduces over heads with ReLU and the head weights thread-locally (no
+// shuffles) and writes a coalesced row segment of scores per token.
+//
+// Warp roles (192 threads): warps 0-3 epilogue (thread = TMEM lane = key),
+// warp 4 TMA producer, warp 5 MMA issuer (and TMEM owner).  The key tiles
+// stream through a STAGES-deep shared-memory ring; the accumulator is double
+// buffered in TMEM so the epilogue of tile i overlaps the MMAs of tile i+1.
+#include "common.cuh"
+
+namespace dsa {
+namespace {
+
+template <int NTOK, bool FP8, int STAGES>
+struct IdxCfg {
+  static constexpr int N = NTOK * 32;                // MMA N: (token, head) pairs
+  static constexpr int KSUB = FP8 ? 1 : 2;           // 128-byte swizzle atoms per 128-d row
+  static constexpr int Q_SUB = N * 128;              // bytes of one Q sub-tile
+  static constexpr int Q_BYTES = KSUB * Q_SUB;
+  static constexpr int K_SUB = 128 * 128;            // bytes of one K sub-tile (128 keys)
+  static constexpr int K_BYTES = KSUB * K_SUB;
+  static constexpr int KSTEPS = FP8 ? 4 : 8;         // MMA K-steps of 32 bytes each
+  static constexpr int TMEM_COLS = 2 * N < 32 ? 32 : 2 * N;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_W = OFF_K + STAGES * K_BYTES;
+  static constexpr int OFF_BAR = OFF_W + N * 4;
+  static constexpr int NBAR = 1 + 2 * STAGES + 4 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
+  static_assert(STAGES >= 2, "need a ring");
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+struct IndexerParams {
+  BatchArgs b;
+  const float* w;
+  const float* q_scale;
+  const float* k_scale;
+  int64_t k_rows;
+  float* scores;
+  int* status;
+  int kc_blocks;   // 128-key blocks per CTA
+  int num_kc;      // key chunks per query block
+  int num_qb;      // query blocks per sequence
+  int fill_tail;   // write -inf beyond the computed blocks
+  uint64_t timeout_ns;
+};
+
+// Wait until the tcgen05.ld results in v are valid; the asm takes v as
+// in/out operands so that no use of v can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld_dep(float (&v)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                 "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                 "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]),
+                 "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]),
+                 "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]),
+                 "+f"(v[30]), "+f"(v[31])
+               :
+               : "memory");
+}
+
+template <int NTOK, bool FP8, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap qmap,
+                   const __grid_constant__ CUtensorMap kmap, const IndexerParams p) {
+  using C = IdxCfg<NTOK, FP8, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- work unit: (sequence, query block, key chunk); heavy query blocks first
+  const int seq = blockIdx.y;
+  const int kc = blockIdx.x % p.num_kc;
+  const int qb = p.num_qb - 1 - static_cast<int>(blockIdx.x / p.num_kc);
+  int qs, qe;
+  seq_rows(p.b, seq, p.status, qs, qe);
+  const int q0 = qs + qb * NTOK;
+  if (q0 >= qe) return;
+  const int nq = min(NTOK, qe - q0);
+  int pos[NTOK];
+  int pmax = -1;
+#pragma unroll
+  for (int n = 0; n < NTOK; ++n) {
+    pos[n] = n < nq ? query_pos(p.b, q0 + n, tid == 0 ? p.status : nullptr) : -1;
+    pmax = max(pmax, pos[n]);
+  }
+  const int s_begin = kc * p.kc_blocks * 128;
+  if (s_begin >= p.b.max_len) return;
+  const int s_stop = min(s_begin + p.kc_blocks * 128, p.b.max_len);
+  const int nkb = pmax < s_begin ? 0 : min(p.kc_blocks, (pmax - s_begin) / 128 + 1);
+  if (p.fill_tail) {
+    const int f0 = s_begin + nkb * 128;
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    for (int n = 0; n < nq; ++n) {
+      float* row = p.scores + static_cast<int64_t>(q0 + n) * p.b.max_len;
+      for (int s = f0 + tid * 4; s < s_stop; s += 192 * 4)
+        *reinterpret_cast<float4*>(row + s) = ninf;
+    }
+  }
+  if (nkb == 0) return;
+  const int64_t row0 = p.b.seq_row0[seq];
+
+  // ---- shared memory, barriers, TMEM
+  const uint32_t sQ = smem_u32(sm + C::OFF_Q);
+  const uint32_t sK = smem_u32(sm + C::OFF_K);
+  float* sW = reinterpret_cast<float*>(sm + C::OFF_W);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC + 8);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 1 + STAGES, B_ACCF = 1 + 2 * STAGES,
+            B_ACCE = 3 + 2 * STAGES, B_DONE = 5 + 2 * STAGES;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(B_QFULL), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(B_ACCF + a), 1);
+      mbar_init(bar(B_ACCE + a), 128);
+    }
+    mbar_init(bar(B_DONE), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (tid < 128) {
+    for (int i = tid; i < C::N; i += 128) {
+      const int n = i >> 5, j = i & 31;
+      float v = 0.f;
+      if (n < nq) {
+        v = p.w[static_cast<int64_t>(q0 + n) * 32 + j];
+        if (FP8) v *= p.q_scale[static_cast<int64_t>(q0 + n) * 32 + j];
+      }
+      sW[i] = v;
+    }
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&kmap);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint64_t to = p.timeout_ns;
+  volatile int no_abort = 0;
+
+  if (warp == 4) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(B_QFULL), C::Q_BYTES);
+#pragma unroll
+      for (int ks = 0; ks < C::KSUB; ++ks)
+        tma_load_2d(sQ + ks * C::Q_SUB, &qmap, ks * 64, q0 * 32, bar(B_QFULL));
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int st = i % STAGES;
+        if (i >= STAGES &&
+            !mbar_wait(bar(B_KEMPTY + st), ((i / STAGES) - 1) & 1, abort_flag, p.status, to))
+          break;
+        mbar_arrive_expect_tx(bar(B_KFULL + st), C::K_BYTES);
+        const int y = static_cast<int>(row0 + s_begin + i * 128);
+#pragma unroll
+        for (int ks = 0; ks < C::KSUB; ++ks)
+          tma_load_2d(sK + st * C::K_BYTES + ks * C::K_SUB, &kmap, ks * 64, y, bar(B_KFULL + st));
+        issued = i + 1;
+      }
+      // let every copy this CTA started land before it can exit
+      mbar_wait(bar(B_QFULL), 0, &no_abort, nullptr, to);
+      for (int i = max(0, issued - STAGES); i < issued; ++i)
+        mbar_wait(bar(B_KFULL + i % STAGES), (i / STAGES) & 1, &no_abort, nullptr, to);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = FP8 ? idesc_e4m3(128, C::N) : idesc_bf16(128, C::N, false, false);
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, p.status, to);
+      for (int i = 0; ok && i < nkb; ++i) {
+        const int st = i % STAGES, acc = i & 1;
+        if (!mbar_wait(bar(B_KFULL + st), (i / STAGES) & 1, abort_flag, p.status, to)) break;
+        if (i >= 2 && !mbar_wait(bar(B_ACCE + acc), ((i >> 1) - 1) & 1, abort_flag, p.status, to))
+          break;
+        tc_fence_after();
+        const uint32_t d = tbase + acc * C::N;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS; ++kk) {
+          const uint32_t off = FP8 ? kk * 32 : (kk >> 2) * C::K_SUB + (kk & 3) * 32;
+          const uint32_t qoff = FP8 ? kk * 32 : (kk >> 2) * C::Q_SUB + (kk & 3) * 32;
+          const uint64_t ad = sdesc_sw128(sK + st * C::K_BYTES + off, 0, 1024);
+          const uint64_t bd = sdesc_sw128(sQ + qoff, 0, 1024);
+          if (FP8)
+            umma_f8(d, ad, bd, idesc, kk > 0);
+          else
+            umma_bf16(d, ad, bd, idesc, kk > 0);
+        }
+        umma_commit(bar(B_KEMPTY + st));
+        umma_commit(bar(B_ACCF + acc));
+      }
+      umma_commit(bar(B_DONE));
+      mbar_wait(bar(B_DONE), 0, &no_abort, nullptr, to);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue: ReLU . w over heads
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int i = 0; i < nkb; ++i) {
+      const int acc = i & 1;
+      if (!mbar_wait(bar(B_ACCF + acc), (i >> 1) & 1, abort_flag, p.status, to)) break;
+      tc_fence_after();
+      const int s = s_begin + i * 128 + tid;
+      float kscale = 1.f;
+      if (FP8) {
+        const int64_t kr = row0 + s;
+        kscale = kr < p.k_rows ? p.k_scale[kr] : 0.f;
+      }
+#pragma unroll
+      for (int n = 0; n < NTOK; ++n) {
+        float v[32];
+        tmem_ld32(lane_base + acc * C::N + n * 32, v);
+        tmem_wait_ld_dep(v);
+        if (n < nq) {
+          const float4* wv = reinterpret_cast<const float4*>(sW + n * 32);
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 ww = wv[j4];
+            a0 = fmaf(ww.x, fmaxf(v[4 * j4 + 0], 0.f), a0);
+            a1 = fmaf(ww.y, fmaxf(v[4 * j4 + 1], 0.f), a1);
+            a2 = fmaf(ww.z, fmaxf(v[4 * j4 + 2], 0.f), a2);
+            a3 = fmaf(ww.w, fmaxf(v[4 * j4 + 3], 0.f), a3);
+          }
+          float sc = (a0 + a1) + (a2 + a3);
+          if (FP8) sc *= kscale;
+          if (s > pos[n]) sc = -INFINITY;
+          p.scores[static_cast<int64_t>(q0 + n) * p.b.max_len + s] = sc;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_ACCE + acc));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+template <int NTOK, bool FP8, int STAGES>
+cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, IndexerParams p,
+                       cudaStream_t stream) {
+  using C = IdxCfg<NTOK, FP8, STAGES>;
+  auto* kern = indexer_kernel<NTOK, FP8, STAGES>;
+  static int configured_device = -1;  // attribute is per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  p.num_qb = (p.b.max_q + NTOK - 1) / NTOK;
+  p.num_kc = (p.b.max_len + p.kc_blocks * 128 - 1) / (p.kc_blocks * 128);
+  dim3 grid(static_cast<unsigned>(p.num_qb) * static_cast<unsigned>(p.num_kc),
+            static_cast<unsigned>(p.b.num_seqs));
+  kern<<<grid, 192, C::SMEM, stream>>>(qmap, kmap, p);
+  count_launch(kLaunchIndexer);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float* w,
+                           const void* k_idx, const float* k_scale, int64_t k_rows, bool fp8,
+                           const dsa_batch_t& b, float* scores, bool fill_tail, int* status,
+                           cudaStream_t stream) {
+  if (b.num_q == 0) return cudaSuccess;
+  const bool decode = b.max_q <= 1;
+  const int ntok = decode ? 1 : 8;
+  const auto dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int es = fp8 ? 1 : 2;
+  const uint32_t box_inner = fp8 ? 128 : 64;
+  CUtensorMap qmap, kmap;
+  if (!make_tmap_2d(&qmap, q_idx, dt, es, 128, static_cast<uint64_t>(b.num_q) * 32, box_inner,
+                    ntok * 32))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&kmap, k_idx, dt, es, 128, static_cast<uint64_t>(k_rows), box_inner, 128))
+    return cudaErrorInvalidValue;
+  IndexerParams p{};
+  p.b = to_args(b);
+  p.w = w;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.k_rows = k_rows;
+  p.scores = scores;
+  p.status = status;
+  p.kc_blocks = decode ? 32 : 16;
+  p.fill_tail = fill_tail ? 1 : 0;
+  p.timeout_ns = wait_timeout_ns();
+  if (decode)
+    return fp8 ? launch_one<1, true, 6>(qmap, kmap, p, stream)
+               : launch_one<1, false, 3>(qmap, kmap, p, stream);
+  return fp8 ? launch_one<8, true, 6>(qmap, kmap, p, stream)
+             : launch_one<8, false, 4>(qmap, kmap, p, stream);
+}
+
+}  // namespace dsa

@@ -1,0 +1,542 @@
+// Absorbed-MLA sparse attention over the selected positions of one layer.
+//
+//   z_s = scale * (q_lat[t,h] . C[s,:512] + q_rope[t,h] . C[s,512:])
+//   out[t,h] = sum_s softmax(z)_s C[s,:512]
+//
+// ("GLM-5.2 / 总览" config table: the 512-d latent is both key and value, the
+// 64-d RoPE key enters only the score, QK head dim 256 -> scale 1/16;
+// "GLM-5 -> 5.1 -> 5.2" section 10: each layer gathers the selected entries
+// of its own cache, then runs sparse attention.)
+//
+// GB300 design.  One CTA (or a cluster of NSPLIT CTAs, for decode) per query
+// token.  Both products run on tcgen05 with the 128 gathered KEYS on the MMA
+// M dimension:
+//   S^T[128 keys, H]   = C[128, 576] . Q[H, 576]^T         (A = C, K-major)
+//   O^T[512 dims, H]  += C[128, :512]^T . P^T[H, 128]^T     (A = C^T, MN-major)
+// so both contractions use the full 128-row datapath even with H = 64 (or
+// 16) heads.  The selected rows are gathered with TMA gather4 (four rows per
+// copy, 128-byte swizzle) straight into the MMA operand layout, one 64-column
+// sub-tile at a time, and each sub-tile is refilled for the next block as
+// soon as the P.V chunk that reads it completes.  P^T reuses the RoPE
+// sub-tile, which is free once S^T is computed.
+//
+// Softmax: the thread of TMEM lane i owns key i of the block; at H = 64 two
+// warps share each lane quarter, one per half of the heads.  The running maximum per head is only raised when a block
+// exceeds it by more than 2^8 (then O^T and the partial sums are rescaled in
+// place); row sums are kept per thread and reduced once at the end.
+//
+// Warp roles: softmax / epilogue warps (8 at H = 64, 4 at H = 16), then one
+// TMA producer warp and one MMA issuer warp (also the TMEM owner).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int H>
+struct MlaCfg {
+  static constexpr int QSUB = H * 128;       // one 64-dim sub-tile of Q: H rows x 128 B
+  static constexpr int Q_BYTES = 9 * QSUB;
+  static constexpr int CSUB = 128 * 128;     // one 64-dim sub-tile of 128 gathered rows
+  static constexpr int PSUB = H * 128;       // P^T sub-tile: H rows x 64 keys
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_C = OFF_Q + Q_BYTES;
+  static constexpr int OFF_P = OFF_C + 8 * CSUB;  // the RoPE sub-tile
+  static constexpr int OFF_SCR = OFF_C + 9 * CSUB;
+  // scratch (floats): m_used[H], red[4][H], lsum[H], fac[8][H]; flags[NSW]
+  static constexpr int SCR_FLOATS = H + 4 * H + H + 8 * H;
+  static constexpr int OFF_FLAGS = OFF_SCR + SCR_FLOATS * 4;
+  static constexpr int OFF_BAR = (OFF_FLAGS + 4 * 8 + 7) & ~7;
+  static constexpr int NBAR = 1 + 9 + 4 + 3;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  static constexpr int HW = H > 32 ? 32 : H;       // heads per softmax warp
+  static constexpr int NSW = 4 * (H / HW);           // softmax warps (two per lane quarter at H=64)
+  static constexpr int NT = NSW * 32 + 64;           // + producer warp + MMA warp
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TM_S = 0;        // S^T: H columns
+  static constexpr uint32_t TM_O = 256;      // O^T chunk c: columns 256 + c*H
+  static_assert(OFF_C % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-B alignment");
+  static_assert(PSUB * 2 <= CSUB, "P^T must fit in the RoPE sub-tile");
+  static_assert(H * 512 * 4 <= 9 * CSUB, "O staging must fit in the C tile");
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+struct MlaParams {
+  BatchArgs b;
+  const int32_t* idx;
+  int K;
+  float scale_log2;
+  uint16_t* out;
+  float* lse;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int NV>
+__device__ __forceinline__ void wait_ld_dep(float (&v)[NV]) {
+  static_assert(NV == 16 || NV == 32, "");
+  if constexpr (NV == 32) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                   "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                   "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]),
+                   "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]),
+                   "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]),
+                   "+f"(v[30]), "+f"(v[31])
+                 :
+                 : "memory");
+  } else {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                   "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                   "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15])
+                 :
+                 : "memory");
+  }
+}
+
+// Load / store NV consecutive fp32 TMEM columns of this thread's lane.
+template <int NV>
+__device__ __forceinline__ void tmem_cols_load(uint32_t taddr, float (&v)[NV]) {
+  if constexpr (NV == 16)
+    tmem_ld16(taddr, v);
+  else
+    tmem_ld32(taddr, v);
+  wait_ld_dep(v);
+}
+template <int NV>
+__device__ __forceinline__ void tmem_cols_store(uint32_t taddr, const float (&v)[NV]) {
+  if constexpr (NV == 16)
+    tmem_st16(taddr, v);
+  else
+    tmem_st32(taddr, v);
+}
+
+template <int H, int NSPLIT>
+__global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap qlat_map,
+                      const __grid_constant__ CUtensorMap qrope_map,
+                      const __grid_constant__ CUtensorMap kv_map, const MlaParams p) {
+  using C = MlaCfg<H>;
+  constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
+  constexpr int W_PROD = NSW, W_MMA = NSW + 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = NSPLIT > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+
+  // ---- token of this CTA (cluster): heaviest (latest) tokens first
+  const int seq = blockIdx.y;
+  const int qi = p.b.max_q - 1 - static_cast<int>(blockIdx.x / NSPLIT);
+  int qs, qe;
+  seq_rows(p.b, seq, p.status, qs, qe);
+  const int t = qs + qi;
+  if (t >= qe) return;  // uniform over the cluster
+  const int pos = query_pos(p.b, t, (tid == 0 && rank == 0) ? p.status : nullptr);
+  const int nvalid = pos < 0 ? 0 : min(p.K, pos + 1);
+  const int nb = (nvalid + 127) / 128;
+  const int j0 = rank * nb / NSPLIT, j1 = (rank + 1) * nb / NSPLIT;  // this CTA's blocks
+  const int64_t row0 = p.b.seq_row0[seq];
+  const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.K;
+  if (nb == 0) {  // nothing visible: zero output, lse = -inf
+    constexpr int DS = 512 / NSPLIT;
+    for (int i = tid; i < H * DS; i += NT) {
+      const int h = i / DS, d = rank * DS + i % DS;
+      p.out[(static_cast<int64_t>(t) * H + h) * 512 + d] = 0;
+    }
+    if (rank == 0 && p.lse && tid < H) p.lse[static_cast<int64_t>(t) * H + tid] = -INFINITY;
+    return;
+  }
+
+  const uint32_t sQ = smem_u32(sm + C::OFF_Q);
+  const uint32_t sC = smem_u32(sm + C::OFF_C);
+  const uint32_t sP = smem_u32(sm + C::OFF_P);
+  float* m_used = reinterpret_cast<float*>(sm + C::OFF_SCR);
+  float* red = m_used + H;
+  float* lsum = red + 4 * H;
+  float* fac = lsum + H;
+  int* flags = reinterpret_cast<int*>(sm + C::OFF_FLAGS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC + 8);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const int B_Q = 0, B_CFULL = 1, B_CFREE = 10, B_S = 14, B_P = 15, B_O = 16;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(B_Q), 1);
+    for (int i = 0; i < 9; ++i) mbar_init(bar(B_CFULL + i), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(B_CFREE + i), 1);
+    mbar_init(bar(B_S), 1);
+    mbar_init(bar(B_P), NST);
+    mbar_init(bar(B_O), 1);
+    fence_mbar_init();
+  }
+  if (tid < H) m_used[tid] = -INFINITY;
+  if (warp == W_MMA) {
+    tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == W_PROD && lane == 0) {
+    tma_prefetch_desc(&qlat_map);
+    tma_prefetch_desc(&qrope_map);
+    tma_prefetch_desc(&kv_map);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint64_t to = p.timeout_ns;
+  volatile int no_abort = 0;
+
+  if (warp == W_PROD) {
+    // ------------------------------------------------ producer: Q once, gathered C per block
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
+      for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, t * H, bar(B_Q));
+      tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, t * H, bar(B_Q));
+    }
+    int uses = 0;  // completed issue rounds of every sub-tile
+    for (int j = j0; j < j1; ++j) {
+      int r[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int sl = j * 128 + 4 * lane + q;
+        int e = -1;
+        if (sl < nvalid) e = idx_row[sl];
+        const bool ok = e >= 0 && e <= pos;
+        if (sl < nvalid && !ok && e != -1) atomicOr(p.status, DSA_DEVERR_INDEX);
+        r[q] = static_cast<int>(row0 + (ok ? e : 0));
+      }
+      bool alive = true;
+#pragma unroll 1
+      for (int i = 0; i < 9; ++i) {
+        if (j > j0) {
+          const int chunk = i < 8 ? (i >> 1) : 3;
+          if (!mbar_wait(bar(B_CFREE + chunk), (j - j0 - 1) & 1, abort_flag, p.status, to)) {
+            alive = false;
+            break;
+          }
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar(B_CFULL + i), C::CSUB);
+        __syncwarp();
+        tma_gather4(sC + i * C::CSUB + lane * 512, &kv_map, 64 * i, r[0], r[1], r[2], r[3],
+                    bar(B_CFULL + i));
+      }
+      __syncwarp();
+      if (!alive) break;
+      ++uses;
+    }
+    // let every copy this CTA started land before it can exit
+    if (lane == 0) {
+      mbar_wait(bar(B_Q), 0, &no_abort, nullptr, to);
+      if (uses > 0)
+        for (int i = 0; i < 9; ++i) mbar_wait(bar(B_CFULL + i), (uses - 1) & 1, &no_abort, nullptr, to);
+    }
+    __syncwarp();
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(128, H, false, false);
+      constexpr uint32_t id_pv = idesc_bf16(128, H, true, false);
+      bool ok = mbar_wait(bar(B_Q), 0, abort_flag, p.status, to);
+      for (int j = j0; ok && j < j1; ++j) {
+        const int u = j - j0;
+        for (int i = 0; i < 9 && ok; ++i) {
+          ok = mbar_wait(bar(B_CFULL + i), u & 1, abort_flag, p.status, to);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tbase + C::TM_S, sdesc_sw128(sC + i * C::CSUB + kk * 32, 0, 1024),
+                      sdesc_sw128(sQ + i * C::QSUB + kk * 32, 0, 1024), id_qk, (i | kk) != 0);
+        }
+        if (!ok) break;
+        umma_commit(bar(B_S));
+        ok = mbar_wait(bar(B_P), u & 1, abort_flag, p.status, to);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16(tbase + C::TM_O + c * H,
+                      sdesc_sw128(sC + 2 * c * C::CSUB + kk * 2048, C::CSUB, 1024),
+                      sdesc_sw128(sP + (kk >> 2) * C::PSUB + (kk & 3) * 32, 0, 1024), id_pv,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(B_CFREE + c));
+        }
+      }
+      umma_commit(bar(B_O));
+      mbar_wait(bar(B_O), 0, &no_abort, nullptr, to);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax: key = TMEM lane, HW heads
+    const int quarter = warp & 3;              // TMEM lane quarter this warp may access
+    const int h0 = (warp >> 2) * HW;           // first head of this warp
+    const int key = quarter * 32 + lane;       // key of the block (= TMEM lane)
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = p.scale_log2;
+    float lpart[HW];
+#pragma unroll
+    for (int h = 0; h < HW; ++h) lpart[h] = 0.f;
+    uint8_t* pbase = sm + C::OFF_P + (key >> 6) * C::PSUB;
+    const int kb = (key & 63) * 2;  // byte offset of this key inside a P^T row
+    for (int j = j0; j < j1; ++j) {
+      const int u = j - j0;
+      if (!mbar_wait(bar(B_S), u & 1, abort_flag, p.status, to)) break;
+      tc_fence_after();
+      const int sl = j * 128 + key;
+      int e = -1;
+      if (sl < nvalid) e = idx_row[sl];
+      const bool valid = e >= 0 && e <= pos;
+      float z[HW];
+      tmem_cols_load<HW>(lane_base + C::TM_S + h0, z);
+      bool exceed = false;
+#pragma unroll
+      for (int h = 0; h < HW; ++h) {
+        z[h] = valid ? z[h] * sl2 : -INFINITY;
+        exceed |= z[h] > m_used[h0 + h] + kRescaleThreshold;
+      }
+      const unsigned any = __any_sync(0xffffffffu, exceed);
+      if (lane == 0) flags[warp] = any ? 1 : 0;
+      named_bar_sync(1, NST);
+      int resc = 0;
+#pragma unroll
+      for (int w = 0; w < NSW; ++w) resc |= flags[w];
+      if (resc) {
+#pragma unroll
+        for (int h = 0; h < HW; ++h) {
+          float v = z[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+          if (lane == 0) red[quarter * H + h0 + h] = v;
+        }
+        named_bar_sync(1, NST);
+        if (tid < H) {
+          const float mo = m_used[tid];
+          const float mb = fmaxf(fmaxf(red[tid], red[H + tid]), fmaxf(red[2 * H + tid], red[3 * H + tid]));
+          const float mn = fmaxf(mo, mb);
+          fac[tid] = (mn == -INFINITY) ? 1.f : ex2(mo - mn);
+          m_used[tid] = mn;
+        }
+        named_bar_sync(1, NST);
+#pragma unroll
+        for (int h = 0; h < HW; ++h) lpart[h] *= fac[h0 + h];
+        if (u > 0) {  // O^T rows of this thread: dims 128c + key
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float o[HW];
+            tmem_cols_load<HW>(lane_base + C::TM_O + c * H + h0, o);
+#pragma unroll
+            for (int h = 0; h < HW; ++h) o[h] *= fac[h0 + h];
+            tmem_cols_store<HW>(lane_base + C::TM_O + c * H + h0, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P^T[h][key] = bf16(2^(z - m)); 128-byte swizzled K-major rows of 64 keys
+#pragma unroll
+      for (int h = 0; h < HW; ++h) {
+        const int hg = h0 + h;
+        const float pv = valid ? ex2(z[h] - m_used[hg]) : 0.f;
+        lpart[h] += pv;
+        const int off = hg * 128 + ((((kb >> 4) ^ (hg & 7)) << 4) | (kb & 15));
+        *reinterpret_cast<__nv_bfloat16*>(pbase + off) = __float2bfloat16_rn(pv);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(B_P));
+    }
+    // row sums over the 128 keys
+#pragma unroll
+    for (int h = 0; h < HW; ++h) {
+      float v = lpart[h];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) red[quarter * H + h0 + h] = v;
+    }
+    named_bar_sync(1, NST);
+    if (tid < H) lsum[tid] = (red[tid] + red[H + tid]) + (red[2 * H + tid] + red[3 * H + tid]);
+    // stage the unnormalised O^T of this CTA in shared memory as [h][512]
+    const bool have = j1 > j0 && mbar_wait(bar(B_O), 0, abort_flag, p.status, to);
+    tc_fence_after();
+    float* Os = reinterpret_cast<float*>(sm + C::OFF_C);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float o[HW];
+      if (have) {
+        tmem_cols_load<HW>(lane_base + C::TM_O + c * H + h0, o);
+      } else {
+#pragma unroll
+        for (int h = 0; h < HW; ++h) o[h] = 0.f;
+      }
+#pragma unroll
+      for (int h = 0; h < HW; ++h) Os[(h0 + h) * 512 + c * 128 + key] = o[h];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == W_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+
+  // ---- combine the NSPLIT partial results and write bf16 out (+ lse)
+  float* Os = reinterpret_cast<float*>(sm + C::OFF_C);
+  if constexpr (NSPLIT > 1) {
+    cluster_sync();
+    if (tid < H) {
+      float mr[NSPLIT], lr[NSPLIT];
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < NSPLIT; ++r) {
+        mr[r] = __uint_as_float(ld_dsmem_u32(mapa_shared(smem_u32(&m_used[tid]), r)));
+        lr[r] = __uint_as_float(ld_dsmem_u32(mapa_shared(smem_u32(&lsum[tid]), r)));
+        M = fmaxf(M, mr[r]);
+      }
+      float L = 0.f;
+#pragma unroll
+      for (int r = 0; r < NSPLIT; ++r) L += (mr[r] == -INFINITY) ? 0.f : lr[r] * ex2(mr[r] - M);
+#pragma unroll
+      for (int r = 0; r < NSPLIT; ++r)
+        fac[r * H + tid] = (L > 0.f && mr[r] != -INFINITY) ? ex2(mr[r] - M) / L : 0.f;
+      if (rank == 0 && p.lse)
+        p.lse[static_cast<int64_t>(t) * H + tid] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    constexpr int DS = 512 / NSPLIT;
+    for (int i = tid; i < H * DS / 4; i += NT) {
+      const int h = i / (DS / 4);
+      const int d = rank * DS + (i % (DS / 4)) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < NSPLIT; ++r) {
+        const float f = fac[r * H + h];
+        const float4 v = ld_dsmem_f4(mapa_shared(smem_u32(&Os[h * 512 + d]), r));
+        acc.x = fmaf(f, v.x, acc.x);
+        acc.y = fmaf(f, v.y, acc.y);
+        acc.z = fmaf(f, v.z, acc.z);
+        acc.w = fmaf(f, v.w, acc.w);
+      }
+      __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * H + h) * 512 + d) = pk;
+    }
+    cluster_sync();  // keep this CTA's shared memory alive until every rank has read it
+  } else {
+    if (tid < H) {
+      const float L = lsum[tid];
+      fac[tid] = L > 0.f ? 1.f / L : 0.f;
+      if (p.lse)
+        p.lse[static_cast<int64_t>(t) * H + tid] =
+            L > 0.f ? (m_used[tid] + log2f(L)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    for (int i = tid; i < H * 128; i += NT) {
+      const int h = i >> 7, d = (i & 127) * 4;
+      const float f = fac[h];
+      const float4 v = *reinterpret_cast<const float4*>(&Os[h * 512 + d]);
+      __nv_bfloat162 lo2 = __floats2bfloat162_rn(v.x * f, v.y * f);
+      __nv_bfloat162 hi2 = __floats2bfloat162_rn(v.z * f, v.w * f);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * H + h) * 512 + d) = pk;
+    }
+  }
+}
+
+template <int H, int NSPLIT>
+cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const CUtensorMap& kvm,
+                       const MlaParams& p, cudaStream_t stream) {
+  using C = MlaCfg<H>;
+  auto* kern = sparse_mla_kernel<H, NSPLIT>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.b.max_q) * NSPLIT, static_cast<unsigned>(p.b.num_seqs));
+  cfg.blockDim = dim3(C::NT);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = NSPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ql, qr, kvm, p);
+  count_launch(kLaunchMla);
+  return e;
+}
+
+template <int H>
+cudaError_t launch_h(const CUtensorMap& ql, const CUtensorMap& qr, const CUtensorMap& kvm,
+                     const MlaParams& p, int nsplit, cudaStream_t stream) {
+  switch (nsplit) {
+    case 1: return launch_mla<H, 1>(ql, qr, kvm, p, stream);
+    case 2: return launch_mla<H, 2>(ql, qr, kvm, p, stream);
+    case 4: return launch_mla<H, 4>(ql, qr, kvm, p, stream);
+    default: return launch_mla<H, 8>(ql, qr, kvm, p, stream);
+  }
+}
+
+}  // namespace
+
+size_t mla_workspace_bytes(const dsa_batch_t&, int, int) { return 0; }
+
+cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void* kv,
+                              int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
+                              const dsa_batch_t& b, void* out, float* lse, void*, size_t,
+                              int* status, cudaStream_t stream) {
+  if (b.num_q == 0) return cudaSuccess;
+  CUtensorMap ql, qr, kvm;
+  const uint64_t qrows = static_cast<uint64_t>(b.num_q) * heads;
+  if (!make_tmap_2d(&ql, q_lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 512, qrows, 64, heads) ||
+      !make_tmap_2d(&qr, q_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, qrows, 64, heads) ||
+      !make_tmap_2d(&kvm, kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 576, static_cast<uint64_t>(kv_rows), 64, 1))
+    return cudaErrorInvalidValue;
+  MlaParams p{};
+  p.b = to_args(b);
+  p.idx = idx;
+  p.K = k;
+  p.scale_log2 = scale * kLog2e;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.status = status;
+  p.timeout_ns = wait_timeout_ns();
+  // Split each token's blocks over a cluster when there are too few tokens
+  // to cover the SMs (decode).
+  const int nblk = (k + 127) / 128;
+  int nsplit = 1;
+  while (nsplit < 8 && nsplit * 2 <= nblk && static_cast<int64_t>(b.num_q) * nsplit * 2 <= 152)
+    nsplit *= 2;
+  return heads == 16 ? launch_h<16>(ql, qr, kvm, p, nsplit, stream)
+                     : launch_h<64>(ql, qr, kvm, p, nsplit, stream);
+}
+
+}  // namespace dsa

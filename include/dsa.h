@@ -1,0 +1,260 @@
+/*
+ * dsa.h - C ABI of the GB300 (sm_103a) DSA attention layer group with
+ * IndexShare.
+ *
+ * The method (GLM-5.2 pages):
+ *  - "GLM-5.2 / 总览", config table (@tbl-glm52-config): 64 MLA heads, QK head
+ *    dim 256 (NoPE 192 + RoPE 64), per-token per-layer KV = 512-d latent plus
+ *    64-d RoPE key (1152 B in bf16); IndexShare indexer 32 heads x 128 dims,
+ *    top-K = 2048, shared every 4 layers.  Sub-doc index row 02: indexer with
+ *    ReLU and an "FP8 per-block + Hadamard" variant.
+ *  - "GLM-5.2 架构深度拆解" CH 2.2: an F (full) layer scores every earlier token
+ *    and keeps the top 2048 as the sparse set of its attention; an S (shared)
+ *    layer skips the indexer and reuses the nearest F layer's indices; CH 2.4:
+ *    the indices are written at F and read at S through an outer buffer.
+ *  - "GLM-5 -> 5.1 -> 5.2" section 10: indexer once per layer group, shared
+ *    indices written to a buffer reused within the group, each layer gathers
+ *    the selected entries from its own K/V cache, then sparse attention.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named d_* and every tensor argument are DEVICE pointers owned by
+ *    the caller; the library allocates and frees nothing.  Host structs
+ *    (dsa_batch_t, dsa_group_t) are read during the call only.
+ *  - Calls are asynchronous on `stream`: they validate their host-side
+ *    arguments, enqueue kernels and return.  Argument errors are reported
+ *    synchronously before anything is enqueued.  Errors only a kernel can see
+ *    (an index outside [-1, q_pos], inconsistent batch arrays, a bounded wait
+ *    that ran out) are OR-ed into the status word at the head of the
+ *    workspace; dsa_status_fetch() reads and clears it.
+ *  - Nothing falls back: an unsupported shape or dtype returns
+ *    DSA_ERR_UNSUPPORTED.  No exception crosses the ABI.
+ *  - bf16 tensors are IEEE bfloat16 bit patterns; fp8 tensors are OCP E4M3
+ *    codes.  All layouts are row-major and densely packed.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad layer string */
+  DSA_ERR_UNSUPPORTED = 2, /* a shape / dtype outside what the kernels implement */
+  DSA_ERR_WORKSPACE = 3,   /* workspace null or smaller than the matching *_workspace_size */
+  DSA_ERR_CUDA = 4,        /* a CUDA runtime call failed (see dsa_last_error_string) */
+  DSA_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel ran out */
+  DSA_ERR_DEVICE_INDEX = 6 /* device: an index outside [-1, q_pos], or bad batch arrays */
+} dsa_status_t;
+
+typedef enum { DSA_BF16 = 0, DSA_FP8_E4M3 = 1 } dsa_dtype_t;
+
+/* Fixed widths of the method (config table of "GLM-5.2 / 总览"). */
+enum {
+  DSA_INDEX_HEADS = 32, /* indexer heads */
+  DSA_INDEX_DIM = 128,  /* indexer width; one shared 128-d key per position */
+  DSA_LATENT = 512,     /* MLA KV latent */
+  DSA_ROPE = 64,        /* MLA RoPE key */
+  DSA_KV_ROW = 576      /* latent + RoPE key, one cache row */
+};
+
+/*
+ * Batch layout shared by every call.  Queries are rows 0..num_q-1; the rows
+ * of sequence b are [q_start[b], q_start[b+1]).  Query t sits at absolute
+ * position q_pos[t] of its sequence and sees positions 0..q_pos[t] (causal,
+ * itself included).  Every per-layer cache (indexer keys, KV latent) stores
+ * position s of sequence b at row seq_row0[b] + s.
+ *   num_seqs  >= 1
+ *   num_q     >= 0 (0 is a no-op)
+ *   max_q     >= the largest query count of one sequence
+ *   max_len   capacity of a score row: a multiple of 128 and > every q_pos
+ *   q_start   device int32 [num_seqs + 1], non-decreasing, q_start[0] = 0,
+ *             q_start[num_seqs] = num_q
+ *   q_pos     device int32 [num_q]
+ *   seq_row0  device int64 [num_seqs]
+ * A kernel that finds q_start / q_pos inconsistent with these sizes skips the
+ * affected rows and raises DSA_ERR_DEVICE_INDEX in the status word.
+ */
+typedef struct {
+  int32_t num_seqs;
+  int32_t num_q;
+  int32_t max_q;
+  int32_t max_len;
+  const int32_t* q_start;
+  const int32_t* q_pos;
+  const int64_t* seq_row0;
+} dsa_batch_t;
+
+/* ------------------------------------------------------------------ status */
+
+/* Text of the last host-side error of the calling thread ("" if none). */
+DSA_API const char* dsa_last_error_string(void);
+
+/* Bytes of the status block at the head of every workspace (256). */
+DSA_API size_t dsa_status_bytes(void);
+
+/* Zero the status block of `d_ws` on `stream` (once before first use). */
+DSA_API dsa_status_t dsa_workspace_init(void* d_ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* Synchronise `stream`, return the device status accumulated in `d_ws` as a
+ * dsa_status_t (DSA_OK if clean; otherwise the most severe recorded error,
+ * DSA_ERR_TIMEOUT before DSA_ERR_DEVICE_INDEX) and clear it.  *raw_bits, if
+ * non-null, receives the raw error bits. */
+DSA_API dsa_status_t dsa_status_fetch(void* d_ws, dsa_stream_t stream, int32_t* raw_bits);
+
+/* Per-kernel launch counters kept by the host side of the library (for
+ * tests and benchmarks): counts[0] indexer, [1] top-K, [2] sparse MLA,
+ * [3] split combine, [4] FP8 quantiser, [5] other.  `n` is the length of
+ * `counts`; returns how many counters exist. */
+DSA_API int dsa_launch_counts(uint64_t* counts, int n);
+DSA_API void dsa_launch_counts_reset(void);
+
+/* Upper bound in nanoseconds on every spin-wait inside the kernels launched
+ * after this call (default 2e9).  Exposed so that tests can shorten it. */
+DSA_API void dsa_set_wait_timeout_ns(uint64_t ns);
+
+/* Test aid for the failure path: launch one CTA that waits on an mbarrier
+ * nothing ever arrives on, bounded by the current wait limit, records
+ * DSA_ERR_TIMEOUT in the status block of `d_ws` and exits cleanly. */
+DSA_API dsa_status_t dsa_selftest_wait_timeout(void* d_ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------ step a1 */
+
+/*
+ * Lightning-indexer scores (the candidate-scoring step of an F layer):
+ *   scores[t, s] = sum_{j<32} w[t,j] * ReLU(q_idx[t,j,:] . k_idx[row(s),:])
+ * for 0 <= s <= q_pos[t], and -inf for q_pos[t] < s < max_len.
+ *   dt = DSA_BF16:     q_idx bf16 [num_q, 32, 128], k_idx bf16 [k_rows, 128];
+ *                      q_scale and k_scale are ignored (may be NULL).
+ *   dt = DSA_FP8_E4M3: q_idx E4M3 [num_q, 32, 128] with q_scale fp32
+ *                      [num_q, 32]; k_idx E4M3 [k_rows, 128] with k_scale
+ *                      fp32 [k_rows]; an element's value is code * scale, and
+ *                      scales must be > 0 (as dsa_fp8_quantize writes them).
+ *   w       fp32 [num_q, 32]
+ *   scores  fp32 [num_q, max_len] (written in full)
+ * Pointers to q_idx / k_idx must be 16-byte aligned.  The reduction over
+ * heads and the products are fp32 (tensor-core accumulation of the dots).
+ * ws: status block only (dsa_indexer_workspace_size).
+ */
+DSA_API size_t dsa_indexer_workspace_size(const dsa_batch_t* b);
+DSA_API dsa_status_t dsa_indexer_scores(const void* q_idx, const float* q_scale, const float* w,
+                                const void* k_idx, const float* k_scale, int64_t k_rows,
+                                dsa_dtype_t dt, const dsa_batch_t* b, float* scores, void* ws,
+                                size_t ws_bytes, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------ step a2 */
+
+/*
+ * Top-K selection ("keep the top 2048 as the sparse set", CH 2.2 of
+ * "GLM-5.2 架构深度拆解"): for each query t, the k positions s in
+ * [0, q_pos[t]] with the largest scores[t, s]; equal scores go to the lower
+ * position.  idx[t, :] receives them in ascending position order; if
+ * q_pos[t] + 1 < k every visible position is taken and the remaining slots
+ * are -1.  scores is fp32 [num_q, max_len] (only s <= q_pos[t] is read), idx
+ * int32 [num_q, k].  1 <= k <= 4096.  The comparison uses the fp32 bit
+ * order (NaN ranks above +inf).  ws: dsa_topk_workspace_size.
+ */
+DSA_API size_t dsa_topk_workspace_size(const dsa_batch_t* b, int32_t k);
+DSA_API dsa_status_t dsa_topk(const float* scores, const dsa_batch_t* b, int32_t k, int32_t* idx,
+                      void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------ steps a4-a5 */
+
+/*
+ * Absorbed-MLA sparse attention over the selected positions of one layer
+ * (gather from this layer's own cache, then attention):
+ *   z_s = scale * (q_lat[t,h,:] . kv[row(s), :512] + q_rope[t,h,:] . kv[row(s), 512:])
+ *   out[t,h,:] = sum_s softmax(z)_s kv[row(s), :512],  lse[t,h] = ln sum_s exp(z_s)
+ * over s in idx[t, :] (k entries; -1 = empty slot).  Valid entries must be
+ * distinct positions in [0, q_pos[t]] and occupy the first slots of the row
+ * (dsa_topk output does); slots from index min(k, q_pos[t]+1) on are not
+ * read.  An entry outside [-1, q_pos[t]] is skipped and raises
+ * DSA_ERR_DEVICE_INDEX.  A row with no valid entry gives out = 0,
+ * lse = -inf.
+ *   q_lat  bf16 [num_q, heads, 512], q_rope bf16 [num_q, heads, 64]
+ *   kv     bf16 [kv_rows, 576] (latent then RoPE key), 16-byte aligned
+ *   out    bf16 [num_q, heads, 512]; lse fp32 [num_q, heads] or NULL
+ *   heads in {16, 64}; 1 <= k <= 4096 (slots are processed in blocks of 128,
+ *   the last one masked).  Softmax statistics are fp32; P is
+ *   rounded to bf16 for the P.V product (fp32 accumulation).
+ * ws: dsa_sparse_mla_workspace_size.
+ */
+DSA_API size_t dsa_sparse_mla_workspace_size(const dsa_batch_t* b, int32_t heads, int32_t k);
+DSA_API dsa_status_t dsa_sparse_mla_attn(const void* q_lat, const void* q_rope, const void* kv,
+                                 int64_t kv_rows, const int32_t* idx, int32_t k, int32_t heads,
+                                 float scale, const dsa_batch_t* b, void* out, float* lse,
+                                 void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------ step a6 */
+
+/*
+ * One layer group with IndexShare.  layer_types is a string over {F, S}
+ * ("FSSS", "FSSSFSSS", or "FFFF" for the every-layer-indexer ablation) whose
+ * first letter is F.  Per layer l (arrays of num_layers host-side pointers to
+ * device tensors):
+ *   F layer: dsa_indexer_scores(q_idx[l], w[l], k_idx[l]) -> dsa_topk -> idx_buf
+ *   every layer: dsa_sparse_mla_attn(q_lat[l], q_rope[l], kv[l], idx_buf) -> out[l]
+ * so the indexer runs exactly once per F layer and every S layer reads the
+ * index buffer its F layer wrote.  q_idx/w/k_idx/q_scale/k_scale entries of S
+ * layers are ignored (may be NULL).  lse[l] may be NULL.
+ * idx_buf: int32 [num_q, k], caller-owned; after the call it holds the
+ * indices of the last F layer.  The workspace holds the status block and the
+ * fp32 score matrix; size from dsa_group_workspace_size.
+ */
+typedef struct {
+  const char* layer_types;
+  int32_t heads;
+  int32_t k;
+  float scale;
+  dsa_dtype_t idx_dtype;
+  int64_t kv_rows;  /* rows of every kv[l] */
+  int64_t k_rows;   /* rows of every k_idx[l] */
+  const void* const* q_lat;
+  const void* const* q_rope;
+  const void* const* kv;
+  void* const* out;
+  float* const* lse;
+  const void* const* q_idx;
+  const float* const* q_scale;
+  const float* const* w;
+  const void* const* k_idx;
+  const float* const* k_scale;
+} dsa_group_t;
+
+DSA_API size_t dsa_group_workspace_size(const dsa_group_t* g, const dsa_batch_t* b);
+DSA_API dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b,
+                                      int32_t* idx_buf, void* ws, size_t ws_bytes,
+                                      dsa_stream_t stream);
+
+/* ------------------------------------------------------------------ step a7 */
+
+/*
+ * FP8 per-block quantiser of the indexer ("FP8 per-block + Hadamard",
+ * sub-doc index row 02 of "GLM-5.2 / 总览"): each 128-element row of x (bf16
+ * [rows, 128]) is rotated by the normalised 128-point Hadamard matrix
+ * (Sylvester order, 1/sqrt(128)), its scale is amax/448 (1 for an all-zero
+ * row) and each element becomes the E4M3 code of x/scale (round to nearest
+ * even, saturating).  codes uint8 [rows, 128], scale fp32 [rows].  The same
+ * call quantises indexer keys (rows = cache rows) and queries
+ * (rows = num_q * 32).  Every step is one IEEE fp32 operation in a fixed
+ * order, so results are reproducible bit for bit.
+ */
+DSA_API dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
+                              dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H_ */

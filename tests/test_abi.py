@@ -1,0 +1,96 @@
+"""The C-ABI library loads without a GPU, exports every entry point that
+include/dsa.h declares, and rejects bad host-side arguments before touching
+the device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"DSA_API\s+[\w\s\*]+?\b((?:dsa|indexshare)_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import dsa_indexer_indexshare_gb300 as m
+    return m
+
+
+def test_header_declares_the_hot_path_calls():
+    fns = declared_functions()
+    for name in ("dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_attn",
+                 "indexshare_group_forward", "dsa_fp8_quantize"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(dsa):
+    lib = ctypes.CDLL(dsa.LIB_PATH)
+    missing = [f for f in declared_functions() if not hasattr(lib, f)]
+    assert not missing, missing
+
+
+def _batch(dsa, num_q=4, max_q=4, max_len=256, ptr=256):
+    return dsa._Batch(1, num_q, max_q, max_len, ctypes.c_void_p(ptr), ctypes.c_void_p(ptr),
+                      ctypes.c_void_p(ptr))
+
+
+def test_argument_errors_without_a_device(dsa):
+    L = dsa.lib
+    fake = ctypes.c_void_p(4096)
+    b = _batch(dsa)
+    # max_len not a multiple of 128
+    bad = _batch(dsa, max_len=200)
+    assert L.dsa_topk(fake, ctypes.byref(bad), 16, fake, fake, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    assert b"multiple of 128" in L.dsa_last_error_string()
+    # k out of range
+    assert L.dsa_topk(fake, ctypes.byref(b), 0, fake, fake, 256, None) == dsa.DSA_ERR_UNSUPPORTED
+    # workspace too small / misaligned
+    assert L.dsa_topk(fake, ctypes.byref(b), 16, fake, fake, 8, None) == dsa.DSA_ERR_WORKSPACE
+    assert L.dsa_topk(fake, ctypes.byref(b), 16, fake, ctypes.c_void_p(4097), 256,
+                      None) == dsa.DSA_ERR_WORKSPACE
+    # unsupported head count
+    assert L.dsa_sparse_mla_attn(fake, fake, fake, 100, fake, 64, 32, 0.0625, ctypes.byref(b), fake,
+                                 None, fake, 256, None) == dsa.DSA_ERR_UNSUPPORTED
+    # misaligned operand
+    assert L.dsa_sparse_mla_attn(ctypes.c_void_p(4098), fake, fake, 100, fake, 64, 64, 0.0625,
+                                 ctypes.byref(b), fake, None, fake, 256,
+                                 None) == dsa.DSA_ERR_INVALID_ARG
+    # FP8 indexer without scales
+    assert L.dsa_indexer_scores(fake, None, fake, fake, None, 100, dsa.DSA_FP8_E4M3, ctypes.byref(b),
+                                fake, fake, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    # NULL batch
+    assert L.dsa_indexer_scores(fake, None, fake, fake, None, 100, 0, None, fake, fake, 256,
+                                None) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_group_layer_string_is_validated(dsa):
+    L = dsa.lib
+    b = _batch(dsa)
+    arr = (ctypes.c_void_p * 4)(*[4096] * 4)
+    pp = ctypes.cast(arr, dsa._PP)
+    for types, ok in ((b"SFSS", False), (b"FXSS", False), (b"", False)):
+        g = dsa._Group(types, 64, 2048, 0.0625, 0, 100, 100, pp, pp, pp, pp, None, pp, None, pp, pp,
+                       None)
+        st = L.indexshare_group_forward(ctypes.byref(g), ctypes.byref(b), ctypes.c_void_p(4096),
+                                        ctypes.c_void_p(4096), 1 << 30, None)
+        assert st == dsa.DSA_ERR_INVALID_ARG
+    # a valid string with a workspace below the required size
+    g = dsa._Group(b"FSSS", 64, 2048, 0.0625, 0, 100, 100, pp, pp, pp, pp, None, pp, None, pp, pp,
+                   None)
+    need = L.dsa_group_workspace_size(ctypes.byref(g), ctypes.byref(b))
+    assert need >= 256 + 4 * 256 * 4
+    st = L.indexshare_group_forward(ctypes.byref(g), ctypes.byref(b), ctypes.c_void_p(4096),
+                                    ctypes.c_void_p(4096), need - 256, None)
+    assert st == dsa.DSA_ERR_WORKSPACE
+
+
+def test_launch_counters_and_timeout_setter(dsa):
+    dsa.launch_counts_reset()
+    assert set(dsa.launch_counts().values()) == {0}
+    dsa.set_wait_timeout_ns(2_000_000_000)

@@ -1,0 +1,246 @@
+"""GPU parity of each hot-path step against the oracle, through the C ABI.
+
+Bars (the benchmark spec): integer-valued inputs give bit-exact scores and index
+sets; Gaussian inputs give index sets that differ only within 1e-3 of the
+K-th score; attention outputs within 2e-2 * max|ref| (bf16)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from gpu_helpers import (assert_close, assert_topk_within_band, bf16_dev, bits,  # noqa: E402
+                         device_layers, make_batch)
+
+dsa = pytest.importorskip("dsa_indexer_indexshare_gb300")
+DEV = torch.device("cuda:0")
+
+
+def rows_meta(lay, rows):
+    return oracle.row_metadata(lay.q_start, lay.q_pos, lay.seq_row0, rows)
+
+
+LAYOUTS = {
+    "prefill512": ([512], [512]),
+    "ragged3": ([300, 77, 1000], [300, 5, 129]),
+    "decode5": ([1, 129, 1000, 4097, 256], [1, 1, 1, 1, 1]),
+    "empty_middle": ([200, 50, 333], [17, 0, 40]),
+}
+
+
+@pytest.mark.parametrize("name", list(LAYOUTS))
+def test_indexer_scores_bit_exact_on_integers(name):
+    lay = synth.make_layout(*LAYOUTS[name])
+    host = synth.host_layers(lay, "F", 16, ints=True, seed=3)[0]
+    d = device_layers([host], DEV)[0]
+    batch = make_batch(dsa, lay, DEV)
+    ws = dsa.workspace(256, DEV)
+    sc = dsa.dsa_indexer_scores(d["q_idx"], d["w"], d["k_idx"], batch, ws=ws)
+    dsa.status_fetch(ws)
+    rows = np.arange(lay.num_q, dtype=np.int32)
+    pos, key0 = rows_meta(lay, rows)
+    ref = oracle.indexer_scores(host["q_idx"], host["w"], host["k_idx"], rows, pos, key0, lay.max_len)
+    got = sc.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, ref)
+
+
+def test_indexer_scores_gaussian_fp32_accuracy():
+    lay = synth.make_layout([1000], [1000])
+    host = synth.host_layers(lay, "F", 16, ints=False, seed=4)[0]
+    d = device_layers([host], DEV)[0]
+    batch = make_batch(dsa, lay, DEV)
+    sc = dsa.dsa_indexer_scores(d["q_idx"], d["w"], d["k_idx"], batch).cpu().numpy()
+    rows = np.arange(lay.num_q, dtype=np.int32)
+    pos, key0 = rows_meta(lay, rows)
+    ref = oracle.indexer_scores(host["q_idx"], host["w"], host["k_idx"], rows, pos, key0, lay.max_len)
+    fin = np.isfinite(ref)
+    assert np.array_equal(fin, np.isfinite(sc))
+    # fp32 tensor-core accumulation of exact bf16 products + fp32 head reduction
+    assert np.abs(sc[fin] - ref[fin]).max() <= 1e-5 * np.abs(ref[fin]).max()
+
+
+def _topk_case(lens, qcounts, K, values, seed):
+    lay = synth.make_layout(lens, qcounts)
+    rng = np.random.default_rng(seed)
+    if values == "ties":
+        sc = rng.integers(-3, 4, (lay.num_q, lay.max_len)).astype(np.float32)
+    elif values == "gauss":
+        sc = rng.standard_normal((lay.num_q, lay.max_len)).astype(np.float32)
+    else:  # constant rows
+        sc = np.zeros((lay.num_q, lay.max_len), np.float32)
+    sc[0, : min(5, sc.shape[1])] = -np.inf
+    batch = make_batch(dsa, lay, DEV)
+    ws = dsa.workspace(256, DEV)
+    got = dsa.dsa_topk(torch.from_numpy(sc).to(DEV), batch, K, ws=ws).cpu().numpy()
+    dsa.status_fetch(ws)
+    lens_q = lay.q_pos.astype(np.int64) + 1
+    ref = oracle.topk(sc.astype(np.float64), lens_q.astype(np.int32), K)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("values", ["ties", "gauss", "const"])
+def test_topk_bit_exact_short_rows(values):
+    _topk_case([3000], [3000], 64, values, 1)          # one CTA per row, 256 threads
+    _topk_case([5000, 20000], [40, 60], 2048, values, 2)  # 1024-thread rows, pos+1 <= K rows
+
+
+@pytest.mark.parametrize("values", ["ties", "gauss", "const"])
+def test_topk_bit_exact_long_rows_cluster(values):
+    _topk_case([40000, 70001, 131072], [1, 1, 1], 2048, values, 3)  # cluster of 8 per row
+
+
+def _mla_case(lens, qcounts, H, K, ints, seed, sample=None, bad_index=False, holes=False):
+    lay = synth.make_layout(lens, qcounts)
+    host = synth.host_layers(lay, "S", H, ints=ints, seed=seed)[0]
+    rng = np.random.default_rng(seed)
+    # indices: a random distinct subset of visible positions, ascending, -1 padded
+    idx = np.full((lay.num_q, K), -1, np.int32)
+    for t in range(lay.num_q):
+        n = int(lay.q_pos[t]) + 1
+        take = min(n, K)
+        sel = np.sort(rng.choice(n, take, replace=False))
+        if holes and take > 10:
+            sel = sel[: take // 2]
+        idx[t, : len(sel)] = sel
+    if bad_index:
+        idx[0, 0] = int(lay.q_pos[0]) + 5       # beyond the causal range
+    d = device_layers([host], DEV)[0]
+    batch = make_batch(dsa, lay, DEV)
+    ws = dsa.workspace(dsa.lib.dsa_sparse_mla_workspace_size(batch.c, H, K), DEV)
+    out, lse = dsa.dsa_sparse_mla_attn(d["q_lat"], d["q_rope"], d["kv"], torch.from_numpy(idx).to(DEV),
+                                       batch, scale=1 / 16, ws=ws)
+    if bad_index:
+        with pytest.raises(dsa.DsaError) as e:
+            dsa.status_fetch(ws)
+        assert e.value.status == dsa.DSA_ERR_DEVICE_INDEX
+        idx[0, 0] = -1
+    else:
+        dsa.status_fetch(ws)
+    rows = np.arange(lay.num_q, dtype=np.int32) if sample is None else np.asarray(sample, np.int32)
+    pos, key0 = rows_meta(lay, rows)
+    ref_o, ref_l = oracle.sparse_mla(host["q_lat"][rows], host["q_rope"][rows], host["kv"],
+                                     np.arange(len(rows), dtype=np.int32), key0, idx[rows], 1 / 16)
+    got = out.float().cpu().numpy()[rows]
+    assert_close(got, ref_o, 2e-2, "out")
+    gl = lse.cpu().numpy()[rows]
+    assert np.allclose(gl, ref_l, rtol=0, atol=1e-3 * max(1.0, np.abs(ref_l).max()))
+
+
+def test_mla_h16_k64_integers():
+    _mla_case([300], [300], 16, 64, True, 5)
+
+
+def test_mla_h64_k2048_gaussian_prefill():
+    sample = [0, 1, 126, 127, 128, 2046, 2047, 2048, 2049, 2599]
+    _mla_case([2600], [2600], 64, 2048, False, 6, sample=sample)
+
+
+def test_mla_h64_decode_split_clusters():
+    _mla_case([100000, 3000, 2047, 4100], [1, 1, 1, 1], 64, 2048, False, 7)
+
+
+def test_mla_holes_and_bad_index():
+    _mla_case([700, 300], [20, 30], 64, 256, False, 8, holes=True, bad_index=True)
+
+
+def test_mla_h16_ragged_batch():
+    _mla_case([300, 77, 1000], [300, 5, 129], 16, 128, False, 9)
+
+
+@pytest.mark.parametrize("types", ["FSSS", "FFFF", "FSSSFSSS"])
+def test_group_tiny_bit_exact_indices(types):
+    lay = synth.workload_layout("tiny")
+    H, K = 16, 64
+    host = synth.host_layers(lay, types, H, ints=True, seed=11)
+    layers = device_layers(host, DEV)
+    batch = make_batch(dsa, lay, DEV)
+    group = dsa.Group(types, layers, k=K, scale=1 / 16, with_lse=True)
+    ws = dsa.workspace(group.workspace_size(batch), DEV)
+    dsa.launch_counts_reset()
+    outs, lses, idx = dsa.indexshare_group_forward(group, batch, ws=ws)
+    torch.cuda.synchronize()
+    counts = dsa.launch_counts()
+    dsa.status_fetch(ws)
+    nf = types.count("F")
+    assert counts["indexer"] == nf and counts["topk"] == nf and counts["sparse_mla"] == len(types)
+    rows = np.arange(lay.num_q, dtype=np.int32)
+    pos, key0 = rows_meta(lay, rows)
+    ref = oracle.group_forward(types, host, rows, pos, key0, lay.max_len, K, 1 / 16)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"][-1])
+    for l in range(len(types)):
+        assert_close(outs[l].float().cpu().numpy(), ref["out"][l], 2e-2, f"layer {l}")
+    # an S layer is the standalone sparse MLA over the same buffer, bit for bit
+    # (indices of the last F layer are in idx_buf after the call)
+    last_f = types.rfind("F")
+    for l in range(last_f, len(types)):
+        o, _ = dsa.dsa_sparse_mla_attn(layers[l]["q_lat"], layers[l]["q_rope"], layers[l]["kv"], idx,
+                                       batch, scale=1 / 16)
+        assert torch.equal(o, outs[l])
+
+
+def test_fp8_quantiser_bit_exact():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((4099, 128)).astype(np.float32) / np.sqrt(128)
+    x[7] = 0
+    x[8] *= 1e4
+    x[9, :3] = [1e-30, -3e38, 2.5]
+    xb = synth.f32_to_bf16_bits(x)
+    codes, scale = dsa.dsa_fp8_quantize(bf16_dev(xb, DEV))
+    rc, rs = oracle.fp8_quantize_rows(xb)
+    assert np.array_equal(scale.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_fp8_indexer_scores_and_topk():
+    lay = synth.make_layout([1500, 2300], [1, 1])
+    host = synth.host_layers(lay, "F", 16, ints=False, seed=13)[0]
+    qc, qs = oracle.fp8_quantize_rows(host["q_idx"].reshape(-1, 128))
+    kc, ks = oracle.fp8_quantize_rows(host["k_idx"])
+    qc = qc.reshape(lay.num_q, 32, 128)
+    qs = qs.reshape(lay.num_q, 32)
+    batch = make_batch(dsa, lay, DEV)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    sc = dsa.dsa_indexer_scores(T(qc), T(host["w"]), T(kc), batch, q_scale=T(qs), k_scale=T(ks))
+    rows = np.arange(lay.num_q, dtype=np.int32)
+    pos, key0 = rows_meta(lay, rows)
+    ref = oracle.indexer_scores(qc, host["w"], kc, rows, pos, key0, lay.max_len, dtype=1,
+                                q_scale=qs, k_scale=ks)
+    got = sc.cpu().numpy()
+    fin = np.isfinite(ref)
+    assert np.array_equal(fin, np.isfinite(got))
+    assert np.abs(got[fin] - ref[fin]).max() <= 1e-5 * np.abs(ref[fin]).max()
+    idx = dsa.dsa_topk(sc, batch, 512).cpu().numpy()
+    assert_topk_within_band(idx, ref, pos + 1, 512, what="fp8")
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    ws = dsa.workspace(256, DEV)
+    dsa.set_wait_timeout_ns(1_000_000)  # 1 ms
+    try:
+        dsa.dsa_selftest_wait_timeout(ws)
+        with pytest.raises(dsa.DsaError) as e:
+            dsa.status_fetch(ws)
+        assert e.value.status == dsa.DSA_ERR_TIMEOUT
+    finally:
+        dsa.set_wait_timeout_ns(2_000_000_000)
+    # the context is still usable
+    test_indexer_scores_bit_exact_on_integers("decode5")
+
+
+def test_host_argument_errors():
+    lay = synth.make_layout([300], [3])
+    batch = make_batch(dsa, lay, DEV)
+    z = torch.zeros((lay.num_q, 32, 128), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_topk(torch.zeros((3, lay.max_len), device=DEV), batch, 5000)
+    assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
+    ql = torch.zeros((3, 32, 512), dtype=torch.bfloat16, device=DEV)
+    qr = torch.zeros((3, 32, 64), dtype=torch.bfloat16, device=DEV)
+    kv = torch.zeros((300, 576), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_sparse_mla_attn(ql, qr, kv, torch.zeros((3, 64), dtype=torch.int32, device=DEV),
+                                batch, scale=1 / 16)
+    assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
+    del z
