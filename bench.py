@@ -1,0 +1,532 @@
+#!/usr/bin/env python
+"""Benchmark: query-tokens/s of one DSA layer group with IndexShare on GB300.
+
+A step is one indexshare_group_forward call (every hot-path step: indexer
+scoring and top-K on F layers, gather + sparse MLA on every layer) over one
+batch of seeded synthetic inputs already resident in HBM.  Default workload:
+the 8192-token causal prefill, layers F,S,S,S, H=64, K=2048.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   (the CPU oracle, timed on a sample)
+
+Rank 0 prints one JSON line.  Under torchrun (N > 1) every rank runs its own
+replica of the workload (no data-path collective); value = all ranks' query
+tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "query-tokens/s per 4-layer F+3S DSA group (prefill & decode); % TC/HBM roofline"
+UNIT = "query-tokens/s"
+DESCR = {
+    "tiny": "tiny prefill: 1 sequence, T=512 causal, layers FSSS, H=16, K=64, integer-valued bf16",
+    "prefill8k": "prefill 8K: 1 sequence, T=8192 causal, layers FSSS, H=64, latent 512 + rope 64, "
+                 "indexer 32x128, K=2048, bf16 N(0,1)/sqrt(d)",
+    "decode64": "decode: 64 sequences x 1 query, context U[98304,131072], layers FSSS, H=64, K=2048, bf16",
+    "chunked": "chunked prefill: 4096 queries after a 131072-token prefix, layers FSSSFSSS, H=64, "
+               "K=2048, bf16",
+    "decode1m": "1M decode: 4 sequences x 1 query, context 1048576, layers FSSS, H=64, K=2048, "
+                "FP8 E4M3 + Hadamard indexer keys/queries, bf16 KV latent",
+}
+# ncu DRAM traffic of the dominant kernel (bytes per launch), with the hash of
+# the kernel sources it was measured on; ignored once the sources change.
+NCU_TRAFFIC = {}
+
+
+def kernel_src_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "dsa_indexer_indexshare_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KSRC = {"sparse_mla": ["sparse_mla.cu", "ptx.cuh", "common.cuh"],
+        "indexer": ["indexer.cu", "ptx.cuh", "common.cuh"],
+        "topk": ["topk.cu", "ptx.cuh", "common.cuh"]}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm": d["hbm_gbs"], "bf16": d["bf16_tflops"],
+                "bf16_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
+
+
+# ---------------------------------------------------------------- algorithmic work
+def algorithmic(lay, cfg, fp8):
+    """Per-launch algorithmic FLOPs / bytes of each kernel for this layout."""
+    pos = lay.q_pos.astype(np.int64)
+    vis = pos + 1
+    H, K = cfg["H"], cfg["K"]
+    nvalid = np.minimum(vis, K)
+    # keys scanned by the indexer: every visible position of each query
+    # (decode: one query per sequence, so each key row is read once)
+    idx_flops = 2.0 * 32 * 128 * vis.sum()
+    kbytes_per_pos = 128 * (1 if fp8 else 2) + (4 if fp8 else 0)
+    seq_len = np.array([lay.q_pos[lay.q_start[b + 1] - 1] + 1 if lay.q_start[b + 1] > lay.q_start[b]
+                        else 0 for b in range(lay.num_seqs)], np.int64)
+    idx_bytes = (seq_len.sum() * kbytes_per_pos + lay.num_q * 32 * (128 * (1 if fp8 else 2) + 4)
+                 + vis.sum() * 4)
+    topk_bytes = vis.sum() * 4 + lay.num_q * K * 4
+    mla_flops = 2.0 * H * (576 + 512) * nvalid.sum()
+    # distinct cache rows a launch must read: per sequence, at most its length
+    rows_read = sum(min(int(nvalid[lay.q_start[b]:lay.q_start[b + 1]].sum()), int(seq_len[b]))
+                    for b in range(lay.num_seqs))
+    mla_bytes = rows_read * 1152 + lay.num_q * H * (576 + 512) * 2
+    return {"indexer": {"flops": idx_flops, "bytes": float(idx_bytes)},
+            "topk": {"flops": 0.0, "bytes": float(topk_bytes)},
+            "sparse_mla": {"flops": mla_flops, "bytes": float(mla_bytes)}}
+
+
+def kernel_bound(name, work, peaks, fp8):
+    """Roofline bound of a kernel: whichever of tensor / HBM time is larger."""
+    tc = peaks["bf16_sustained"] * (2.0 if (fp8 and name == "indexer") else 1.0)
+    t_tc = work["flops"] / (tc * 1e12) if work["flops"] else 0.0
+    t_hbm = work["bytes"] / (peaks["hbm"] * 1e9)
+    if t_tc >= t_hbm:
+        return "tensor", tc, "TFLOP/s"
+    return "hbm", peaks["hbm"], "GB/s"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 9]
+        if self.bus_id:
+            mine = [r for r in rows if self.bus_id.endswith(r[1].lower()[-12:]) or
+                    r[1].lower().endswith(self.bus_id[-12:])]
+            rows = mine or rows
+        idx0 = rows[0][0] if rows else None
+        rows = [r for r in rows if r[0] == idx0]
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.strip() == "Active"})
+        load = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- inputs
+def setup(workload, dev, seed=0):
+    import torch
+
+    import dsa_indexer_indexshare_gb300 as dsa
+    import synth
+
+    cfg = dict(synth.WORKLOADS[workload])
+    lay = synth.workload_layout(workload, seed)
+    types = cfg["layers"]
+    fp8 = bool(cfg.get("fp8"))
+    layers = synth.device_layers(lay, types, cfg["H"], device=dev, seed=seed,
+                                 ints=bool(cfg.get("ints")))
+    if fp8:  # the FP8 indexer consumes Hadamard-rotated E4M3 codes from the library's quantiser
+        for L in layers:
+            if "q_idx" in L:
+                qc, qs = dsa.dsa_fp8_quantize(L["q_idx"])
+                kc, ks = dsa.dsa_fp8_quantize(L["k_idx"])
+                L.update(q_idx=qc, q_scale=qs, k_idx=kc, k_scale=ks)
+        torch.cuda.synchronize(dev)
+    batch = dsa.Batch(lay.q_start, lay.q_pos, lay.seq_row0, lay.max_len, device=dev)
+    return cfg, lay, layers, batch, fp8
+
+
+def time_steps(run, steps, warmup, flush, stream):
+    import torch
+    for _ in range(warmup):
+        run()
+        flush()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        evs.append((a, b))
+        flush()  # outside the timed events: L2 is cold at every step
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(workload, lay, layers, cfg, fp8, nrows, seed=1):
+    """Host copies of a sampled set of query rows (and the caches they read)."""
+    import torch
+    rng = np.random.default_rng(seed)
+    nq = lay.num_q
+    K = cfg["K"]
+    fixed = [r for r in (0, K - 2, K - 1, K, nq - 1) if 0 <= r < nq]
+    rest = rng.choice(nq, size=max(0, min(nq, nrows) - len(fixed)), replace=False)
+    rows = np.unique(np.concatenate([fixed, rest]).astype(np.int64))[:max(nrows, 1)]
+
+    def hb(t):  # bf16 tensor -> uint16 bits
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    host = []
+    rt = torch.as_tensor(rows, device=layers[0]["q_lat"].device)
+    for L in layers:
+        d = {"q_lat": hb(L["q_lat"].index_select(0, rt)), "q_rope": hb(L["q_rope"].index_select(0, rt)),
+             "kv": hb(L["kv"])}
+        if "q_idx" in L:
+            if fp8:
+                d.update(q_idx=L["q_idx"].index_select(0, rt).cpu().numpy(),
+                         q_scale=L["q_scale"].index_select(0, rt).cpu().numpy(),
+                         k_idx=L["k_idx"].cpu().numpy(), k_scale=L["k_scale"].cpu().numpy())
+            else:
+                d.update(q_idx=hb(L["q_idx"].index_select(0, rt)), k_idx=hb(L["k_idx"]))
+            d["w"] = L["w"].index_select(0, rt).cpu().numpy()
+        host.append(d)
+    return rows, host
+
+
+def run_oracle(lay, host, rows, cfg, fp8):
+    import oracle
+    pos, key0 = oracle.row_metadata(lay.q_start, lay.q_pos, lay.seq_row0, rows)
+    t0 = time.perf_counter()
+    oracle.group_forward(cfg["layers"], host, np.arange(len(rows), dtype=np.int32), pos, key0,
+                         lay.max_len, cfg["K"], 1 / 16, idx_dtype=1 if fp8 else 0)
+    return time.perf_counter() - t0
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill8k", choices=list(DESCR))
+    ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=0)
+    args = ap.parse_args()
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return reference_arm(args)
+
+    import torch.distributed as dist
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import dsa_indexer_indexshare_gb300 as dsa
+    peaks = load_peaks()
+    cfg, lay, layers, batch, fp8 = setup(args.workload, dev)
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.fill_(1)
+
+    def make_group(types):
+        g = dsa.Group(types, layers_for(types), k=cfg["K"], scale=1 / 16)
+        ws = dsa.workspace(g.workspace_size(batch), dev)
+        idx = torch.empty((lay.num_q, cfg["K"]), dtype=torch.int32, device=dev)
+        return g, ws, idx
+
+    def layers_for(types):
+        if types == cfg["layers"]:
+            return layers
+        # every-layer-indexer ablation: each layer runs its own indexer over
+        # the F layer's indexer inputs of its group
+        out = []
+        last_f = None
+        for l, c in enumerate(cfg["layers"]):
+            if c == "F":
+                last_f = layers[l]
+            d = dict(layers[l])
+            for k_ in ("q_idx", "w", "k_idx", "q_scale", "k_scale"):
+                if k_ in last_f:
+                    d[k_] = last_f[k_]
+            out.append(d)
+        return out
+
+    group, ws, idx_buf = make_group(cfg["layers"])
+    run = lambda: dsa.indexshare_group_forward(group, batch, idx_buf, ws=ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- timed region
+    for _ in range(args.warmup):
+        run()
+        flush()
+    dsa.status_fetch(ws)
+    barrier()
+    dsa.launch_counts_reset()
+    dsa.dsa_profile_enable(True)
+    try:
+        bus = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None)
+    except Exception:
+        bus = None
+    clk = ClockSampler(bus)
+    clk.start()
+    time.sleep(0.3)
+    barrier()
+    wall0 = time.perf_counter()
+    times = time_steps(run, args.steps, 0, flush, stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks = clk.stop()
+    dsa.dsa_profile_enable(False)
+    prof = dsa.dsa_profile_collect()
+    launches = sum(dsa.launch_counts().values())
+    dsa.status_fetch(ws)
+
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens_per_step = lay.num_q
+    value = world * tokens_per_step * args.steps / (total_ms / 1e3)
+
+    # ---- per-kernel roofline (live CUDA events around each launch)
+    work = algorithmic(lay, cfg, fp8)
+    kernels = {}
+    for name in ("indexer", "topk", "sparse_mla"):
+        ms, n = prof[name]
+        if n == 0:
+            continue
+        avg_s = ms / n / 1e3
+        bound, peak, unit = kernel_bound(name, work[name], peaks, fp8)
+        ach = (work[name]["flops"] / avg_s / 1e12) if bound == "tensor" else (
+            work[name]["bytes"] / avg_s / 1e9)
+        kernels[name] = {"launches": n, "ms_per_launch": round(ms / n, 4), "share": None,
+                         "bound": bound, "achieved": round(ach, 2), "peak": peak, "unit": unit,
+                         "frac": round(ach / peak, 4)}
+    ktot = sum(v["ms_per_launch"] * v["launches"] for v in kernels.values())
+    for v in kernels.values():
+        v["share"] = round(v["ms_per_launch"] * v["launches"] / ktot, 4) if ktot else None
+    top = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"])
+    tk = kernels[top]
+    traffic = None
+    if top in NCU_TRAFFIC and NCU_TRAFFIC[top].get("src") == kernel_src_hash(KSRC[top]) and \
+            NCU_TRAFFIC[top].get("workload") == args.workload:
+        traffic = NCU_TRAFFIC[top]["bytes"]
+    roofline = {"kernel": top, "bound": tk["bound"], "achieved": tk["achieved"], "peak": tk["peak"],
+                "unit": tk["unit"], "frac": tk["frac"], "traffic": traffic,
+                "peak_src": f"{peaks['src']} ({'sustained bf16' if tk['bound'] == 'tensor' else 'HBM copy'})",
+                "units_per_launch": (work[top]["flops"] if tk["bound"] == "tensor" else work[top]["bytes"])}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" + ("+fp8-indexer" if fp8 else ""),
+            "data": "synthetic (seeded N(0,1)/sqrt(d) bf16, device-resident)",
+            "config": {"workload": DESCR[args.workload], "global_batch": world * tokens_per_step,
+                       "seq_len": int(lay.max_len), "layers": cfg["layers"],
+                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "flushed between steps (256 MiB write, outside the timed events)"},
+            "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
+            "clocks": clocks, "wall_s_timed": round(wall, 3)}
+
+    # ---- IndexShare ablation: every layer runs its own indexer
+    if not args.no_ablation:
+        types_all = "F" * len(cfg["layers"])
+        g2, ws2, idx2 = make_group(types_all)
+        t2 = time_steps(lambda: dsa.indexshare_group_forward(g2, batch, idx2, ws=ws2),
+                        args.steps, args.warmup, flush, stream)
+        dsa.status_fetch(ws2)
+        v2 = tokens_per_step * args.steps / (sum(t2) / 1e3)
+        line["ablation"] = {"layers": types_all, "value": round(world * v2, 1),
+                            "ms_per_step": round(sum(t2) / args.steps, 4),
+                            "indexshare_speedup": round(sum(t2) / total_ms, 3)}
+        del g2, ws2, idx2
+
+    # ---- end to end through the public API with host buffers
+    if not args.no_e2e:
+        line["e2e"] = e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, world)
+
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
+    if not args.no_cpu and rank == 0 and world == 1:
+        nrows = args.cpu_rows or {"tiny": 512, "prefill8k": 48, "decode64": 4, "chunked": 24,
+                                  "decode1m": 1}[args.workload]
+        rows, host = oracle_sample(args.workload, lay, layers, cfg, fp8, nrows)
+        import oracle
+        secs = run_oracle(lay, host, rows, cfg, fp8)
+        line["cpu_baseline"] = {"value": round(len(rows) / secs, 3), "unit": UNIT,
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{len(rows)} query rows of the same workload (full group, "
+                                          f"all layers), {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, world):
+    """Same metric through indexshare_group_forward, with every step's inputs
+    copied from pinned host memory and the outputs copied back inside the
+    timed region."""
+    import torch
+    keys = ("q_lat", "q_rope", "kv", "q_idx", "w", "k_idx", "q_scale", "k_scale")
+    pairs = []
+    for L in layers:
+        for k_ in keys:
+            if k_ in L:
+                h = torch.empty(L[k_].shape, dtype=L[k_].dtype, pin_memory=True)
+                h.copy_(L[k_])
+                pairs.append((h, L[k_]))
+    outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in group.outs]
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
+    d2h = sum(o.numel() * o.element_size() for o in outs_h)
+
+    def step():
+        for h, d in pairs:
+            d.copy_(h, non_blocking=True)
+        dsa.indexshare_group_forward(group, batch, idx_buf, ws=ws)
+        for o_h, o_d in zip(outs_h, group.outs):
+            o_h.copy_(o_d, non_blocking=True)
+
+    steps = max(3, args.steps // 2)
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(world * lay.num_q * steps / (ms / 1e3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms / steps, 3)}
+
+
+def reference_arm(args):
+    """The CPU oracle as the reference arm: each step runs the full group on a
+    bounded sample of the workload's query rows."""
+    import oracle
+    import synth
+    cfg = dict(synth.WORKLOADS[args.workload])
+    lay = synth.workload_layout(args.workload)
+    fp8 = bool(cfg.get("fp8"))
+    nrows = args.cpu_rows or {"tiny": 64, "prefill8k": 8, "decode64": 1, "chunked": 4,
+                              "decode1m": 1}[args.workload]
+    sub, rows, host = reference_inputs(lay, cfg, fp8, nrows)
+    for _ in range(args.warmup):
+        run_oracle(sub, host, rows, cfg, fp8)
+    t = 0.0
+    for _ in range(args.steps):
+        t += run_oracle(sub, host, rows, cfg, fp8)
+    value = len(rows) * args.steps / t
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t / args.steps, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": DESCR[args.workload], "layers": cfg["layers"]},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{len(rows)} query rows per step of the same workload"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def reference_inputs(lay, cfg, fp8, nrows):
+    """Host inputs for the oracle arm: a sampled set of query rows and the
+    caches of their sequences, drawn with the seeded host generator.  Returns
+    a sub-layout holding just those sequences, the sampled rows in it, and the
+    per-layer host tensors (query tensors hold the sampled rows only)."""
+    import oracle
+    import synth
+    rng = np.random.default_rng(1)
+    K = cfg["K"]
+    fixed = [r for r in (lay.num_q - 1, K, K - 1) if 0 <= r < lay.num_q]
+    pick = rng.choice(lay.num_q, min(nrows, lay.num_q), replace=False)
+    rows = np.sort(np.unique(np.concatenate([fixed, pick]))[:nrows]).astype(np.int64)
+    seq = np.searchsorted(lay.q_start, rows, side="right") - 1
+    useq = list(np.unique(seq))
+    lens = [int(lay.q_pos[lay.q_start[b + 1] - 1]) + 1 for b in useq]
+    counts = [int(lay.q_start[b + 1] - lay.q_start[b]) for b in useq]
+    sub = synth.make_layout(lens, counts)
+    sub_rows = np.array([sub.q_start[useq.index(b)] + (r - lay.q_start[b]) for r, b in zip(rows, seq)],
+                        np.int64)
+    g = synth.HostGen(0)
+    n = len(rows)
+    host = []
+    for l, tch in enumerate(cfg["layers"]):
+        base = 100 * (l + 1)
+        d = {"q_lat": g.gauss_bf16(base, (n, cfg["H"], 512), 512),
+             "q_rope": g.gauss_bf16(base + 1, (n, cfg["H"], 64), 64),
+             "kv": np.concatenate([g.gauss_bf16(base + 2, (sub.rows, 512), 512),
+                                   g.gauss_bf16(base + 3, (sub.rows, 64), 64)], axis=1)}
+        if tch == "F":
+            q = g.gauss_bf16(base + 10, (n, 32, 128), 128)
+            k = g.gauss_bf16(base + 12, (sub.rows, 128), 128)
+            d["w"] = g.gauss_f32(base + 11, (n, 32), 32)
+            if fp8:
+                qc, qs = oracle.fp8_quantize_rows(q.reshape(-1, 128))
+                kc, ks = oracle.fp8_quantize_rows(k)
+                d.update(q_idx=qc.reshape(n, 32, 128), q_scale=qs.reshape(n, 32), k_idx=kc,
+                         k_scale=ks)
+            else:
+                d.update(q_idx=q, k_idx=k)
+        host.append(d)
+    return sub, sub_rows, host
+
+
+if __name__ == "__main__":
+    main()

@@ -65,6 +65,8 @@ def _load():
         "dsa_launch_counts": (c_int, [POINTER(c_uint64), c_int]),
         "dsa_launch_counts_reset": (None, []),
         "dsa_set_wait_timeout_ns": (None, [c_uint64]),
+        "dsa_profile_enable": (None, [c_int]),
+        "dsa_profile_collect": (c_int, [POINTER(ctypes.c_double), POINTER(c_uint64), c_int]),
         "dsa_selftest_wait_timeout": (st, [c_void_p, c_size_t, c_void_p]),
         "dsa_indexer_workspace_size": (c_size_t, [B]),
         "dsa_indexer_scores": (st, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
@@ -167,6 +169,20 @@ def launch_counts() -> dict:
 
 def launch_counts_reset():
     lib.dsa_launch_counts_reset()
+
+
+def dsa_profile_enable(on: bool = True):
+    lib.dsa_profile_enable(1 if on else 0)
+
+
+def dsa_profile_collect() -> dict:
+    """{kind: (total_ms, launches)} of the launches recorded since the last collect."""
+    n = len(LAUNCH_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (c_uint64 * n)()
+    if lib.dsa_profile_collect(ms, cnt, n) < 0:
+        raise DsaError(DSA_ERR_CUDA, "dsa_profile_collect")
+    return {k: (ms[i], int(cnt[i])) for i, k in enumerate(LAUNCH_KINDS)}
 
 
 def set_wait_timeout_ns(ns: int):

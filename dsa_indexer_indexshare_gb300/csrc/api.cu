@@ -6,7 +6,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
+#include <vector>
 
 #include "common.cuh"
 
@@ -137,6 +139,46 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
 }
 
 void count_launch(int which) { g_launches[which].fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+struct ProfRec {
+  cudaEvent_t start, stop;
+  int kind;
+};
+std::mutex g_prof_mu;
+std::atomic<int> g_prof_on{0};
+std::vector<ProfRec> g_prof_recs;      // recorded, not yet collected
+std::vector<cudaEvent_t> g_prof_free;  // reusable events
+thread_local cudaEvent_t g_prof_pending = nullptr;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_free.empty()) {
+    cudaEvent_t e = g_prof_free.back();
+    g_prof_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+}  // namespace
+
+void prof_begin(cudaStream_t stream) {
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_pending = prof_event();
+  if (g_prof_pending) cudaEventRecord(g_prof_pending, stream);
+}
+
+void prof_end(int which, cudaStream_t stream) {
+  if (!g_prof_on.load(std::memory_order_relaxed) || !g_prof_pending) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  cudaEvent_t stop = prof_event();
+  if (!stop) return;
+  cudaEventRecord(stop, stream);
+  g_prof_recs.push_back(ProfRec{g_prof_pending, stop, which});
+  g_prof_pending = nullptr;
+}
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 
 }  // namespace dsa
@@ -180,6 +222,31 @@ void dsa_launch_counts_reset(void) {
 }
 
 void dsa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
+
+void dsa_profile_enable(int on) { g_prof_on.store(on ? 1 : 0); }
+
+int dsa_profile_collect(double* ms, uint64_t* launches, int n) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (int i = 0; i < n; ++i) {
+    ms[i] = 0.0;
+    launches[i] = 0;
+  }
+  int rc = kNumLaunchKinds;
+  for (const ProfRec& r : g_prof_recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      rc = -1;
+    if (r.kind < n) {
+      ms[r.kind] += t;
+      launches[r.kind] += 1;
+    }
+    g_prof_free.push_back(r.start);
+    g_prof_free.push_back(r.stop);
+  }
+  g_prof_recs.clear();
+  return rc;
+}
 
 dsa_status_t dsa_selftest_wait_timeout(void* d_ws, size_t ws_bytes, dsa_stream_t stream) {
   if (dsa_status_t s = check_ws(d_ws, ws_bytes, kStatusBytes)) return s;

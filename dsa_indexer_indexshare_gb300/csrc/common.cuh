@@ -50,6 +50,9 @@ __device__ __forceinline__ int query_pos(const BatchArgs& b, int t, int* status)
 bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
                   uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows);
 void count_launch(int which);
+// Event pair around a launch when profiling is enabled (no-ops otherwise).
+void prof_begin(cudaStream_t stream);
+void prof_end(int which, cudaStream_t stream);
 uint64_t wait_timeout_ns();
 
 enum LaunchKind { kLaunchIndexer = 0, kLaunchTopk, kLaunchMla, kLaunchCombine, kLaunchQuant,

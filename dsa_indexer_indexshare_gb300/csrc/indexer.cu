@@ -283,7 +283,9 @@ cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, Indexer
   p.num_kc = (p.b.max_len + p.kc_blocks * 128 - 1) / (p.kc_blocks * 128);
   dim3 grid(static_cast<unsigned>(p.num_qb) * static_cast<unsigned>(p.num_kc),
             static_cast<unsigned>(p.b.num_seqs));
+  prof_begin(stream);
   kern<<<grid, 192, C::SMEM, stream>>>(qmap, kmap, p);
+  prof_end(kLaunchIndexer, stream);
   count_launch(kLaunchIndexer);
   return cudaGetLastError();
 }

@@ -96,8 +96,10 @@ cudaError_t launch_quantize(const void* x, int64_t rows, uint8_t* codes, float* 
                             cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + 7) / 8;
+  prof_begin(stream);
   fp8_quant_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       static_cast<const uint16_t*>(x), rows, codes, scale);
+  prof_end(kLaunchQuant, stream);
   count_launch(kLaunchQuant);
   return cudaGetLastError();
 }

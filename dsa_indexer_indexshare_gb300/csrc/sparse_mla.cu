@@ -14,10 +14,12 @@
 //   S^T[128 keys, H]   = C[128, 576] . Q[H, 576]^T         (A = C, K-major)
 //   O^T[512 dims, H]  += C[128, :512]^T . P^T[H, 128]^T     (A = C^T, MN-major)
 // so both contractions use the full 128-row datapath even with H = 64 (or
-// 16) heads.  The selected rows are gathered with TMA gather4 (four rows per
-// copy, 128-byte swizzle) straight into the MMA operand layout, one 64-column
-// sub-tile at a time, and each sub-tile is refilled for the next block as
-// soon as the P.V chunk that reads it completes.  P^T reuses the RoPE
+// 16) heads.  The selected rows are gathered by two producer warps with
+// 16-byte cp.async straight into the 128-byte-swizzled MMA operand layout,
+// one 64-column sub-tile at a time (completion tracked on an mbarrier), and
+// each sub-tile is refilled for the next block as soon as the P.V chunk that
+// reads it completes.  (TMA gather4 of 128-byte row segments sustains only
+// about 2 TB/s over the whole chip; cp.async sustains several times that.)  P^T reuses the RoPE
 // sub-tile, which is free once S^T is computed.
 //
 // Softmax: the thread of TMEM lane i owns key i of the block; at H = 64 two
@@ -25,8 +27,9 @@
 // exceeds it by more than 2^8 (then O^T and the partial sums are rescaled in
 // place); row sums are kept per thread and reduced once at the end.
 //
-// Warp roles: softmax / epilogue warps (8 at H = 64, 4 at H = 16), then one
-// TMA producer warp and one MMA issuer warp (also the TMEM owner).
+// Warp roles: softmax / epilogue warps (8 at H = 64, 4 at H = 16), then two
+// producer warps (Q by TMA, gathered rows by cp.async) and one MMA issuer
+// warp (also the TMEM owner).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -43,7 +46,9 @@ struct MlaCfg {
   static constexpr int QSUB = H * 128;       // one 64-dim sub-tile of Q: H rows x 128 B
   static constexpr int Q_BYTES = 9 * QSUB;
   static constexpr int CSUB = 128 * 128;     // one 64-dim sub-tile of 128 gathered rows
-  static constexpr int PSUB = H * 128;       // P^T sub-tile: H rows x 64 keys
+  static constexpr int PSUB = H * 128;       // P^T sub-tile (H = 16): H rows x 64 keys
+  // At H = 64, P is stored MN-major: one 128-byte row of 64 heads per key.
+  static constexpr bool P_MN = H == 64;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_C = OFF_Q + Q_BYTES;
   static constexpr int OFF_P = OFF_C + 8 * CSUB;  // the RoPE sub-tile
@@ -57,7 +62,8 @@ struct MlaCfg {
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static constexpr int HW = H > 32 ? 32 : H;       // heads per softmax warp
   static constexpr int NSW = 4 * (H / HW);           // softmax warps (two per lane quarter at H=64)
-  static constexpr int NT = NSW * 32 + 64;           // + producer warp + MMA warp
+  static constexpr int NPW = 2;                      // cp.async producer warps
+  static constexpr int NT = NSW * 32 + NPW * 32 + 32; // + producers + MMA warp
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_S = 0;        // S^T: H columns
   static constexpr uint32_t TM_O = 256;      // O^T chunk c: columns 256 + c*H
@@ -69,6 +75,8 @@ struct MlaCfg {
 
 struct MlaParams {
   BatchArgs b;
+  const uint16_t* kv;  // [kv_rows, 576] bf16
+  int64_t kv_rows;
   const int32_t* idx;
   int K;
   float scale_log2;
@@ -127,11 +135,10 @@ __device__ __forceinline__ void tmem_cols_store(uint32_t taddr, const float (&v)
 template <int H, int NSPLIT>
 __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap qlat_map,
-                      const __grid_constant__ CUtensorMap qrope_map,
-                      const __grid_constant__ CUtensorMap kv_map, const MlaParams p) {
+                      const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
   using C = MlaCfg<H>;
   constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
-  constexpr int W_PROD = NSW, W_MMA = NSW + 1;
+  constexpr int W_PROD = NSW, W_MMA = NSW + C::NPW, NPT = C::NPW * 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(bar(B_Q), 1);
-    for (int i = 0; i < 9; ++i) mbar_init(bar(B_CFULL + i), 1);
+    for (int i = 0; i < 9; ++i) mbar_init(bar(B_CFULL + i), NPT);
     for (int i = 0; i < 4; ++i) mbar_init(bar(B_CFREE + i), 1);
     mbar_init(bar(B_S), 1);
     mbar_init(bar(B_P), NST);
@@ -193,7 +200,6 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   if (warp == W_PROD && lane == 0) {
     tma_prefetch_desc(&qlat_map);
     tma_prefetch_desc(&qrope_map);
-    tma_prefetch_desc(&kv_map);
   }
   tc_fence_before();
   __syncthreads();
@@ -202,25 +208,33 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   const uint64_t to = p.timeout_ns;
   volatile int no_abort = 0;
 
-  if (warp == W_PROD) {
-    // ------------------------------------------------ producer: Q once, gathered C per block
-    if (lane == 0) {
+  if (warp >= W_PROD && warp < W_MMA) {
+    // ------------------------------------------------ producers: Q once (TMA), gathered C
+    // rows per block with 16-byte cp.async (TMA gather4 of 128-byte row
+    // segments is far slower per SM).  Thread pt copies 16-byte chunk
+    // (pt & 7) of rows (pt >> 3) + 8c, c < 16, of every 64-column sub-tile,
+    // into the 128-byte-swizzled K-major layout the MMA reads.
+    const int pt = tid - NST;
+    if (pt == 0) {
       mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
       for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, t * H, bar(B_Q));
       tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, t * H, bar(B_Q));
     }
-    int uses = 0;  // completed issue rounds of every sub-tile
+    const int kch = pt & 7, rb = pt >> 3;
+    const uint32_t dst0 = sC + rb * 128 + ((kch ^ rb) << 4);  // row rb + 8c has the same swizzle
     for (int j = j0; j < j1; ++j) {
-      int r[4];
+      int rows[16];  // cache rows (< kv_rows < 2^31) of this thread's 16 keys
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int sl = j * 128 + 4 * lane + q;
+      for (int c = 0; c < 16; ++c) {
+        const int sl = j * 128 + rb + 8 * c;
         int e = -1;
         if (sl < nvalid) e = idx_row[sl];
-        const bool ok = e >= 0 && e <= pos;
-        if (sl < nvalid && !ok && e != -1) atomicOr(p.status, DSA_DEVERR_INDEX);
-        r[q] = static_cast<int>(row0 + (ok ? e : 0));
+        const int64_t rr = row0 + e;
+        const bool ok = e >= 0 && e <= pos && rr < p.kv_rows;
+        if (sl < nvalid && !ok && e != -1 && kch == 0) atomicOr(p.status, DSA_DEVERR_INDEX);
+        rows[c] = ok ? static_cast<int>(rr) : 0;
       }
+      const uint16_t* kvk = p.kv + kch * 8;
       bool alive = true;
 #pragma unroll 1
       for (int i = 0; i < 9; ++i) {
@@ -231,33 +245,31 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
             break;
           }
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar(B_CFULL + i), C::CSUB);
-        __syncwarp();
-        tma_gather4(sC + i * C::CSUB + lane * 512, &kv_map, 64 * i, r[0], r[1], r[2], r[3],
-                    bar(B_CFULL + i));
+        const uint32_t dst = dst0 + i * C::CSUB;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + c * 1024),
+                       "l"(kvk + static_cast<int64_t>(rows[c]) * 576 + 64 * i)
+                       : "memory");
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(B_CFULL + i))
+                     : "memory");
       }
-      __syncwarp();
       if (!alive) break;
-      ++uses;
     }
-    // let every copy this CTA started land before it can exit
-    if (lane == 0) {
-      mbar_wait(bar(B_Q), 0, &no_abort, nullptr, to);
-      if (uses > 0)
-        for (int i = 0; i < 9; ++i) mbar_wait(bar(B_CFULL + i), (uses - 1) & 1, &no_abort, nullptr, to);
-    }
-    __syncwarp();
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (pt == 0) mbar_wait(bar(B_Q), 0, &no_abort, nullptr, to);
   } else if (warp == W_MMA) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, H, false, false);
-      constexpr uint32_t id_pv = idesc_bf16(128, H, true, false);
+      constexpr uint32_t id_pv = idesc_bf16(128, H, true, C::P_MN);
       bool ok = mbar_wait(bar(B_Q), 0, abort_flag, p.status, to);
       for (int j = j0; ok && j < j1; ++j) {
         const int u = j - j0;
         for (int i = 0; i < 9 && ok; ++i) {
           ok = mbar_wait(bar(B_CFULL + i), u & 1, abort_flag, p.status, to);
           if (!ok) break;
+          fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05.mma reads
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -275,7 +287,9 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
           for (int kk = 0; kk < 8; ++kk)
             umma_bf16(tbase + C::TM_O + c * H,
                       sdesc_sw128(sC + 2 * c * C::CSUB + kk * 2048, C::CSUB, 1024),
-                      sdesc_sw128(sP + (kk >> 2) * C::PSUB + (kk & 3) * 32, 0, 1024), id_pv,
+                      C::P_MN ? sdesc_sw128(sP + kk * 2048, 8192, 1024)
+                              : sdesc_sw128(sP + (kk >> 2) * C::PSUB + (kk & 3) * 32, 0, 1024),
+                      id_pv,
                       (u > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(B_CFREE + c));
         }
@@ -291,27 +305,34 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     const int key = quarter * 32 + lane;       // key of the block (= TMEM lane)
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
-    float lpart[HW];
+    float lpart[HW];  // this thread's share of the softmax denominators
+    float mneg[HW];   // minus the running maximum (log2 units); +inf before any key
 #pragma unroll
-    for (int h = 0; h < HW; ++h) lpart[h] = 0.f;
-    uint8_t* pbase = sm + C::OFF_P + (key >> 6) * C::PSUB;
-    const int kb = (key & 63) * 2;  // byte offset of this key inside a P^T row
+    for (int h = 0; h < HW; ++h) {
+      lpart[h] = 0.f;
+      mneg[h] = INFINITY;
+    }
+    int e_next = (j0 * 128 + key < nvalid && j0 < j1) ? idx_row[j0 * 128 + key] : -1;
     for (int j = j0; j < j1; ++j) {
       const int u = j - j0;
+      const int e = e_next;  // index of this thread's key, loaded one block ahead
+      {
+        const int sn = (j + 1) * 128 + key;
+        e_next = (j + 1 < j1 && sn < nvalid) ? idx_row[sn] : -1;
+      }
       if (!mbar_wait(bar(B_S), u & 1, abort_flag, p.status, to)) break;
       tc_fence_after();
-      const int sl = j * 128 + key;
-      int e = -1;
-      if (sl < nvalid) e = idx_row[sl];
-      const bool valid = e >= 0 && e <= pos;
-      float z[HW];
-      tmem_cols_load<HW>(lane_base + C::TM_S + h0, z);
-      bool exceed = false;
+      const bool valid = e >= 0 && e <= pos && row0 + e < p.kv_rows;
+      // d = scale*log2(e)*s - m: the exponent of P and the rescale test in one FFMA
+      float d[HW];
+      tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
+      float dmax = -INFINITY;
 #pragma unroll
       for (int h = 0; h < HW; ++h) {
-        z[h] = valid ? z[h] * sl2 : -INFINITY;
-        exceed |= z[h] > m_used[h0 + h] + kRescaleThreshold;
+        d[h] = fmaf(d[h], sl2, mneg[h]);
+        dmax = fmaxf(dmax, d[h]);
       }
+      const bool exceed = valid && dmax > kRescaleThreshold;
       const unsigned any = __any_sync(0xffffffffu, exceed);
       if (lane == 0) flags[warp] = any ? 1 : 0;
       named_bar_sync(1, NST);
@@ -319,9 +340,13 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
 #pragma unroll
       for (int w = 0; w < NSW; ++w) resc |= flags[w];
       if (resc) {
+        // raise the running maximum to this block's maximum (rare after the
+        // first block): exact per-head maximum over the valid keys
+        tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);  // raw scores again
 #pragma unroll
         for (int h = 0; h < HW; ++h) {
-          float v = z[h];
+          d[h] *= sl2;
+          float v = valid ? d[h] : -INFINITY;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
           if (lane == 0) red[quarter * H + h0 + h] = v;
@@ -336,27 +361,57 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         }
         named_bar_sync(1, NST);
 #pragma unroll
-        for (int h = 0; h < HW; ++h) lpart[h] *= fac[h0 + h];
-        if (u > 0) {  // O^T rows of this thread: dims 128c + key
+        for (int h = 0; h < HW; ++h) {
+          mneg[h] = -m_used[h0 + h];
+          lpart[h] *= fac[h0 + h];
+          d[h] += mneg[h];
+        }
+        if (u > 0) {  // O^T rows of this thread: dims 128c + key, 16 heads at a time
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float o[HW];
-            tmem_cols_load<HW>(lane_base + C::TM_O + c * H + h0, o);
+          for (int c = 0; c < 4 * (HW / 16); ++c) {
+            const int hh = (c % (HW / 16)) * 16;
+            const uint32_t col = C::TM_O + (c / (HW / 16)) * H + h0 + hh;
+            float o[16];
+            tmem_cols_load<16>(lane_base + col, o);
 #pragma unroll
-            for (int h = 0; h < HW; ++h) o[h] *= fac[h0 + h];
-            tmem_cols_store<HW>(lane_base + C::TM_O + c * H + h0, o);
+            for (int h = 0; h < 16; ++h) o[h] *= fac[h0 + hh + h];
+            tmem_cols_store<16>(lane_base + col, o);
           }
           tmem_wait_st();
         }
       }
-      // P^T[h][key] = bf16(2^(z - m)); 128-byte swizzled K-major rows of 64 keys
+      if constexpr (C::P_MN) {
+        // P[key][h] = bf16(2^d): one 128-byte swizzled row per key (heads
+        // contiguous), written as 16-byte vectors of eight heads
+        uint8_t* prow = sm + C::OFF_P + key * 128;
 #pragma unroll
-      for (int h = 0; h < HW; ++h) {
-        const int hg = h0 + h;
-        const float pv = valid ? ex2(z[h] - m_used[hg]) : 0.f;
-        lpart[h] += pv;
-        const int off = hg * 128 + ((((kb >> 4) ^ (hg & 7)) << 4) | (kb & 15));
-        *reinterpret_cast<__nv_bfloat16*>(pbase + off) = __float2bfloat16_rn(pv);
+        for (int q = 0; q < HW / 8; ++q) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const int h = q * 8 + k2 * 2;
+            const float p0 = valid ? ex2(d[h]) : 0.f;
+            const float p1 = valid ? ex2(d[h + 1]) : 0.f;
+            lpart[h] += p0;
+            lpart[h + 1] += p1;
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            wv[k2] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          const int chunk = ((h0 >> 3) + q) ^ (key & 7);
+          *reinterpret_cast<uint4*>(prow + (chunk << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+      } else {
+        // P^T[h][key]: K-major rows of 64 keys per head (H = 16)
+        uint8_t* pbase = sm + C::OFF_P + (key >> 6) * C::PSUB;
+        const int kb = (key & 63) * 2;
+#pragma unroll
+        for (int h = 0; h < HW; ++h) {
+          const int hg = h0 + h;
+          const float pv = valid ? ex2(d[h]) : 0.f;
+          lpart[h] += pv;
+          const int off = hg * 128 + ((((kb >> 4) ^ (hg & 7)) << 4) | (kb & 15));
+          *reinterpret_cast<__nv_bfloat16*>(pbase + off) = __float2bfloat16_rn(pv);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -465,8 +520,8 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
 }
 
 template <int H, int NSPLIT>
-cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const CUtensorMap& kvm,
-                       const MlaParams& p, cudaStream_t stream) {
+cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p,
+                       cudaStream_t stream) {
   using C = MlaCfg<H>;
   auto* kern = sparse_mla_kernel<H, NSPLIT>;
   static int configured_device = -1;
@@ -489,19 +544,21 @@ cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const CUten
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ql, qr, kvm, p);
+  prof_begin(stream);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ql, qr, p);
+  prof_end(kLaunchMla, stream);
   count_launch(kLaunchMla);
   return e;
 }
 
 template <int H>
-cudaError_t launch_h(const CUtensorMap& ql, const CUtensorMap& qr, const CUtensorMap& kvm,
-                     const MlaParams& p, int nsplit, cudaStream_t stream) {
+cudaError_t launch_h(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p, int nsplit,
+                     cudaStream_t stream) {
   switch (nsplit) {
-    case 1: return launch_mla<H, 1>(ql, qr, kvm, p, stream);
-    case 2: return launch_mla<H, 2>(ql, qr, kvm, p, stream);
-    case 4: return launch_mla<H, 4>(ql, qr, kvm, p, stream);
-    default: return launch_mla<H, 8>(ql, qr, kvm, p, stream);
+    case 1: return launch_mla<H, 1>(ql, qr, p, stream);
+    case 2: return launch_mla<H, 2>(ql, qr, p, stream);
+    case 4: return launch_mla<H, 4>(ql, qr, p, stream);
+    default: return launch_mla<H, 8>(ql, qr, p, stream);
   }
 }
 
@@ -514,14 +571,15 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
                               const dsa_batch_t& b, void* out, float* lse, void*, size_t,
                               int* status, cudaStream_t stream) {
   if (b.num_q == 0) return cudaSuccess;
-  CUtensorMap ql, qr, kvm;
+  CUtensorMap ql, qr;
   const uint64_t qrows = static_cast<uint64_t>(b.num_q) * heads;
   if (!make_tmap_2d(&ql, q_lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 512, qrows, 64, heads) ||
-      !make_tmap_2d(&qr, q_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, qrows, 64, heads) ||
-      !make_tmap_2d(&kvm, kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 576, static_cast<uint64_t>(kv_rows), 64, 1))
+      !make_tmap_2d(&qr, q_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, qrows, 64, heads))
     return cudaErrorInvalidValue;
   MlaParams p{};
   p.b = to_args(b);
+  p.kv = static_cast<const uint16_t*>(kv);
+  p.kv_rows = kv_rows;
   p.idx = idx;
   p.K = k;
   p.scale_log2 = scale * kLog2e;
@@ -535,8 +593,8 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   int nsplit = 1;
   while (nsplit < 8 && nsplit * 2 <= nblk && static_cast<int64_t>(b.num_q) * nsplit * 2 <= 152)
     nsplit *= 2;
-  return heads == 16 ? launch_h<16>(ql, qr, kvm, p, nsplit, stream)
-                     : launch_h<64>(ql, qr, kvm, p, nsplit, stream);
+  return heads == 16 ? launch_h<16>(ql, qr, p, nsplit, stream)
+                     : launch_h<64>(ql, qr, p, nsplit, stream);
 }
 
 }  // namespace dsa

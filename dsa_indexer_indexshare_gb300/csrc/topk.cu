@@ -214,7 +214,9 @@ cudaError_t launch_cl(const float* scores, const dsa_batch_t& b, int k, int32_t*
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  prof_begin(stream);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, scores, to_args(b), k, idx, status);
+  prof_end(kLaunchTopk, stream);
   count_launch(kLaunchTopk);
   return e;
 }

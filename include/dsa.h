@@ -121,6 +121,15 @@ DSA_API dsa_status_t dsa_status_fetch(void* d_ws, dsa_stream_t stream, int32_t* 
 DSA_API int dsa_launch_counts(uint64_t* counts, int n);
 DSA_API void dsa_launch_counts_reset(void);
 
+/* Per-launch timing for benchmarks: while enabled, the library records a
+ * CUDA event pair on the launching stream around every kernel it launches.
+ * dsa_profile_collect() waits for the recorded events, adds the elapsed
+ * milliseconds and launch counts per kind (same order as dsa_launch_counts)
+ * into ms[0..n) / launches[0..n) (zeroed by the call), and clears the record.
+ * Returns how many kinds exist, or -1 on a CUDA error. */
+DSA_API void dsa_profile_enable(int on);
+DSA_API int dsa_profile_collect(double* ms, uint64_t* launches, int n);
+
 /* Upper bound in nanoseconds on every spin-wait inside the kernels launched
  * after this call (default 2e9).  Exposed so that tests can shorten it. */
 DSA_API void dsa_set_wait_timeout_ns(uint64_t ns);
