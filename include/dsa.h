@@ -263,6 +263,40 @@ DSA_API dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_ba
 DSA_API dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
                               dsa_stream_t stream);
 
+/* ------------------------------------------------------------------ no workspace */
+
+/*
+ * dsa_indexer_scores followed by dsa_topk, with no caller workspace.  This
+ * entry point has no counterpart in the method's description; it exists for
+ * callers that cannot allocate device memory: a host framework that owns all
+ * of the device memory and gives its plugins no allocator, or a serving loop
+ * that must not call cudaMalloc / cudaFree because those calls can
+ * synchronise the device and stall every stream.
+ *
+ * The fp32 score matrix and the device status word live in a file-scope
+ * device array of 64 MiB that every GPU loading this library holds until the
+ * process exits.  Limit: num_q * max_len * 4 bytes must not exceed 64 MiB
+ * minus 256 bytes (16,777,152 scores, e.g. 64 decode rows of 128K positions
+ * or 4 rows of 1M); larger batches return DSA_ERR_WORKSPACE before anything
+ * is enqueued.  Arguments, layouts and results are those of
+ * dsa_indexer_scores and dsa_topk; idx is int32 [num_q, k].
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  Every
+ * call clears the status word, then enqueues both kernels on `stream`; if
+ * d_status_out (a device int32) is non-NULL the call's device status bits are
+ * copied there at the end (0 = clean).  All calls share the array and it
+ * keeps the last call's contents, so calls whose kernels overlap on the GPU
+ * (other streams, other host threads on the same device) race on it.  Nothing
+ * is allocated or freed by this call.
+ */
+DSA_API dsa_status_t dsa_indexer_topk_noalloc(const void* q_idx, const float* q_scale,
+                                              const float* w, const void* k_idx,
+                                              const float* k_scale, int64_t k_rows,
+                                              dsa_dtype_t dt, const dsa_batch_t* b, int32_t k,
+                                              int32_t* idx, int32_t* d_status_out,
+                                              dsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
