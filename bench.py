@@ -41,6 +41,9 @@ DESCR = {
                "K=2048, bf16",
     "decode1m": "1M decode: 4 sequences x 1 query, context 1048576, layers FSSS, H=64, K=2048, "
                 "FP8 E4M3 + Hadamard indexer keys/queries, bf16 KV latent",
+    "prefill2k": "profiling case: prefill of 2560 tokens, layers FSSS, H=64, K=2048, bf16",
+    "decode8": "profiling case: decode of 8 sequences x 1 query, context U[98304,131072], FSSS, "
+               "H=64, K=2048, bf16",
 }
 # ncu DRAM traffic of the dominant kernel (bytes per launch), with the hash of
 # the kernel sources it was measured on; ignored once the sources change.
@@ -395,7 +398,7 @@ def main():
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
     if not args.no_cpu and rank == 0 and world == 1:
         nrows = args.cpu_rows or {"tiny": 512, "prefill8k": 48, "decode64": 4, "chunked": 24,
-                                  "decode1m": 1}[args.workload]
+                                  "decode1m": 1, "prefill2k": 48, "decode8": 4}[args.workload]
         rows, host = oracle_sample(args.workload, lay, layers, cfg, fp8, nrows)
         import oracle
         secs = run_oracle(lay, host, rows, cfg, fp8)
@@ -464,7 +467,7 @@ def reference_arm(args):
     lay = synth.workload_layout(args.workload)
     fp8 = bool(cfg.get("fp8"))
     nrows = args.cpu_rows or {"tiny": 64, "prefill8k": 8, "decode64": 1, "chunked": 4,
-                              "decode1m": 1}[args.workload]
+                              "decode1m": 1, "prefill2k": 8, "decode8": 1}[args.workload]
     sub, rows, host = reference_inputs(lay, cfg, fp8, nrows)
     for _ in range(args.warmup):
         run_oracle(sub, host, rows, cfg, fp8)

@@ -11,8 +11,9 @@
 // reduces over heads with ReLU and the head weights thread-locally (no
 // shuffles) and writes a coalesced row segment of scores per token.
 //
-// Warp roles (192 threads): warps 0-3 epilogue (thread = TMEM lane = key),
-// warp 4 TMA producer, warp 5 MMA issuer (and TMEM owner).  The key tiles
+// Warp roles: epilogue warps first (thread = TMEM lane = key; 8 warps, two
+// per lane quarter splitting the tokens, when a tile holds 8 tokens; 4 for
+// decode), then one TMA producer warp and one MMA issuer warp (TMEM owner).  The key tiles
 // stream through a STAGES-deep shared-memory ring; the accumulator is double
 // buffered in TMEM so the epilogue of tile i overlaps the MMAs of tile i+1.
 #include "common.cuh"
@@ -23,6 +24,11 @@ namespace {
 template <int NTOK, bool FP8, int STAGES>
 struct IdxCfg {
   static constexpr int N = NTOK * 32;                // MMA N: (token, head) pairs
+  // epilogue warps: two per TMEM lane quarter (each takes half of the tokens)
+  // when a tile holds several tokens, one per quarter otherwise
+  static constexpr int NEPI = NTOK >= 2 ? 8 : 4;
+  static constexpr int TOK_PER_WARP = NTOK * 4 / NEPI;
+  static constexpr int NT = NEPI * 32 + 64;          // + TMA producer warp + MMA warp
   static constexpr int KSUB = FP8 ? 1 : 2;           // 128-byte swizzle atoms per 128-d row
   static constexpr int Q_SUB = N * 128;              // bytes of one Q sub-tile
   static constexpr int Q_BYTES = KSUB * Q_SUB;
@@ -71,10 +77,11 @@ __device__ __forceinline__ void tmem_wait_ld_dep(float (&v)[32]) {
 }
 
 template <int NTOK, bool FP8, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap, const IndexerParams p) {
   using C = IdxCfg<NTOK, FP8, STAGES>;
+  constexpr int W_PROD = C::NEPI, W_MMA = C::NEPI + 1, NEPT = C::NEPI * 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(192, 1)
     const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     for (int n = 0; n < nq; ++n) {
       float* row = p.scores + static_cast<int64_t>(q0 + n) * p.b.max_len;
-      for (int s = f0 + tid * 4; s < s_stop; s += 192 * 4)
+      for (int s = f0 + tid * 4; s < s_stop; s += C::NT * 4)
         *reinterpret_cast<float4*>(row + s) = ninf;
     }
   }
@@ -132,17 +139,17 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(B_ACCF + a), 1);
-      mbar_init(bar(B_ACCE + a), 128);
+      mbar_init(bar(B_ACCE + a), NEPT);
     }
     mbar_init(bar(B_DONE), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (tid < 128) {
-    for (int i = tid; i < C::N; i += 128) {
+  if (tid < NEPT) {
+    for (int i = tid; i < C::N; i += NEPT) {
       const int n = i >> 5, j = i & 31;
       float v = 0.f;
       if (n < nq) {
@@ -152,7 +159,7 @@ __global__ void __launch_bounds__(192, 1)
       sW[i] = v;
     }
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == W_PROD && lane == 0) {
     tma_prefetch_desc(&qmap);
     tma_prefetch_desc(&kmap);
   }
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint64_t to = p.timeout_ns;
   volatile int no_abort = 0;
 
-  if (warp == 4) {
+  if (warp == W_PROD) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(B_QFULL), C::Q_BYTES);
@@ -189,7 +196,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait(bar(B_KFULL + i % STAGES), (i / STAGES) & 1, &no_abort, nullptr, to);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == W_MMA) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = FP8 ? idesc_e4m3(128, C::N) : idesc_bf16(128, C::N, false, false);
@@ -221,19 +228,28 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------ epilogue: ReLU . w over heads
-    const uint32_t lane_base = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+    // warp w reads TMEM lane quarter (w & 3), i.e. keys 32*(w & 3) + lane of
+    // the tile, for tokens [(w >> 2) * TOK_PER_WARP, +TOK_PER_WARP)
+    const int quarter = warp & 3;
+    const int n0 = (warp >> 2) * C::TOK_PER_WARP;
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     for (int i = 0; i < nkb; ++i) {
       const int acc = i & 1;
       if (!mbar_wait(bar(B_ACCF + acc), (i >> 1) & 1, abort_flag, p.status, to)) break;
       tc_fence_after();
-      const int s = s_begin + i * 128 + tid;
+      const int s = s_begin + i * 128 + quarter * 32 + lane;
       float kscale = 1.f;
       if (FP8) {
         const int64_t kr = row0 + s;
         kscale = kr < p.k_rows ? p.k_scale[kr] : 0.f;
       }
 #pragma unroll
-      for (int n = 0; n < NTOK; ++n) {
+      for (int nn = 0; nn < C::TOK_PER_WARP; ++nn) {
+        const int n = n0 + nn;
+        int pn = -1;  // pos[n] without dynamic indexing (keeps pos[] in registers)
+#pragma unroll
+        for (int k = 0; k < NTOK; ++k)
+          if (k == n) pn = pos[k];
         float v[32];
         tmem_ld32(lane_base + acc * C::N + n * 32, v);
         tmem_wait_ld_dep(v);
@@ -250,7 +266,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           float sc = (a0 + a1) + (a2 + a3);
           if (FP8) sc *= kscale;
-          if (s > pos[n]) sc = -INFINITY;
+          if (s > pn) sc = -INFINITY;
           p.scores[static_cast<int64_t>(q0 + n) * p.b.max_len + s] = sc;
         }
       }
@@ -260,7 +276,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }
@@ -284,7 +300,7 @@ cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, Indexer
   dim3 grid(static_cast<unsigned>(p.num_qb) * static_cast<unsigned>(p.num_kc),
             static_cast<unsigned>(p.b.num_seqs));
   prof_begin(stream);
-  kern<<<grid, 192, C::SMEM, stream>>>(qmap, kmap, p);
+  kern<<<grid, C::NT, C::SMEM, stream>>>(qmap, kmap, p);
   prof_end(kLaunchIndexer, stream);
   count_launch(kLaunchIndexer);
   return cudaGetLastError();

@@ -10,7 +10,8 @@
 // `need` lowest positions equal to it, in ascending order, independent of
 // thread scheduling.
 //
-// A row is handled by a cluster of CL CTAs, each owning a contiguous slice;
+// A row is handled by one CTA, or by a cluster of CL CTAs each owning a
+// contiguous slice that it may stage in shared memory once;
 // per-pass histograms and slice counts are merged through distributed
 // shared memory, so long rows (128K..1M) spread over several SMs without any
 // global atomics or spin-waits.
@@ -18,6 +19,9 @@
 
 namespace dsa {
 namespace {
+
+constexpr int kStageMax = 18432;                 // positions staged per CTA
+constexpr int kStageBytesMax = kStageMax * 4;    // 72 KB of shared memory
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x);
@@ -52,9 +56,13 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int* total
   return before + x - v;
 }
 
-template <int CL, int BS>
+// STAGE: the CTA's slice of the row is read from global memory once, as
+// order keys into shared memory, and every pass runs from there; otherwise
+// each pass re-reads the slice from global memory (L2).
+template <int CL, int BS, bool STAGE>
 __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scores, BatchArgs b,
                                                   int K, int32_t* __restrict__ idx, int* status) {
+  extern __shared__ uint32_t skeys[];
   __shared__ int hist[2048];
   __shared__ int tot[CL > 1 ? 2048 : 1];
   __shared__ int warp_sums[32];
@@ -75,6 +83,20 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
   const int lo = min(rank * chunk, len);
   const int hi = min(lo + chunk, len);
   const int hi4 = lo + ((hi - lo) & ~3);
+  if constexpr (STAGE) {
+    for (int s = lo + tid * 4; s < hi4; s += BS * 4) {
+      const float4 v = *reinterpret_cast<const float4*>(row + s);
+      *reinterpret_cast<uint4*>(skeys + (s - lo)) =
+          make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+    }
+    for (int s = hi4 + tid; s < hi; s += BS) skeys[s - lo] = order_key(row[s]);
+    __syncthreads();
+  }
+  // order key of position s of this CTA's slice
+  auto key_at = [&](int s) -> uint32_t {
+    if constexpr (STAGE) return skeys[s - lo];
+    else return order_key(row[s]);
+  };
 
   uint32_t prefix = 0;
   int need = K;
@@ -85,19 +107,24 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
     const int nbins = 1 << bits;
     for (int i = tid; i < nbins; i += BS) hist[i] = 0;
     __syncthreads();
-    auto add = [&](float x) {
-      const uint32_t k = order_key(x);
+    auto add = [&](uint32_t k) {
       if (pass == 0 || (k >> (shift + bits)) == prefix)
         atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1);
     };
     for (int s = lo + tid * 4; s < hi4; s += BS * 4) {
-      const float4 v = *reinterpret_cast<const float4*>(row + s);
-      add(v.x);
-      add(v.y);
-      add(v.z);
-      add(v.w);
+      uint4 k4;
+      if constexpr (STAGE) {
+        k4 = *reinterpret_cast<const uint4*>(skeys + (s - lo));
+      } else {
+        const float4 v = *reinterpret_cast<const float4*>(row + s);
+        k4 = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+      }
+      add(k4.x);
+      add(k4.y);
+      add(k4.z);
+      add(k4.w);
     }
-    for (int s = hi4 + tid; s < hi; s += BS) add(row[s]);
+    for (int s = hi4 + tid; s < hi; s += BS) add(key_at(s));
     __syncthreads();
     const int* cnt = hist;
     if constexpr (CL > 1) {
@@ -142,7 +169,7 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
   // ---- slice counts, cluster prefix
   int cg = 0, ce = 0;
   for (int s = lo + tid; s < hi; s += BS) {
-    const uint32_t k = order_key(row[s]);
+    const uint32_t k = key_at(s);
     cg += k > thr;
     ce += k == thr;
   }
@@ -171,7 +198,7 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
     int ng = 0, ne = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      k4[q] = (s0 + q < hi) ? order_key(row[s0 + q]) : 0u;
+      k4[q] = (s0 + q < hi) ? key_at(s0 + q) : 0u;
       const bool in = s0 + q < hi;
       ng += in && k4[q] > thr;
       ne += in && k4[q] == thr;
@@ -198,14 +225,25 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
   if constexpr (CL > 1) cluster_sync();  // keep s_cnt alive until every rank has read it
 }
 
-template <int CL, int BS>
+template <int CL, int BS, bool STAGE>
 cudaError_t launch_cl(const float* scores, const dsa_batch_t& b, int k, int32_t* idx, int* status,
-                      cudaStream_t stream) {
-  auto* kern = topk_kernel<CL, BS>;
+                      size_t smem, cudaStream_t stream) {
+  auto* kern = topk_kernel<CL, BS, STAGE>;
+  if (STAGE) {
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytesMax);
+      if (e != cudaSuccess) return e;
+      configured_device = dev;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(CL) * static_cast<unsigned>(b.num_q));
   cfg.blockDim = dim3(BS);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = STAGE ? smem : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -226,20 +264,18 @@ cudaError_t launch_cl(const float* scores, const dsa_batch_t& b, int k, int32_t*
 cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_t* idx,
                         int* status, cudaStream_t stream) {
   if (b.num_q == 0) return cudaSuccess;
-  // Enough CTAs to cover the SMs, but at least ~8K positions per CTA.
-  int cl = 1;
-  while (cl < 8 && static_cast<int64_t>(b.num_q) * cl < 2 * 152 &&
-         static_cast<int64_t>(b.max_len) / (cl * 2) >= 8192)
-    cl *= 2;
-  if (cl == 1) {
-    return b.max_len > 16384 ? launch_cl<1, 1024>(scores, b, k, idx, status, stream)
-                             : launch_cl<1, 256>(scores, b, k, idx, status, stream);
+  // Many rows (prefill, chunked prefill): one CTA per row, its row re-read
+  // from L2 per pass (rows up to 16K positions use 256 threads, longer ones
+  // 1024).  Few rows (decode): a cluster of 8 CTAs per row, each staging its
+  // slice in shared memory once; 1M-position rows, whose slices exceed the
+  // staging buffer, make their passes over L2.
+  if (static_cast<int64_t>(b.num_q) >= 2 * 152) {
+    return b.max_len <= 16384 ? launch_cl<1, 256, false>(scores, b, k, idx, status, 0, stream)
+                              : launch_cl<1, 1024, false>(scores, b, k, idx, status, 0, stream);
   }
-  switch (cl) {
-    case 2: return launch_cl<2, 1024>(scores, b, k, idx, status, stream);
-    case 4: return launch_cl<4, 1024>(scores, b, k, idx, status, stream);
-    default: return launch_cl<8, 1024>(scores, b, k, idx, status, stream);
-  }
+  const int64_t slice = ((b.max_len + 7) / 8 + 3) & ~3;
+  if (slice > kStageMax) return launch_cl<8, 1024, false>(scores, b, k, idx, status, 0, stream);
+  return launch_cl<8, 1024, true>(scores, b, k, idx, status, static_cast<size_t>(slice) * 4, stream);
 }
 
 }  // namespace dsa

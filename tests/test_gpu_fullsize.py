@@ -1,0 +1,145 @@
+"""Full-size parity in the launch configuration the benchmark times.
+
+Each workload is built exactly as bench.py builds it (seeded device inputs,
+one indexshare_group_forward call) and sampled query rows are recomputed by
+the oracle from host copies of the same inputs:
+
+* indices (Gaussian scores): the GPU set may differ from the oracle's only at
+  positions whose oracle score lies within 1e-3 of the K-th score;
+* attention outputs: within 2e-2 * max|ref| for rows whose index set equals
+  the oracle's (a near-tie swap changes the sparse set, and with it the
+  output, legitimately; such rows are validated through their index set);
+* sparse MLA alone: the oracle's own index rows are fed to the GPU kernel for
+  the sampled rows, and the outputs must agree within the same bound;
+* FP8 variant: the library quantiser's codes must equal the oracle's.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from gpu_helpers import assert_close, assert_topk_within_band, bits  # noqa: E402
+
+dsa = pytest.importorskip("dsa_indexer_indexshare_gb300")
+DEV = torch.device("cuda:0")
+SCALE = 1 / 16
+
+
+def _host_inputs(lay, layers, rows, fp8):
+    """Host copies for the sampled rows: query tensors of those rows, and the
+    cache rows of the sequences they belong to, re-based into a compact host
+    cache.  Returns (host layers, row_pos, row_key0 into the compact cache)."""
+    rows = np.asarray(rows, np.int64)
+    seq = np.searchsorted(lay.q_start, rows, side="right") - 1
+    useq = sorted(set(seq.tolist()))
+    spans, base = {}, 0
+    for b in useq:
+        n = int(lay.q_pos[lay.q_start[b + 1] - 1]) + 1
+        spans[b] = (int(lay.seq_row0[b]), n, base)
+        base += n
+    pos = lay.q_pos[rows].astype(np.int32)
+    key0 = np.array([spans[b][2] for b in seq], np.int64)
+    rt = torch.as_tensor(rows, device=DEV)
+
+    def cache(t):
+        parts = [t[r0:r0 + n] for (r0, n, _) in (spans[b] for b in useq)]
+        return torch.cat(parts).contiguous()
+
+    host = []
+    for L in layers:
+        d = {"q_lat": bits(L["q_lat"].index_select(0, rt)),
+             "q_rope": bits(L["q_rope"].index_select(0, rt)), "kv": bits(cache(L["kv"]))}
+        if "q_idx" in L:
+            d["w"] = L["w"].index_select(0, rt).cpu().numpy()
+            if fp8:
+                # the oracle quantises the bf16 indexer inputs itself
+                d["q_bf16"] = bits(L["q_idx_bf16"].index_select(0, rt))
+                d["k_bf16"] = bits(cache(L["k_idx_bf16"]))
+                qc, qs = oracle.fp8_quantize_rows(d["q_bf16"].reshape(-1, 128))
+                kc, ks = oracle.fp8_quantize_rows(d["k_bf16"])
+                d.update(q_idx=qc.reshape(len(rows), 32, 128), q_scale=qs.reshape(len(rows), 32),
+                         k_idx=kc, k_scale=ks)
+                # the library's codes for the same rows must be the oracle's
+                assert np.array_equal(L["q_idx"].index_select(0, rt).cpu().numpy(), d["q_idx"])
+                assert np.array_equal(cache(L["k_idx"]).cpu().numpy(), kc)
+                assert np.array_equal(cache(L["k_scale"]).cpu().numpy(), ks)
+            else:
+                d["q_idx"] = bits(L["q_idx"].index_select(0, rt))
+                d["k_idx"] = bits(cache(L["k_idx"]))
+        host.append(d)
+    return host, pos, key0
+
+
+def _run(name, sample):
+    cfg = dict(synth.WORKLOADS[name])
+    lay = synth.workload_layout(name)
+    types, H, K = cfg["layers"], cfg["H"], cfg["K"]
+    fp8 = bool(cfg.get("fp8"))
+    layers = synth.device_layers(lay, types, H, device=DEV, seed=0)
+    if fp8:
+        for L in layers:
+            if "q_idx" in L:
+                L["q_idx_bf16"], L["k_idx_bf16"] = L["q_idx"], L["k_idx"]
+                qc, qs = dsa.dsa_fp8_quantize(L["q_idx"])
+                kc, ks = dsa.dsa_fp8_quantize(L["k_idx"])
+                L.update(q_idx=qc, q_scale=qs, k_idx=kc, k_scale=ks)
+    batch = dsa.Batch(lay.q_start, lay.q_pos, lay.seq_row0, lay.max_len, device=DEV)
+    rows = np.array(sorted(set(r for r in sample if 0 <= r < lay.num_q)), np.int64)
+    host, pos, key0 = _host_inputs(lay, layers, rows, fp8)
+
+    # the oracle: whole group on the sampled rows, scores kept for the band test
+    ref = oracle.group_forward(types, host, np.arange(len(rows), dtype=np.int32), pos, key0,
+                               lay.max_len, K, SCALE, idx_dtype=1 if fp8 else 0, keep_scores=True)
+    lens = pos.astype(np.int64) + 1
+    f_layers = [l for l, c in enumerate(types) if c == "F"]
+
+    # the GPU: each F-led group of layers as the benchmark runs it
+    starts = f_layers + [len(types)]
+    for gi in range(len(f_layers)):
+        lo, hi = starts[gi], starts[gi + 1]
+        sub = types[lo:hi]
+        group = dsa.Group(sub, layers[lo:hi], k=K, scale=SCALE)
+        ws = dsa.workspace(group.workspace_size(batch), DEV)
+        outs, _, idx = dsa.indexshare_group_forward(group, batch, ws=ws)
+        torch.cuda.synchronize()
+        dsa.status_fetch(ws)
+        got_idx = idx.index_select(0, torch.as_tensor(rows, device=DEV)).cpu().numpy()
+        assert_topk_within_band(got_idx, ref["scores"][gi], lens, K, what=f"{name} F layer {lo}")
+        same = np.array([np.array_equal(got_idx[i], ref["idx"][lo][i]) for i in range(len(rows))])
+        for l in range(lo, hi):
+            if not same.any():
+                break
+            got = outs[l - lo].index_select(0, torch.as_tensor(rows[same], device=DEV))
+            assert_close(got.float().cpu().numpy(), ref["out"][l][same], 2e-2, f"{name} layer {l}")
+
+        # sparse MLA alone with the oracle's indices in the sampled rows
+        idx_in = idx.clone()
+        idx_in[torch.as_tensor(rows, device=DEV)] = torch.from_numpy(ref["idx"][lo]).to(DEV)
+        o, lse = dsa.dsa_sparse_mla_attn(layers[lo]["q_lat"], layers[lo]["q_rope"], layers[lo]["kv"],
+                                         idx_in, batch, scale=SCALE)
+        o = o.index_select(0, torch.as_tensor(rows, device=DEV)).float().cpu().numpy()
+        assert_close(o, ref["out"][lo], 2e-2, f"{name} sparse MLA layer {lo}")
+        lse = lse.index_select(0, torch.as_tensor(rows, device=DEV)).cpu().numpy()
+        assert np.allclose(lse, ref["lse"][lo], rtol=0, atol=1e-3 * max(1.0, np.abs(ref["lse"][lo]).max()))
+        del group, ws, outs, idx, idx_in
+    del layers
+    torch.cuda.empty_cache()
+
+
+def test_prefill8k_full_size():
+    _run("prefill8k", [0, 1, 2046, 2047, 2048, 5000, 8191])
+
+
+def test_decode64_full_size():
+    _run("decode64", [0, 17, 40, 63])
+
+
+def test_chunked_full_size():
+    _run("chunked", [0, 1, 2047, 4095])
+
+
+def test_decode1m_fp8_full_size():
+    _run("decode1m", [2])
