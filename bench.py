@@ -47,7 +47,11 @@ DESCR = {
 }
 # ncu DRAM traffic of the dominant kernel (bytes per launch), with the hash of
 # the kernel sources it was measured on; ignored once the sources change.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch, scaled by
+    # tokens to the 8192-token launch (q/out traffic is per token; the kv cache is a few MB)
+    "sparse_mla": {"bytes": 1.0577e+09, "workload": "prefill8k", "src": "4c89d053fc2c247b"},
+}
 
 
 def kernel_src_hash(files):
