@@ -35,7 +35,7 @@ def make_batch(dsa, lay, dev):
 
 
 def assert_close(got, ref, rel, what=""):
-    """max |got - ref| <= rel * max |ref| (the spec attention bound)."""
+    """max |got - ref| <= rel * max |ref| (the bound used for attention outputs)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     scale = np.abs(ref).max()
@@ -47,7 +47,7 @@ def assert_close(got, ref, rel, what=""):
 def assert_topk_within_band(got_idx, scores, lens, K, rel=1e-3, what=""):
     """Top-K parity on real-valued scores: the GPU set may differ from the
     exact set only at positions whose exact score lies within rel * |I_K| of
-    the K-th largest exact score I_K (spec tolerance).  scores are the
+    the K-th largest exact score I_K (the tie band).  scores are the
     oracle's fp64 scores of the same rows."""
     got_idx = np.asarray(got_idx)
     for i in range(got_idx.shape[0]):

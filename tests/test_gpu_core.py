@@ -1,6 +1,6 @@
 """GPU parity of each hot-path step against the oracle, through the C ABI.
 
-Bars (the benchmark spec): integer-valued inputs give bit-exact scores and index
+Bars: integer-valued inputs give bit-exact scores and index
 sets; Gaussian inputs give index sets that differ only within 1e-3 of the
 K-th score; attention outputs within 2e-2 * max|ref| (bf16)."""
 import numpy as np
