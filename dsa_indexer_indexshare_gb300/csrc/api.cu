@@ -271,7 +271,10 @@ dsa_status_t dsa_indexer_scores(const void* q_idx, const float* q_scale, const f
 }
 
 // ------------------------------------------------------------- a2: top-K
-size_t dsa_topk_workspace_size(const dsa_batch_t*, int32_t) { return kStatusBytes; }
+size_t dsa_topk_workspace_size(const dsa_batch_t* b, int32_t k) {
+  if (!b) return kStatusBytes;
+  return kStatusBytes + round256(topk_scratch_bytes(*b, k));
+}
 
 dsa_status_t dsa_topk(const float* scores, const dsa_batch_t* b, int32_t k, int32_t* idx, void* ws,
                       size_t ws_bytes, dsa_stream_t stream) {
@@ -279,8 +282,12 @@ dsa_status_t dsa_topk(const float* scores, const dsa_batch_t* b, int32_t k, int3
   if (k < 1 || k > 4096) return fail(DSA_ERR_UNSUPPORTED, "k=%d (supported: 1..4096)", k);
   if (!scores || !idx) return fail(DSA_ERR_INVALID_ARG, "scores and idx are required");
   if (!aligned16(scores)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
-  if (dsa_status_t s = check_ws(ws, ws_bytes, kStatusBytes)) return s;
-  return launch_status(launch_topk(scores, *b, k, idx, static_cast<int*>(ws), stream), "top-K launch");
+  const size_t need = dsa_topk_workspace_size(b, k);
+  if (dsa_status_t s = check_ws(ws, ws_bytes, need)) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  return launch_status(launch_topk(scores, *b, k, idx, static_cast<int*>(ws), wsb + kStatusBytes,
+                                   need - kStatusBytes, stream),
+                       "top-K launch");
 }
 
 // ------------------------------------------------------------- a4-a5: sparse MLA
@@ -307,7 +314,8 @@ dsa_status_t dsa_sparse_mla_attn(const void* q_lat, const void* q_rope, const vo
 // ------------------------------------------------------------- a6: group
 size_t dsa_group_workspace_size(const dsa_group_t* g, const dsa_batch_t* b) {
   if (!g || !b) return kStatusBytes;
-  const size_t scores = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4);
+  const size_t scores = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4) +
+                        round256(topk_scratch_bytes(*b, g->k));
   const size_t mla = round256(mla_workspace_bytes(*b, g->heads, g->k));
   return kStatusBytes + (scores > mla ? scores : mla);
 }
@@ -345,6 +353,9 @@ dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   int* status = static_cast<int*>(ws);
   float* scores = reinterpret_cast<float*>(wsb + kStatusBytes);
+  const size_t score_bytes = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4);
+  uint8_t* topk_scratch = wsb + kStatusBytes + score_bytes;
+  const size_t topk_bytes = round256(topk_scratch_bytes(*b, g->k));
   const bool fp8 = g->idx_dtype == DSA_FP8_E4M3;
   for (int l = 0; l < nl; ++l) {
     if (g->layer_types[l] == 'F') {
@@ -355,7 +366,8 @@ dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b
                              status, stream),
               "indexer launch"))
         return s;
-      if (dsa_status_t s = launch_status(launch_topk(scores, *b, g->k, idx_buf, status, stream),
+      if (dsa_status_t s = launch_status(launch_topk(scores, *b, g->k, idx_buf, status,
+                                                     topk_scratch, topk_bytes, stream),
                                          "top-K launch"))
         return s;
     }

@@ -63,8 +63,9 @@ cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float*
                            const void* k_idx, const float* k_scale, int64_t k_rows, bool fp8,
                            const dsa_batch_t& b, float* scores, bool fill_tail, int* status,
                            cudaStream_t stream);
+size_t topk_scratch_bytes(const dsa_batch_t& b, int k);
 cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_t* idx,
-                        int* status, cudaStream_t stream);
+                        int* status, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 size_t mla_workspace_bytes(const dsa_batch_t& b, int heads, int k);
 cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void* kv,
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,

@@ -19,6 +19,8 @@ namespace dsa {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+// the last 16 MiB hold the top-K scratch of decode-sized batches
+constexpr size_t kNoAllocTopkBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -65,9 +67,11 @@ extern "C" DSA_API dsa_status_t dsa_indexer_topk_noalloc(
     return DSA_ERR_INVALID_ARG;
   if (k_rows < 1 || k_rows > (int64_t(1) << 31) - 1) return DSA_ERR_INVALID_ARG;
   if (k < 1 || k > 4096) return DSA_ERR_UNSUPPORTED;
-  // The score matrix must fit the fixed array after the status block.
+  // The score matrix must fit the fixed array after the status block, and
+  // the top-K scratch its reserved tail.
   const size_t need = static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4;
-  if (need > kNoAllocScratchBytes - kStatusBytes) return DSA_ERR_WORKSPACE;
+  if (need > kNoAllocScratchBytes - kNoAllocTopkBytes - kStatusBytes) return DSA_ERR_WORKSPACE;
+  if (topk_scratch_bytes(*b, k) > kNoAllocTopkBytes) return DSA_ERR_WORKSPACE;
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return DSA_ERR_CUDA;
   int* status = static_cast<int*>(base);
@@ -79,7 +83,11 @@ extern "C" DSA_API dsa_status_t dsa_indexer_topk_noalloc(
     if (launch_indexer(q_idx, q_scale, w, k_idx, k_scale, k_rows, dt == DSA_FP8_E4M3, *b, scores,
                        false, status, stream) != cudaSuccess)
       return DSA_ERR_CUDA;
-    if (launch_topk(scores, *b, k, idx, status, stream) != cudaSuccess) return DSA_ERR_CUDA;
+    unsigned char* topk_scratch =
+        static_cast<unsigned char*>(base) + kNoAllocScratchBytes - kNoAllocTopkBytes;
+    if (launch_topk(scores, *b, k, idx, status, topk_scratch, kNoAllocTopkBytes, stream) !=
+        cudaSuccess)
+      return DSA_ERR_CUDA;
   }
   if (d_status_out &&
       cudaMemcpyAsync(d_status_out, status, sizeof(int), cudaMemcpyDeviceToDevice, stream) !=

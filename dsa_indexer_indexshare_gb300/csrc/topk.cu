@@ -11,7 +11,8 @@
 // thread scheduling.
 //
 // A row is handled by one CTA, or by a cluster of CL CTAs each owning a
-// contiguous slice that it may stage in shared memory once;
+// contiguous slice that it stages in shared memory once (few rows of up to
+// 16K positions), or, for few long rows, by the three-launch path below;
 // per-pass histograms and slice counts are merged through distributed
 // shared memory, so long rows (128K..1M) spread over several SMs without any
 // global atomics or spin-waits.
@@ -225,6 +226,355 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
   if constexpr (CL > 1) cluster_sync();  // keep s_cnt alive until every rank has read it
 }
 
+
+// ------------------------------------------------------------------ long rows
+// Few long rows (decode): three launches, no inter-CTA waits.
+//  1. hist:   each CTA adds a 12-bit histogram of its slice of a row into the
+//             row's global histogram.
+//  2. select: every CTA of the row finds the threshold bin b1 (the bin that
+//             holds the k-th largest key) from that histogram, writes every
+//             position of a higher bin straight to the output row and
+//             appends the positions of bin b1 (the candidates) to a per-row
+//             list of up to kCandCap entries.
+//  3. finish: one CTA per row selects the remaining `need` positions among
+//             the candidates (radix on the low 20 key bits, ties to the lower
+//             position), then sorts the row's k positions ascending.  A row
+//             whose candidate list overflowed rescans its scores instead.
+constexpr int kHBits = 12;
+constexpr int kHBins = 1 << kHBits;   // 4096 bins over key bits [31:20]
+constexpr int kCandCap = 8192;        // candidates kept per row
+constexpr int kLongBS = 512;
+constexpr int kFinBS = 512;
+constexpr int kFinDynBytes = 2 * kCandCap * 4;  // candidate keys + positions (64 KB)
+constexpr int kLocalCand = 2048;                 // candidates buffered per select CTA
+
+struct LongScratch {
+  uint32_t* hist;  // [num_q][kHBins]
+  int* cnt;        // [num_q][4]: written-above, candidates, b1, above-count
+  int32_t* cand;   // [num_q][kCandCap]
+};
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Slice [lo, hi) of a row of length len for CTA c of `split`.
+__device__ __forceinline__ void slice_of(int len, int split, int c, int& lo, int& hi) {
+  const int chunk = (((len + split - 1) / split) + 3) & ~3;
+  lo = min(c * chunk, len);
+  hi = min(lo + chunk, len);
+}
+
+__global__ void __launch_bounds__(kLongBS) topk_hist_kernel(const float* __restrict__ scores,
+                                                            BatchArgs b, int K, int split,
+                                                            LongScratch ws) {
+  __shared__ uint32_t h[kHBins];
+  const int t = blockIdx.y, tid = threadIdx.x;
+  const int pos = query_pos(b, t, nullptr);
+  if (pos + 1 <= K) return;
+  int lo, hi;
+  slice_of(pos + 1, split, blockIdx.x, lo, hi);
+  if (lo >= hi) return;
+  for (int i = tid; i < kHBins; i += kLongBS) h[i] = 0;
+  __syncthreads();
+  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
+  const int hi4 = lo + ((hi - lo) & ~3);
+  for (int s = lo + tid * 4; s < hi4; s += kLongBS * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(row + s);
+    atomicAdd(&h[order_key(v.x) >> 20], 1u);
+    atomicAdd(&h[order_key(v.y) >> 20], 1u);
+    atomicAdd(&h[order_key(v.z) >> 20], 1u);
+    atomicAdd(&h[order_key(v.w) >> 20], 1u);
+  }
+  for (int s = hi4 + tid; s < hi; s += kLongBS) atomicAdd(&h[order_key(row[s]) >> 20], 1u);
+  __syncthreads();
+  uint32_t* g = ws.hist + static_cast<int64_t>(t) * kHBins;
+  for (int i = tid; i < kHBins; i += kLongBS)
+    if (h[i]) atomicAdd(&g[i], h[i]);
+}
+
+// Threshold bin of a row from its histogram: the bin d with
+// count(bins > d) < K <= count(bins >= d).  Result in *d, *above.
+template <int BS>
+__device__ void threshold_bin(const uint32_t* hist, int K, int* warp_sums, int* s_d, int* s_above) {
+  constexpr int per = kHBins / BS;
+  const int tid = threadIdx.x;
+  int local = 0;
+#pragma unroll
+  for (int k = 0; k < per; ++k) local += static_cast<int>(hist[kHBins - 1 - (tid * per + k)]);
+  int total;
+  int running = block_excl_scan<BS>(local, warp_sums, &total);
+#pragma unroll
+  for (int k = 0; k < per; ++k) {
+    const int bb = kHBins - 1 - (tid * per + k);
+    const int c = static_cast<int>(hist[bb]);
+    if (running < K && running + c >= K) {
+      *s_d = bb;
+      *s_above = running;
+    }
+    running += c;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kLongBS) topk_select_kernel(const float* __restrict__ scores,
+                                                              BatchArgs b, int K, int split,
+                                                              LongScratch ws, int32_t* idx) {
+  __shared__ uint32_t h[kHBins];
+  __shared__ int warp_sums[32];
+  __shared__ int s_b1, s_above;
+  const int t = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+  const int pos = query_pos(b, t, nullptr);
+  if (pos + 1 <= K) return;
+  int lo, hi;
+  slice_of(pos + 1, split, blockIdx.x, lo, hi);
+  if (lo >= hi) return;
+  const uint32_t* g = ws.hist + static_cast<int64_t>(t) * kHBins;
+  for (int i = tid; i < kHBins; i += kLongBS) h[i] = g[i];
+  __syncthreads();
+  threshold_bin<kLongBS>(h, K, warp_sums, &s_b1, &s_above);
+  const uint32_t b1 = static_cast<uint32_t>(s_b1);
+  int* cnt = ws.cnt + static_cast<int64_t>(t) * 4;
+  if (tid == 0 && blockIdx.x == 0) {
+    cnt[2] = s_b1;
+    cnt[3] = s_above;
+  }
+  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
+  // positions of this slice above the threshold bin (fewer than K in all) and
+  // in it (the candidates) are buffered in shared memory, then appended to
+  // the row's lists with one global atomic each
+  __shared__ int32_t sgt[4096];
+  __shared__ int32_t scand[kLocalCand];
+  __shared__ int s_ng, s_nc, s_bg, s_bc;
+  if (tid == 0) {
+    s_ng = 0;
+    s_nc = 0;
+  }
+  __syncthreads();
+  const int hi4 = lo + ((hi - lo) & ~3);
+  auto visit = [&](int s, uint32_t key) {
+    const uint32_t bin = key >> 20;
+    if (bin > b1) {
+      const int i = atomicAdd(&s_ng, 1);
+      if (i < 4096) sgt[i] = s;
+    } else if (bin == b1) {
+      const int i = atomicAdd(&s_nc, 1);
+      if (i < kLocalCand) scand[i] = s;
+    }
+  };
+  for (int s = lo + tid * 4; s < hi4; s += kLongBS * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(row + s);
+    visit(s, order_key(v.x));
+    visit(s + 1, order_key(v.y));
+    visit(s + 2, order_key(v.z));
+    visit(s + 3, order_key(v.w));
+  }
+  for (int s = hi4 + tid; s < hi; s += kLongBS) visit(s, order_key(row[s]));
+  __syncthreads();
+  if (tid == 0) {
+    s_bg = atomicAdd(&cnt[0], s_ng);
+    // a slice with more candidates than its buffer marks the row as overflowed
+    s_bc = atomicAdd(&cnt[1], s_nc <= kLocalCand ? s_nc : kCandCap + 1);
+  }
+  __syncthreads();
+  int32_t* out = idx + static_cast<int64_t>(t) * K;
+  int32_t* cand = ws.cand + static_cast<int64_t>(t) * kCandCap;
+  const int ng = min(s_ng, 4096), nc = s_nc <= kLocalCand ? s_nc : 0;
+  for (int i = tid; i < ng; i += kLongBS)
+    if (s_bg + i < K) out[s_bg + i] = sgt[i];
+  for (int i = tid; i < nc; i += kLongBS)
+    if (s_bc + i < kCandCap) cand[s_bc + i] = scand[i];
+}
+
+// Radix select inside the finish kernel: among n items (key, position),
+// all with key >> 20 == b1, find the key T of the need-th largest and how
+// many items equal to T are taken (ties to the lower position are resolved
+// afterwards).  get(i) returns the key of item i (or ~0u for a non-member).
+template <typename Get>
+__device__ void select_low_bits(int n, int need, Get get, uint32_t b1, int* hist2, int* warp_sums,
+                                int* s_d, int* s_above, uint32_t* T, int* need_out) {
+  const int tid = threadIdx.x;
+  uint32_t prefix = b1;
+  int rem = need;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0;
+    for (int i = tid; i < 1024; i += kFinBS) hist2[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kFinBS) {
+      const uint32_t k = get(i);
+      if (k != ~0u && (k >> (shift + 10)) == prefix) atomicAdd(&hist2[(k >> shift) & 1023], 1);
+    }
+    __syncthreads();
+    // digit d with count(digits above d) < rem <= count(digits >= d); thread
+    // tid owns digits 1023 - tid*per - k, k < per (top first)
+    constexpr int per = 1024 / kFinBS;
+    int c[per];
+    int local = 0;
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+      c[k] = hist2[1023 - (tid * per + k)];
+      local += c[k];
+    }
+    int total;
+    int run = block_excl_scan<kFinBS>(local, warp_sums, &total);
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+      if (run < rem && run + c[k] >= rem) {
+        *s_d = 1023 - (tid * per + k);
+        *s_above = run;
+      }
+      run += c[k];
+    }
+    __syncthreads();
+    rem -= *s_above;
+    prefix = (prefix << 10) | static_cast<uint32_t>(*s_d);
+    __syncthreads();
+  }
+  *T = prefix;
+  *need_out = rem;
+}
+
+__global__ void __launch_bounds__(kFinBS) topk_finish_kernel(const float* __restrict__ scores,
+                                                             BatchArgs b, int K, LongScratch ws,
+                                                             int32_t* idx, int* status) {
+  __shared__ int hist2[2048];
+  __shared__ int warp_sums[32];
+  __shared__ int s_d, s_above, s_n, s_pstar;
+  extern __shared__ uint32_t fin_dyn[];  // kFinDynBytes
+  uint32_t* ckey = fin_dyn;                                        // [kCandCap]
+  int32_t* cpos = reinterpret_cast<int32_t*>(fin_dyn + kCandCap);  // [kCandCap]
+  int32_t* sorted = reinterpret_cast<int32_t*>(fin_dyn);           // [4096], after ckey is done
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int pos = query_pos(b, t, tid == 0 ? status : nullptr);
+  const int len = pos + 1;
+  int32_t* out = idx + static_cast<int64_t>(t) * K;
+  if (len <= K) {
+    for (int j = tid; j < K; j += kFinBS) out[j] = j < len ? j : -1;
+    return;
+  }
+  const int* cnt = ws.cnt + static_cast<int64_t>(t) * 4;
+  const int nabove = cnt[3];            // positions in bins above b1 (already written)
+  const uint32_t b1 = static_cast<uint32_t>(cnt[2]);
+  const int nc = cnt[1];
+  const int need1 = K - nabove;
+  if (tid == 0 && cnt[0] != nabove) atomicOr(status, DSA_DEVERR_BATCH);
+  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
+  const bool fits = nc <= kCandCap;
+  const int n = fits ? nc : len;  // overflow: scan the whole row, members are bin b1
+  if (fits) {
+    const int32_t* cand = ws.cand + static_cast<int64_t>(t) * kCandCap;
+    for (int i = tid; i < nc; i += kFinBS) {
+      const int32_t p = cand[i];
+      cpos[i] = p;
+      ckey[i] = order_key(row[p]);
+    }
+  }
+  __syncthreads();
+  auto get_key = [&](int i) -> uint32_t {
+    if (fits) return ckey[i];
+    const uint32_t k = order_key(row[i]);
+    return (k >> 20) == b1 ? k : ~0u;
+  };
+  auto get_pos = [&](int i) -> int { return fits ? cpos[i] : i; };
+  uint32_t T;
+  int need;
+  select_low_bits(n, need1, get_key, b1, hist2, warp_sums, &s_d, &s_above, &T, &need);
+  // items equal to T: take the `need` lowest positions (radix over position
+  // bits [30:20], [19:10], [9:0]) unless every tied item is taken
+  {
+    if (tid == 0) s_n = 0;
+    __syncthreads();
+    int my_eq = 0;
+    for (int i = tid; i < n; i += kFinBS) my_eq += get_key(i) == T;
+    atomicAdd(&s_n, my_eq);
+    __syncthreads();
+    const bool all_ties = s_n == need;
+    __syncthreads();
+    uint32_t pprefix = all_ties ? 0x7fffffffu : 0u;
+    int rem = need;
+#pragma unroll 1
+    for (int pass = 0; pass < (all_ties ? 0 : 3); ++pass) {
+      const int shift = pass == 0 ? 20 : (pass == 1 ? 10 : 0);
+      const int nb = pass == 0 ? 2048 : 1024;
+      for (int i = tid; i < nb; i += kFinBS) hist2[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < n; i += kFinBS) {
+        if (get_key(i) != T) continue;
+        const uint32_t p = static_cast<uint32_t>(get_pos(i));
+        if (pass == 0 || (p >> (shift + 10)) == pprefix) atomicAdd(&hist2[(p >> shift) & (nb - 1)], 1);
+      }
+      __syncthreads();
+      // smallest digit e with count(digits below e) < rem <= count(digits <= e);
+      // thread tid owns digits [tid * per, tid * per + per)
+      const int per = nb / kFinBS;  // 4 or 2
+      int c[4] = {0, 0, 0, 0};
+      int local = 0;
+      for (int k = 0; k < per; ++k) {
+        c[k] = hist2[tid * per + k];
+        local += c[k];
+      }
+      int total;
+      const int below = block_excl_scan<kFinBS>(local, warp_sums, &total);
+      int run = below;
+      for (int k = 0; k < per; ++k) {
+        if (run < rem && run + c[k] >= rem) {
+          s_d = tid * per + k;
+          s_above = run;
+        }
+        run += c[k];
+      }
+      __syncthreads();
+      rem -= s_above;
+      pprefix = (pprefix << (pass == 0 ? 0 : 10)) | static_cast<uint32_t>(s_d);
+      __syncthreads();
+    }
+    if (tid == 0) s_pstar = static_cast<int>(pprefix);  // the need-th lowest tied position
+    if (tid == 0) s_n = nabove;
+    __syncthreads();
+  }
+  const int pstar = s_pstar;
+  for (int i = tid; i < n; i += kFinBS) {
+    const uint32_t k = get_key(i);
+    if (k == ~0u) continue;
+    if (k > T || (k == T && get_pos(i) <= pstar)) {
+      const int slot = atomicAdd(&s_n, 1);
+      if (slot < K) out[slot] = get_pos(i);
+    }
+  }
+  __syncthreads();
+  // ascending order: bitonic sort of the row's K positions (padded to a power of 2)
+  int P = 1;
+  while (P < K) P <<= 1;
+  for (int i = tid; i < P; i += kFinBS) sorted[i] = i < K ? out[i] : 0x7fffffff;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P; i += kFinBS) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & size) == 0;
+          const int a = sorted[i], c = sorted[j];
+          if ((a > c) == up) {
+            sorted[i] = c;
+            sorted[j] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = tid; i < K; i += kFinBS) out[i] = sorted[i];
+}
+
+bool use_long_path(const dsa_batch_t& b) {
+  return static_cast<int64_t>(b.num_q) < 2 * 152 && b.max_len > 16384;
+}
+
+size_t round256z(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 template <int CL, int BS, bool STAGE>
 cudaError_t launch_cl(const float* scores, const dsa_batch_t& b, int k, int32_t* idx, int* status,
                       size_t smem, cudaStream_t stream) {
@@ -261,20 +611,60 @@ cudaError_t launch_cl(const float* scores, const dsa_batch_t& b, int k, int32_t*
 
 }  // namespace
 
+size_t topk_scratch_bytes(const dsa_batch_t& b, int) {
+  if (b.num_q == 0 || !use_long_path(b)) return 0;
+  const size_t q = static_cast<size_t>(b.num_q);
+  return round256z(q * kHBins * 4) + round256z(q * 16) + round256z(q * kCandCap * 4);
+}
+
 cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_t* idx,
-                        int* status, cudaStream_t stream) {
+                        int* status, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   if (b.num_q == 0) return cudaSuccess;
+  if (use_long_path(b)) {
+    if (!scratch || scratch_bytes < topk_scratch_bytes(b, k)) return cudaErrorInvalidValue;
+    const size_t q = static_cast<size_t>(b.num_q);
+    uint8_t* base = static_cast<uint8_t*>(scratch);
+    LongScratch ws;
+    ws.hist = reinterpret_cast<uint32_t*>(base);
+    ws.cnt = reinterpret_cast<int*>(base + round256z(q * kHBins * 4));
+    ws.cand = reinterpret_cast<int32_t*>(base + round256z(q * kHBins * 4) + round256z(q * 16));
+    cudaError_t e = cudaMemsetAsync(base, 0, round256z(q * kHBins * 4) + round256z(q * 16), stream);
+    if (e != cudaSuccess) return e;
+    // CTAs per row: about 4 waves of 152 SMs in all, at least 8K positions each
+    int split = static_cast<int>((4 * 152 + b.num_q - 1) / b.num_q);
+    split = max(1, min(split, (b.max_len + 8191) / 8192));
+    const dim3 grid(static_cast<unsigned>(split), static_cast<unsigned>(b.num_q));
+    const BatchArgs a = to_args(b);
+    prof_begin(stream);
+    topk_hist_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws);
+    topk_select_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws, idx);
+    {
+      static int configured_device = -1;
+      int dev = 0;
+      cudaGetDevice(&dev);
+      if (configured_device != dev) {
+        e = cudaFuncSetAttribute(topk_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kFinDynBytes);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+      }
+    }
+    topk_finish_kernel<<<b.num_q, kFinBS, kFinDynBytes, stream>>>(scores, a, k, ws, idx, status);
+    prof_end(kLaunchTopk, stream);
+    count_launch(kLaunchTopk);
+    count_launch(kLaunchTopk);
+    count_launch(kLaunchTopk);
+    return cudaGetLastError();
+  }
   // Many rows (prefill, chunked prefill): one CTA per row, its row re-read
   // from L2 per pass (rows up to 16K positions use 256 threads, longer ones
-  // 1024).  Few rows (decode): a cluster of 8 CTAs per row, each staging its
-  // slice in shared memory once; 1M-position rows, whose slices exceed the
-  // staging buffer, make their passes over L2.
+  // 1024).  Few short rows: a cluster of 8 CTAs per row, each staging its
+  // slice in shared memory once.
   if (static_cast<int64_t>(b.num_q) >= 2 * 152) {
     return b.max_len <= 16384 ? launch_cl<1, 256, false>(scores, b, k, idx, status, 0, stream)
                               : launch_cl<1, 1024, false>(scores, b, k, idx, status, 0, stream);
   }
   const int64_t slice = ((b.max_len + 7) / 8 + 3) & ~3;
-  if (slice > kStageMax) return launch_cl<8, 1024, false>(scores, b, k, idx, status, 0, stream);
   return launch_cl<8, 1024, true>(scores, b, k, idx, status, static_cast<size_t>(slice) * 4, stream);
 }
 

@@ -173,7 +173,9 @@ DSA_API dsa_status_t dsa_indexer_scores(const void* q_idx, const float* q_scale,
  * q_pos[t] + 1 < k every visible position is taken and the remaining slots
  * are -1.  scores is fp32 [num_q, max_len] (only s <= q_pos[t] is read), idx
  * int32 [num_q, k].  1 <= k <= 4096.  The comparison uses the fp32 bit
- * order (NaN ranks above +inf).  ws: dsa_topk_workspace_size.
+ * order (NaN ranks above +inf).  ws: dsa_topk_workspace_size (the status
+ * block, plus 48 KB of scratch per row for batches of fewer than 304 rows
+ * longer than 16K positions).
  */
 DSA_API size_t dsa_topk_workspace_size(const dsa_batch_t* b, int32_t k);
 DSA_API dsa_status_t dsa_topk(const float* scores, const dsa_batch_t* b, int32_t k, int32_t* idx,
@@ -275,10 +277,10 @@ DSA_API dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* code
  *
  * The fp32 score matrix and the device status word live in a file-scope
  * device array of 64 MiB that every GPU loading this library holds until the
- * process exits.  Limit: num_q * max_len * 4 bytes must not exceed 64 MiB
- * minus 256 bytes (16,777,152 scores, e.g. 64 decode rows of 128K positions
- * or 4 rows of 1M); larger batches return DSA_ERR_WORKSPACE before anything
- * is enqueued.  Arguments, layouts and results are those of
+ * process exits.  Limit: num_q * max_len * 4 bytes must not exceed 48 MiB
+ * minus 256 bytes (12,582,848 scores, e.g. 64 decode rows of 128K positions
+ * or 4 rows of 1M; the last 16 MiB hold top-K scratch); larger batches return
+ * DSA_ERR_WORKSPACE before anything is enqueued.  Arguments, layouts and results are those of
  * dsa_indexer_scores and dsa_topk; idx is int32 [num_q, k].
  *
  * The first call on a device looks up the array's device address with that

@@ -72,7 +72,7 @@ def _topk_case(lens, qcounts, K, values, seed):
         sc = np.zeros((lay.num_q, lay.max_len), np.float32)
     sc[0, : min(5, sc.shape[1])] = -np.inf
     batch = make_batch(dsa, lay, DEV)
-    ws = dsa.workspace(256, DEV)
+    ws = dsa.workspace(dsa.lib.dsa_topk_workspace_size(batch.c, K), DEV)
     got = dsa.dsa_topk(torch.from_numpy(sc).to(DEV), batch, K, ws=ws).cpu().numpy()
     dsa.status_fetch(ws)
     lens_q = lay.q_pos.astype(np.int64) + 1
@@ -87,8 +87,16 @@ def test_topk_bit_exact_short_rows(values):
 
 
 @pytest.mark.parametrize("values", ["ties", "gauss", "const"])
-def test_topk_bit_exact_long_rows_cluster(values):
-    _topk_case([40000, 70001, 131072], [1, 1, 1], 2048, values, 3)  # cluster of 8 per row
+def test_topk_bit_exact_long_rows(values):
+    # few rows beyond 16K positions: histogram / select / finish launches
+    # (constant and 7-valued rows overflow the candidate list and rescan)
+    _topk_case([40000, 70001, 131072], [1, 1, 1], 2048, values, 3)
+    _topk_case([1 << 20, 300000], [1, 1], 2048, values, 4)
+
+
+@pytest.mark.parametrize("values", ["ties", "gauss", "const"])
+def test_topk_bit_exact_few_short_rows_cluster(values):
+    _topk_case([9000, 16000, 3000], [1, 2, 1], 512, values, 5)  # cluster of 8, staged
 
 
 def _mla_case(lens, qcounts, H, K, ints, seed, sample=None, bad_index=False, holes=False):

@@ -55,7 +55,7 @@ def test_noalloc_matches_workspace_entry_points_twice(ints):
 
 
 def test_noalloc_rejects_batches_beyond_the_fixed_array():
-    lay = synth.make_layout([1 << 20] * 17, [1] * 17)   # 17 rows x 1M scores > 64 MiB
+    lay = synth.make_layout([1 << 20] * 17, [1] * 17)   # 17 rows x 1M scores > 48 MiB
     batch = dsa.Batch(lay.q_start, lay.q_pos, lay.seq_row0, lay.max_len, device=DEV)
     L = {"q_idx": torch.zeros((17, 32, 128), dtype=torch.bfloat16, device=DEV),
          "w": torch.zeros((17, 32), device=DEV),
