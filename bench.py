@@ -112,6 +112,25 @@ def kernel_bound(name, work, peaks, fp8):
     return "hbm", peaks["hbm"], "GB/s"
 
 
+# ---------------------------------------------------------------- replicas
+def slowest_rank_ms(ms: float, world: int, device=None) -> float:
+    """The largest of every rank's timed milliseconds (replicas report the
+    slowest rank's time); a no-op for a single process.  Works with the nccl
+    (device tensor) and gloo (host tensor) backends."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_rank_step: int, steps: int, world: int, slowest_ms: float) -> float:
+    """Whole-job query-tokens/s: every replica processes the same workload."""
+    return world * tokens_per_rank_step * steps / (slowest_ms / 1e3)
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -334,13 +353,9 @@ def main():
     launches = sum(dsa.launch_counts().values())
     dsa.status_fetch(ws)
 
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(sum(times), world, dev)
     tokens_per_step = lay.num_q
-    value = world * tokens_per_step * args.steps / (total_ms / 1e3)
+    value = replica_throughput(tokens_per_step, args.steps, world, total_ms)
 
     # ---- per-kernel roofline (live CUDA events around each launch)
     work = algorithmic(lay, cfg, fp8)
@@ -451,13 +466,8 @@ def e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, worl
         step()
     b.record(stream)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(world * lay.num_q * steps / (ms / 1e3), 1), "unit": UNIT,
+    ms = slowest_rank_ms(a.elapsed_time(b), world, dev)
+    return {"value": round(replica_throughput(lay.num_q, steps, world, ms), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms / steps, 3)}
 
