@@ -332,7 +332,7 @@ cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float*
   p.k_rows = k_rows;
   p.scores = scores;
   p.status = status;
-  p.kc_blocks = decode ? 32 : 16;
+  p.kc_blocks = decode ? 32 : 64;  // 128-key tiles per CTA (one Q load per 8K keys)
   p.fill_tail = fill_tail ? 1 : 0;
   p.timeout_ns = wait_timeout_ns();
   if (decode)
