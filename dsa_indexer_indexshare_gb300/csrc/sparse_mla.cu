@@ -14,22 +14,27 @@
 //   S^T[128 keys, H]   = C[128, 576] . Q[H, 576]^T         (A = C, K-major)
 //   O^T[512 dims, H]  += C[128, :512]^T . P^T[H, 128]^T     (A = C^T, MN-major)
 // so both contractions use the full 128-row datapath even with H = 64 (or
-// 16) heads.  The selected rows are gathered by two producer warps with
-// 16-byte cp.async straight into the 128-byte-swizzled MMA operand layout,
-// one 64-column sub-tile at a time (completion tracked on an mbarrier), and
-// each sub-tile is refilled for the next block as soon as the P.V chunk that
-// reads it completes.  (TMA gather4 of 128-byte row segments sustains only
-// about 2 TB/s over the whole chip; cp.async sustains several times that.)  P^T reuses the RoPE
-// sub-tile, which is free once S^T is computed.
+// 16) heads.  The selected rows are gathered with 16-byte cp.async straight
+// into the 128-byte-swizzled MMA operand layout, in four groups of 64-column
+// sub-tiles (completion tracked on one mbarrier per group), and each group is
+// refilled for the next block as soon as the P.V chunk that reads it
+// completes.  (TMA gather4 of 128-byte row segments sustains only about
+// 2 TB/s over the whole chip; cp.async sustains several times that.)  P^T
+// reuses the RoPE sub-tile, which is free once S^T is computed.
 //
 // Softmax: the thread of TMEM lane i owns key i of the block; at H = 64 two
-// warps share each lane quarter, one per half of the heads.  The running maximum per head is only raised when a block
-// exceeds it by more than 2^8 (then O^T and the partial sums are rescaled in
-// place); row sums are kept per thread and reduced once at the end.
+// warps share each lane quarter, one per half of the heads.  The running
+// maximum per head is only raised when a block exceeds it by more than 2^8
+// (then O^T and the partial sums are rescaled in place); row sums are kept
+// per thread and reduced once at the end.
 //
-// Warp roles: softmax / epilogue warps (8 at H = 64, 4 at H = 16), then two
-// producer warps (Q by TMA, gathered rows by cp.async) and one MMA issuer
-// warp (also the TMEM owner).
+// Warp roles: softmax / gather / epilogue warps (8 at H = 64, 4 at H = 16;
+// idle during the products, so they also issue the next block's gathers),
+// then the QK issuer warp (also loads Q by TMA) and the P.V issuer warp
+// (also the TMEM owner).  Issuing the two products from different warps
+// matters: an mbarrier wait in an issuing thread stalls until that thread's
+// queued MMAs have drained, so one issuer waiting for gathered data would
+// empty the tensor pipe every time.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -57,13 +62,12 @@ struct MlaCfg {
   static constexpr int SCR_FLOATS = H + 4 * H + H + 8 * H;
   static constexpr int OFF_FLAGS = OFF_SCR + SCR_FLOATS * 4;
   static constexpr int OFF_BAR = (OFF_FLAGS + 4 * 8 + 7) & ~7;
-  static constexpr int NBAR = 1 + 9 + 4 + 3;
+  static constexpr int NBAR = 1 + 4 + 4 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static constexpr int HW = H > 32 ? 32 : H;       // heads per softmax warp
   static constexpr int NSW = 4 * (H / HW);           // softmax warps (two per lane quarter at H=64)
-  static constexpr int NPW = 2;                      // cp.async producer warps
-  static constexpr int NT = NSW * 32 + NPW * 32 + 32; // + producers + MMA warp
+  static constexpr int NT = NSW * 32 + 64;           // + the QK and the P.V issuer warps
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_S = 0;        // S^T: H columns
   static constexpr uint32_t TM_O = 256;      // O^T chunk c: columns 256 + c*H
@@ -138,7 +142,15 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
                       const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
   using C = MlaCfg<H>;
   constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
-  constexpr int W_PROD = NSW, W_MMA = NSW + C::NPW, NPT = C::NPW * 32;
+  // Two issuer warps: an mbarrier wait in the issuing thread stalls until its
+  // own queued MMAs have drained, so the QK products (which wait for each
+  // gathered group) and the P.V products (which wait for P) come from
+  // different warps and the tensor pipe keeps the other stream's work.
+  constexpr int W_QK = NSW, W_PV = NSW + 1;
+  // gathering: thread g of the softmax warps copies 16-byte chunk (g & 7) of
+  // rows (g >> 3) + GROW * c, c < RPT, of every 64-column sub-tile
+  constexpr int GROW = NST / 8, RPT = 128 / GROW;
+  static_assert(GROW % 8 == 0, "rows of one thread must share the swizzle phase");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -180,24 +192,27 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC + 8);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const int B_Q = 0, B_CFULL = 1, B_CFREE = 10, B_S = 14, B_P = 15, B_O = 16;
+  // CFULL(g) / CFREE(g): gathered group g landed / P.V chunk g done reading it.
+  // Group g = sub-tiles 2g, 2g+1 (group 3 also the RoPE sub-tile 8).
+  const int B_Q = 0, B_CFULL = 1, B_CFREE = 5, B_S = 9, B_P = 10, B_O = 11, B_QD = 12;
 
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(bar(B_Q), 1);
-    for (int i = 0; i < 9; ++i) mbar_init(bar(B_CFULL + i), NPT);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(B_CFULL + i), NST);
     for (int i = 0; i < 4; ++i) mbar_init(bar(B_CFREE + i), 1);
     mbar_init(bar(B_S), 1);
     mbar_init(bar(B_P), NST);
     mbar_init(bar(B_O), 1);
+    mbar_init(bar(B_QD), 1);
     fence_mbar_init();
   }
   if (tid < H) m_used[tid] = -INFINITY;
-  if (warp == W_MMA) {
+  if (warp == W_PV) {
     tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == W_PROD && lane == 0) {
+  if (warp == W_QK && lane == 0) {
     tma_prefetch_desc(&qlat_map);
     tma_prefetch_desc(&qrope_map);
   }
@@ -208,76 +223,45 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   const uint64_t to = p.timeout_ns;
   volatile int no_abort = 0;
 
-  if (warp >= W_PROD && warp < W_MMA) {
-    // ------------------------------------------------ producers: Q once (TMA), gathered C
-    // rows per block with 16-byte cp.async (TMA gather4 of 128-byte row
-    // segments is far slower per SM).  Thread pt copies 16-byte chunk
-    // (pt & 7) of rows (pt >> 3) + 8c, c < 16, of every 64-column sub-tile,
-    // into the 128-byte-swizzled K-major layout the MMA reads.
-    const int pt = tid - NST;
-    if (pt == 0) {
+  if (warp == W_QK) {
+    // ------------------------------------------------ QK issuer: S^T = C . Q^T per block
+    if (lane == 0) {
+      // Q of the token, once, by TMA
       mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
       for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, t * H, bar(B_Q));
       tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, t * H, bar(B_Q));
-    }
-    const int kch = pt & 7, rb = pt >> 3;
-    const uint32_t dst0 = sC + rb * 128 + ((kch ^ rb) << 4);  // row rb + 8c has the same swizzle
-    for (int j = j0; j < j1; ++j) {
-      int rows[16];  // cache rows (< kv_rows < 2^31) of this thread's 16 keys
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int sl = j * 128 + rb + 8 * c;
-        int e = -1;
-        if (sl < nvalid) e = idx_row[sl];
-        const int64_t rr = row0 + e;
-        const bool ok = e >= 0 && e <= pos && rr < p.kv_rows;
-        if (sl < nvalid && !ok && e != -1 && kch == 0) atomicOr(p.status, DSA_DEVERR_INDEX);
-        rows[c] = ok ? static_cast<int>(rr) : 0;
-      }
-      const uint16_t* kvk = p.kv + kch * 8;
-      bool alive = true;
-#pragma unroll 1
-      for (int i = 0; i < 9; ++i) {
-        if (j > j0) {
-          const int chunk = i < 8 ? (i >> 1) : 3;
-          if (!mbar_wait(bar(B_CFREE + chunk), (j - j0 - 1) & 1, abort_flag, p.status, to)) {
-            alive = false;
-            break;
-          }
-        }
-        const uint32_t dst = dst0 + i * C::CSUB;
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + c * 1024),
-                       "l"(kvk + static_cast<int64_t>(rows[c]) * 576 + 64 * i)
-                       : "memory");
-        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(B_CFULL + i))
-                     : "memory");
-      }
-      if (!alive) break;
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    if (pt == 0) mbar_wait(bar(B_Q), 0, &no_abort, nullptr, to);
-  } else if (warp == W_MMA) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, H, false, false);
-      constexpr uint32_t id_pv = idesc_bf16(128, H, true, C::P_MN);
       bool ok = mbar_wait(bar(B_Q), 0, abort_flag, p.status, to);
       for (int j = j0; ok && j < j1; ++j) {
         const int u = j - j0;
-        for (int i = 0; i < 9 && ok; ++i) {
-          ok = mbar_wait(bar(B_CFULL + i), u & 1, abort_flag, p.status, to);
+        for (int g = 0; g < 4 && ok; ++g) {
+          ok = mbar_wait(bar(B_CFULL + g), u & 1, abort_flag, p.status, to);
           if (!ok) break;
           fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05.mma reads
           tc_fence_after();
+          const int i_end = g == 3 ? 9 : 2 * g + 2;
+          for (int i = 2 * g; i < i_end; ++i) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tbase + C::TM_S, sdesc_sw128(sC + i * C::CSUB + kk * 32, 0, 1024),
-                      sdesc_sw128(sQ + i * C::QSUB + kk * 32, 0, 1024), id_qk, (i | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tbase + C::TM_S, sdesc_sw128(sC + i * C::CSUB + kk * 32, 0, 1024),
+                        sdesc_sw128(sQ + i * C::QSUB + kk * 32, 0, 1024), id_qk, (i | kk) != 0);
+          }
         }
         if (!ok) break;
         umma_commit(bar(B_S));
+      }
+      umma_commit(bar(B_QD));  // drain this warp's products before exit
+      mbar_wait(bar(B_QD), 0, &no_abort, nullptr, to);
+      mbar_wait(bar(B_Q), 0, &no_abort, nullptr, to);  // the Q copy has landed before exit
+    }
+    __syncwarp();
+  } else if (warp == W_PV) {
+    // ------------------------------------------------ P.V issuer: O^T += C^T . P per block
+    if (lane == 0) {
+      constexpr uint32_t id_pv = idesc_bf16(128, H, true, C::P_MN);
+      bool ok = true;
+      for (int j = j0; ok && j < j1; ++j) {
+        const int u = j - j0;
         ok = mbar_wait(bar(B_P), u & 1, abort_flag, p.status, to);
         if (!ok) break;
         tc_fence_after();
@@ -312,14 +296,68 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       lpart[h] = 0.f;
       mneg[h] = INFINITY;
     }
+    // ---- gathering role: the selected rows of the next block are copied
+    // with 16-byte cp.async into the 128-byte-swizzled K-major layout the
+    // MMA reads, each sub-tile as soon as the P.V chunk reading it is done.
+    // (Spread over all softmax warps: a warp's cp.async and its mbarrier
+    // waits share one queue, so few gathering warps issue slowly.)
+    const int kch = tid & 7, rb = tid >> 3;
+    const uint32_t gdst0 = sC + rb * 128 + ((kch ^ (rb & 7)) << 4);
+    const uint16_t* kvk = p.kv + kch * 8;
+    int gsel[RPT];  // selected positions of this thread's rows in the block being gathered
+    auto fetch_sel = [&](int jj) {
+#pragma unroll
+      for (int c = 0; c < RPT; ++c) {
+        const int sl = jj * 128 + rb + GROW * c;
+        gsel[c] = sl < nvalid ? idx_row[sl] : -1;
+      }
+    };
+    int grow[RPT];  // cache rows (< kv_rows < 2^31) of those positions; row 0 for padding
+    auto resolve_rows = [&]() {
+#pragma unroll
+      for (int c = 0; c < RPT; ++c) {
+        const int e = gsel[c];
+        const int64_t rr = row0 + e;
+        const bool ok = e >= 0 && e <= pos && rr < p.kv_rows;
+        if (!ok && e != -1 && kch == 0) atomicOr(p.status, DSA_DEVERR_INDEX);
+        grow[c] = ok ? static_cast<int>(rr) : 0;
+      }
+    };
+    auto issue = [&](int i) {
+      const uint32_t dst = gdst0 + i * C::CSUB;
+#pragma unroll
+      for (int c = 0; c < RPT; ++c)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + c * GROW * 128),
+                     "l"(kvk + static_cast<int64_t>(grow[c]) * 576 + 64 * i)
+                     : "memory");
+    };
+    // CFULL(g) completes once every copy this thread issued so far has landed
+    auto signal = [&](int g) {
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(B_CFULL + g))
+                   : "memory");
+    };
+    if (j0 < j1) {
+      fetch_sel(j0);
+      resolve_rows();
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        issue(2 * g);
+        issue(2 * g + 1);
+        if (g == 3) issue(8);
+        signal(g);
+      }
+    }
+
     int e_next = (j0 * 128 + key < nvalid && j0 < j1) ? idx_row[j0 * 128 + key] : -1;
     for (int j = j0; j < j1; ++j) {
       const int u = j - j0;
+      const bool more = j + 1 < j1;
       const int e = e_next;  // index of this thread's key, loaded one block ahead
       {
         const int sn = (j + 1) * 128 + key;
-        e_next = (j + 1 < j1 && sn < nvalid) ? idx_row[sn] : -1;
+        e_next = (more && sn < nvalid) ? idx_row[sn] : -1;
       }
+      if (more) fetch_sel(j + 1);  // consumed after P of this block
       if (!mbar_wait(bar(B_S), u & 1, abort_flag, p.status, to)) break;
       tc_fence_after();
       const bool valid = e >= 0 && e <= pos && row0 + e < p.kv_rows;
@@ -416,7 +454,26 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(B_P));
+      if (more) {
+        // refill for block j+1: chunk c of P.V frees sub-tiles 2c, 2c+1 (the
+        // last one also the RoPE sub-tile holding P)
+        resolve_rows();
+        bool alive = true;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          if (!mbar_wait(bar(B_CFREE + c), u & 1, abort_flag, p.status, to)) {
+            alive = false;
+            break;
+          }
+          issue(2 * c);
+          issue(2 * c + 1);
+          if (c == 3) issue(8);
+          signal(c);
+        }
+        if (!alive) break;
+      }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     // row sums over the 128 keys
 #pragma unroll
     for (int h = 0; h < HW; ++h) {
@@ -446,7 +503,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == W_MMA) {
+  if (warp == W_PV) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }
