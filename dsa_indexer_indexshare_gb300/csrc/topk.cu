@@ -10,12 +10,15 @@
 // `need` lowest positions equal to it, in ascending order, independent of
 // thread scheduling.
 //
-// A row is handled by one CTA, or by a cluster of CL CTAs each owning a
-// contiguous slice that it stages in shared memory once (few rows of up to
-// 16K positions), or, for few long rows, by the three-launch path below;
-// per-pass histograms and slice counts are merged through distributed
-// shared memory, so long rows (128K..1M) spread over several SMs without any
-// global atomics or spin-waits.
+// Rows of up to 16K positions are handled by one CTA each (many rows) or by
+// a cluster of CL CTAs each owning a contiguous slice that it stages in
+// shared memory once (few rows), per-pass histograms and slice counts merged
+// through distributed shared memory.  Longer rows go to a persistent
+// one-CTA-per-SM kernel that reads each row once (32 rows or more) or, for
+// fewer, to a three-launch path that spreads each row over many CTAs; see
+// the sections below.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dsa {
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(kLongBS) topk_select_kernel(const float* __res
 // all with key >> 20 == b1, find the key T of the need-th largest and how
 // many items equal to T are taken (ties to the lower position are resolved
 // afterwards).  get(i) returns the key of item i (or ~0u for a non-member).
-template <typename Get>
+template <int BS, typename Get>
 __device__ void select_low_bits(int n, int need, Get get, uint32_t b1, int* hist2, int* warp_sums,
                                 int* s_d, int* s_above, uint32_t* T, int* need_out) {
   const int tid = threadIdx.x;
@@ -401,16 +404,16 @@ __device__ void select_low_bits(int n, int need, Get get, uint32_t b1, int* hist
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
     const int shift = pass == 0 ? 10 : 0;
-    for (int i = tid; i < 1024; i += kFinBS) hist2[i] = 0;
+    for (int i = tid; i < 1024; i += BS) hist2[i] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kFinBS) {
+    for (int i = tid; i < n; i += BS) {
       const uint32_t k = get(i);
       if (k != ~0u && (k >> (shift + 10)) == prefix) atomicAdd(&hist2[(k >> shift) & 1023], 1);
     }
     __syncthreads();
     // digit d with count(digits above d) < rem <= count(digits >= d); thread
     // tid owns digits 1023 - tid*per - k, k < per (top first)
-    constexpr int per = 1024 / kFinBS;
+    constexpr int per = 1024 / BS;
     int c[per];
     int local = 0;
 #pragma unroll
@@ -419,7 +422,7 @@ __device__ void select_low_bits(int n, int need, Get get, uint32_t b1, int* hist
       local += c[k];
     }
     int total;
-    int run = block_excl_scan<kFinBS>(local, warp_sums, &total);
+    int run = block_excl_scan<BS>(local, warp_sums, &total);
 #pragma unroll
     for (int k = 0; k < per; ++k) {
       if (run < rem && run + c[k] >= rem) {
@@ -437,12 +440,96 @@ __device__ void select_low_bits(int n, int need, Get get, uint32_t b1, int* hist
   *need_out = rem;
 }
 
+// Items whose key equals T: the position of the need-th lowest of them (radix
+// over position bits [30:20], [19:10], [9:0]), or 0x7fffffff when every tied
+// item is taken.  Ends with a CTA barrier.
+template <int BS, typename GetK, typename GetP>
+__device__ int tied_position_cut(int n, int need, uint32_t T, GetK get_key, GetP get_pos,
+                                 int* hist2, int* warp_sums, int* s_d, int* s_above, int* s_n) {
+  const int tid = threadIdx.x;
+  if (tid == 0) *s_n = 0;
+  __syncthreads();
+  int my_eq = 0;
+  for (int i = tid; i < n; i += BS) my_eq += get_key(i) == T;
+  atomicAdd(s_n, my_eq);
+  __syncthreads();
+  const bool all_ties = *s_n == need;
+  __syncthreads();
+  uint32_t pprefix = all_ties ? 0x7fffffffu : 0u;
+  int rem = need;
+#pragma unroll 1
+  for (int pass = 0; pass < (all_ties ? 0 : 3); ++pass) {
+    const int shift = pass == 0 ? 20 : (pass == 1 ? 10 : 0);
+    const int nb = pass == 0 ? 2048 : 1024;
+    for (int i = tid; i < nb; i += BS) hist2[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += BS) {
+      if (get_key(i) != T) continue;
+      const uint32_t p = static_cast<uint32_t>(get_pos(i));
+      if (pass == 0 || (p >> (shift + 10)) == pprefix) atomicAdd(&hist2[(p >> shift) & (nb - 1)], 1);
+    }
+    __syncthreads();
+    // smallest digit e with count(digits below e) < rem <= count(digits <= e);
+    // thread tid owns digits [tid * per, tid * per + per)
+    const int per = (nb + BS - 1) / BS;  // at most 4
+    int c[4] = {0, 0, 0, 0};
+    int local = 0;
+    for (int k = 0; k < per; ++k) {
+      const int d = tid * per + k;
+      c[k] = d < nb ? hist2[d] : 0;
+      local += c[k];
+    }
+    int total;
+    const int below = block_excl_scan<BS>(local, warp_sums, &total);
+    int run = below;
+    for (int k = 0; k < per; ++k) {
+      if (run < rem && run + c[k] >= rem) {
+        *s_d = tid * per + k;
+        *s_above = run;
+      }
+      run += c[k];
+    }
+    __syncthreads();
+    rem -= *s_above;
+    pprefix = (pprefix << (pass == 0 ? 0 : 10)) | static_cast<uint32_t>(*s_d);
+    __syncthreads();
+  }
+  return static_cast<int>(pprefix);
+}
+
+// Ascending bitonic sort of buf[0, K) in shared memory (buf holds P >= K
+// entries, P the next power of two).  Ends with a CTA barrier.
+template <int BS>
+__device__ void sort_positions(int32_t* buf, int K) {
+  const int tid = threadIdx.x;
+  int P = 1;
+  while (P < K) P <<= 1;
+  for (int i = K + tid; i < P; i += BS) buf[i] = 0x7fffffff;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P; i += BS) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & size) == 0;
+          const int a = buf[i], c = buf[j];
+          if ((a > c) == up) {
+            buf[i] = c;
+            buf[j] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kFinBS) topk_finish_kernel(const float* __restrict__ scores,
                                                              BatchArgs b, int K, LongScratch ws,
                                                              int32_t* idx, int* status) {
   __shared__ int hist2[2048];
   __shared__ int warp_sums[32];
-  __shared__ int s_d, s_above, s_n, s_pstar;
+  __shared__ int s_d, s_above, s_n;
   extern __shared__ uint32_t fin_dyn[];  // kFinDynBytes
   uint32_t* ckey = fin_dyn;                                        // [kCandCap]
   int32_t* cpos = reinterpret_cast<int32_t*>(fin_dyn + kCandCap);  // [kCandCap]
@@ -481,61 +568,11 @@ __global__ void __launch_bounds__(kFinBS) topk_finish_kernel(const float* __rest
   auto get_pos = [&](int i) -> int { return fits ? cpos[i] : i; };
   uint32_t T;
   int need;
-  select_low_bits(n, need1, get_key, b1, hist2, warp_sums, &s_d, &s_above, &T, &need);
-  // items equal to T: take the `need` lowest positions (radix over position
-  // bits [30:20], [19:10], [9:0]) unless every tied item is taken
-  {
-    if (tid == 0) s_n = 0;
-    __syncthreads();
-    int my_eq = 0;
-    for (int i = tid; i < n; i += kFinBS) my_eq += get_key(i) == T;
-    atomicAdd(&s_n, my_eq);
-    __syncthreads();
-    const bool all_ties = s_n == need;
-    __syncthreads();
-    uint32_t pprefix = all_ties ? 0x7fffffffu : 0u;
-    int rem = need;
-#pragma unroll 1
-    for (int pass = 0; pass < (all_ties ? 0 : 3); ++pass) {
-      const int shift = pass == 0 ? 20 : (pass == 1 ? 10 : 0);
-      const int nb = pass == 0 ? 2048 : 1024;
-      for (int i = tid; i < nb; i += kFinBS) hist2[i] = 0;
-      __syncthreads();
-      for (int i = tid; i < n; i += kFinBS) {
-        if (get_key(i) != T) continue;
-        const uint32_t p = static_cast<uint32_t>(get_pos(i));
-        if (pass == 0 || (p >> (shift + 10)) == pprefix) atomicAdd(&hist2[(p >> shift) & (nb - 1)], 1);
-      }
-      __syncthreads();
-      // smallest digit e with count(digits below e) < rem <= count(digits <= e);
-      // thread tid owns digits [tid * per, tid * per + per)
-      const int per = nb / kFinBS;  // 4 or 2
-      int c[4] = {0, 0, 0, 0};
-      int local = 0;
-      for (int k = 0; k < per; ++k) {
-        c[k] = hist2[tid * per + k];
-        local += c[k];
-      }
-      int total;
-      const int below = block_excl_scan<kFinBS>(local, warp_sums, &total);
-      int run = below;
-      for (int k = 0; k < per; ++k) {
-        if (run < rem && run + c[k] >= rem) {
-          s_d = tid * per + k;
-          s_above = run;
-        }
-        run += c[k];
-      }
-      __syncthreads();
-      rem -= s_above;
-      pprefix = (pprefix << (pass == 0 ? 0 : 10)) | static_cast<uint32_t>(s_d);
-      __syncthreads();
-    }
-    if (tid == 0) s_pstar = static_cast<int>(pprefix);  // the need-th lowest tied position
-    if (tid == 0) s_n = nabove;
-    __syncthreads();
-  }
-  const int pstar = s_pstar;
+  select_low_bits<kFinBS>(n, need1, get_key, b1, hist2, warp_sums, &s_d, &s_above, &T, &need);
+  const int pstar = tied_position_cut<kFinBS>(n, need, T, get_key, get_pos, hist2, warp_sums, &s_d,
+                                              &s_above, &s_n);
+  if (tid == 0) s_n = nabove;
+  __syncthreads();
   for (int i = tid; i < n; i += kFinBS) {
     const uint32_t k = get_key(i);
     if (k == ~0u) continue;
@@ -545,32 +582,299 @@ __global__ void __launch_bounds__(kFinBS) topk_finish_kernel(const float* __rest
     }
   }
   __syncthreads();
-  // ascending order: bitonic sort of the row's K positions (padded to a power of 2)
-  int P = 1;
-  while (P < K) P <<= 1;
-  for (int i = tid; i < P; i += kFinBS) sorted[i] = i < K ? out[i] : 0x7fffffff;
-  __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P; i += kFinBS) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool up = (i & size) == 0;
-          const int a = sorted[i], c = sorted[j];
-          if ((a > c) == up) {
-            sorted[i] = c;
-            sorted[j] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
+  // ascending order
+  for (int i = tid; i < K; i += kFinBS) sorted[i] = out[i];
+  sort_positions<kFinBS>(sorted, K);
   for (int i = tid; i < K; i += kFinBS) out[i] = sorted[i];
 }
 
+// ------------------------------------------------------------------ many long rows
+// Many long rows (chunked prefill: thousands of rows of 128K+ positions).
+// One CTA per SM loops over rows and normally reads each row from HBM once:
+//  1. a 12-bit histogram of the order keys of the row's first kPrefix
+//     positions gives a cutoff bin that leaves about twice the prefix's share
+//     of K above it;
+//  2. one pass over the row keeps every key in a bin >= the cutoff, with its
+//     position, in shared memory.  With at least K keys kept (and none
+//     dropped) the k-th largest key is >= the cutoff, so every key the
+//     selection needs is kept, and the threshold bin (the one holding the
+//     k-th largest key) follows from a histogram of the kept keys;
+//  3. otherwise (an unrepresentative prefix, or a buffer overflow from many
+//     equal keys) the whole row is histogrammed and a second pass collects
+//     the positions above the threshold bin and its members.
+// The threshold bin's members are resolved as in the finish kernel above,
+// the selected positions are marked in a bitmap over the row and written out
+// in ascending order by one prefix scan (rows beyond the bitmap's reach use a
+// sort instead).
+// The scores of a row fall into few bins of the key's top 12 bits, so the
+// histogram is kept in 8 copies (lane & 7 picks one; copies start 4 banks
+// apart) to spread the shared-memory atomics on those bins, then summed.
+constexpr int kRowBS = 1024;
+constexpr int kRowWarps = kRowBS / 32;
+constexpr int kHCopies = 8;
+constexpr int kHStride = kHBins + 4;                      // words between histogram copies
+constexpr int kRegionA = kHCopies * kHStride;             // words: copies, later hist + bitmap
+constexpr int kBitWords = 28672;                          // bitmap: rows up to 917,504 positions
+constexpr int kSeg = 256;                                 // buffered keys per warp
+constexpr int kRowCand = kRowWarps * kSeg;                // buffer slots (warp segments)
+constexpr int kPrefix = 16384;      // positions whose histogram sets the capture cutoff
+constexpr int kPrefixSlack = 64;
+constexpr int kRowDynBytes = (kRegionA + 2 * kRowCand) * 4;  // 196,736 B: one CTA per SM
+static_assert(kHBins + kBitWords <= kRegionA, "merged histogram + bitmap fit the copies' space");
+
+// Visit positions [0, hi) of a row: f(s, order key, valid) for every
+// position of warp-uniform tiles (valid false past hi), so f may use warp
+// votes.  Lane l of warp w takes the float4 at w * 128 + l * 4 of every
+// 4 * BS positions, UNR float4 loads issued before any is used (enough bytes
+// in flight to keep HBM busy with one CTA per SM).  A float4 read up to the
+// next multiple of 4 stays inside the row, whose capacity is a multiple of
+// 128.
+template <int BS, int UNR, typename F>
+__device__ __forceinline__ void scan_row(const float* __restrict__ row, int hi, F f) {
+  const int lane = threadIdx.x & 31;
+  for (int wbase = (threadIdx.x >> 5) * 128; wbase < hi; wbase += BS * 4 * UNR) {
+    float4 v[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int s = wbase + u * BS * 4 + lane * 4;
+      v[u] = s < hi ? __ldg(reinterpret_cast<const float4*>(row + s))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int s = wbase + u * BS * 4 + lane * 4;
+      f(s, v[u].x, s < hi);
+      f(s + 1, v[u].y, s + 1 < hi);
+      f(s + 2, v[u].z, s + 2 < hi);
+      f(s + 3, v[u].w, s + 3 < hi);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRowBS, 1) topk_rows_kernel(const float* __restrict__ scores,
+                                                             BatchArgs b, int K, int32_t* idx,
+                                                             int* status) {
+  extern __shared__ uint32_t row_dyn[];
+  uint32_t* hcopies = row_dyn;                                  // [kHCopies][kHStride], pass 1
+  uint32_t* hist = row_dyn;                                     // [kHBins], summed copies
+  int* hist2 = reinterpret_cast<int*>(row_dyn);                 // after the threshold bin
+  uint32_t* bits = row_dyn + kHBins;                            // [kBitWords], after the sum
+  int32_t* sel = reinterpret_cast<int32_t*>(bits);              // [4096], rows beyond the bitmap
+  uint32_t* ckey = row_dyn + kRegionA;                          // [kRowWarps][kSeg]
+  int32_t* cpos = reinterpret_cast<int32_t*>(ckey + kRowCand);  // [kRowWarps][kSeg]
+  __shared__ int warp_sums[32];
+  __shared__ int s_wcnt[kRowWarps];
+  __shared__ int s_d, s_above, s_n, s_b1, s_nabove, s_ns, s_cut;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt = lanemask_lt();
+  uint32_t* hmine = hcopies + (lane & 7) * kHStride;
+  uint32_t* wkey = ckey + warp * kSeg;
+  int32_t* wpos = cpos + warp * kSeg;
+  // sum the copies into copy 0's bins (each bin read and written by one thread)
+  auto sum_copies = [&]() {
+    for (int i = tid; i < kHBins; i += kRowBS) {
+      uint32_t sum = 0;
+#pragma unroll
+      for (int c = 0; c < kHCopies; ++c) sum += hcopies[c * kHStride + i];
+      hist[i] = sum;
+    }
+  };
+  // warp-segmented buffer: slot i holds an entry when i % kSeg < its warp's count
+  auto buf_key = [&](int i) -> uint32_t {
+    return (i & (kSeg - 1)) < s_wcnt[i / kSeg] ? ckey[i] : ~0u;
+  };
+#pragma unroll 1
+  for (int t = blockIdx.x; t < b.num_q; t += gridDim.x) {
+    const int pos = query_pos(b, t, tid == 0 ? status : nullptr);
+    const int len = pos + 1;
+    int32_t* out = idx + static_cast<int64_t>(t) * K;
+    if (len <= K) {
+      for (int j = tid; j < K; j += kRowBS) out[j] = j < len ? j : -1;
+      continue;
+    }
+    const float* row = scores + static_cast<int64_t>(t) * b.max_len;
+    const bool use_bits = len <= kBitWords * 32;
+    const int nwords = (len + 31) >> 5;
+    for (int i = tid; i < kRegionA; i += kRowBS) hcopies[i] = 0;
+    if (tid == 0) {
+      s_ns = 0;
+      s_cut = 0;  // no bin found below: keep everything (overflows, second pass)
+    }
+    __syncthreads();
+    // ---- pass 1a: histogram of the row's first kPrefix positions; a cutoff
+    // bin leaving about twice the prefix's share of K above it follows
+    const int P0 = min(len, kPrefix);
+    auto count = [&](int, float x, bool valid) {
+      if (valid) atomicAdd(&hmine[order_key(x) >> 20], 1u);
+    };
+    scan_row<kRowBS, 4>(row, P0, count);
+    __syncthreads();
+    sum_copies();
+    __syncthreads();
+    const int need_p =
+        static_cast<int>(2 * static_cast<int64_t>(K) * P0 / len) + kPrefixSlack;
+    threshold_bin<kRowBS>(hist, need_p, warp_sums, &s_cut, &s_d);
+    const uint32_t cut = static_cast<uint32_t>(s_cut);
+    // ---- pass 1b: every key of the row in a bin >= cut into this warp's
+    // segment.  Compared as floats with the smallest value of bin `cut` (NaN
+    // and, at a cutoff of +0, -0 are kept too: a superset is harmless).
+    {
+      const uint32_t k0 = cut << 20;
+      const float cf = cut == 0 ? -INFINITY
+                                : __uint_as_float((k0 & 0x80000000u) ? (k0 & 0x7fffffffu) : ~k0);
+      int wcount = 0;  // warp-uniform
+      auto capture = [&](int s, float x, bool valid) {
+        const bool p = valid && !(x < cf);
+        const uint32_t m = __ballot_sync(0xffffffffu, p);
+        if (m) {
+          if (p) {
+            const int i = wcount + __popc(m & lt);
+            if (i < kSeg) {
+              wkey[i] = order_key(x);
+              wpos[i] = s;
+            }
+          }
+          wcount += __popc(m);
+        }
+      };
+      scan_row<kRowBS, 8>(row, len, capture);
+      if (lane == 0) s_wcnt[warp] = wcount;
+    }
+    for (int i = tid; i < kRegionA; i += kRowBS) hcopies[i] = 0;
+    if (tid == 0) s_b1 = -1;
+    __syncthreads();
+    // When the threshold bin of the buffered keys (the bin of their k-th
+    // largest) is >= the cutoff and no segment overflowed, at least K keys of
+    // the row are in bins >= the cutoff, all of them buffered: the buffer
+    // holds every key the selection needs.  Otherwise the whole row is
+    // histogrammed and a second pass collects what is needed.
+    bool captured = true;
+    int nbuf = 0;
+    for (int w = 0; w < kRowWarps; ++w) {
+      captured = captured && s_wcnt[w] <= kSeg;
+      nbuf += s_wcnt[w];
+    }
+    captured = captured && nbuf >= K;
+    if (captured) {
+      for (int i = tid; i < kRowCand; i += kRowBS) {
+        const uint32_t k = buf_key(i);
+        if (k != ~0u) atomicAdd(&hmine[k >> 20], 1u);
+      }
+      __syncthreads();
+      sum_copies();
+      __syncthreads();
+      threshold_bin<kRowBS>(hist, K, warp_sums, &s_b1, &s_nabove);
+      captured = s_b1 >= static_cast<int>(cut);
+      if (!captured) {
+        for (int i = tid; i < kRegionA; i += kRowBS) hcopies[i] = 0;
+        __syncthreads();
+      }
+    }
+    if (!captured) {
+      scan_row<kRowBS, 8>(row, len, count);
+      __syncthreads();
+      sum_copies();
+      __syncthreads();
+      threshold_bin<kRowBS>(hist, K, warp_sums, &s_b1, &s_nabove);
+    }
+    if (use_bits)
+      for (int i = tid; i < nwords; i += kRowBS) bits[i] = 0;
+    __syncthreads();
+    const uint32_t b1 = static_cast<uint32_t>(s_b1);
+    const int nabove = s_nabove;
+    auto take = [&](int s) {
+      if (use_bits) {
+        atomicOr(&bits[s >> 5], 1u << (s & 31));
+      } else {
+        const int i = atomicAdd(&s_ns, 1);
+        if (i < K) sel[i] = s;
+      }
+    };
+    if (captured) {
+      for (int i = tid; i < kRowCand; i += kRowBS) {
+        const uint32_t k = buf_key(i);
+        if (k != ~0u && (k >> 20) > b1) take(cpos[i]);
+      }
+    } else {
+      // ---- pass 2: positions above the threshold bin, members of it
+      int wcount = 0;
+      auto visit = [&](int s, float x, bool valid) {
+        const uint32_t key = order_key(x);
+        const uint32_t bin = key >> 20;
+        if (valid && bin > b1) take(s);
+        const bool p = valid && bin == b1;
+        const uint32_t m = __ballot_sync(0xffffffffu, p);
+        if (m) {
+          if (p) {
+            const int i = wcount + __popc(m & lt);
+            if (i < kSeg) {
+              wkey[i] = key;
+              wpos[i] = s;
+            }
+          }
+          wcount += __popc(m);
+        }
+      };
+      scan_row<kRowBS, 8>(row, len, visit);
+      __syncthreads();  // every thread has read the previous counts
+      if (lane == 0) s_wcnt[warp] = wcount;
+      __syncthreads();
+    }
+    // the threshold bin's members: from the buffer, or from the row itself
+    // when a segment overflowed
+    bool fits = true;
+    for (int w = 0; w < kRowWarps; ++w) fits = fits && s_wcnt[w] <= kSeg;
+    const int n = fits ? kRowCand : len;
+    auto get_key = [&](int i) -> uint32_t {
+      const uint32_t k = fits ? buf_key(i) : order_key(row[i]);
+      return (k != ~0u && (k >> 20) == b1) ? k : ~0u;
+    };
+    auto get_pos = [&](int i) -> int { return fits ? cpos[i] : i; };
+    uint32_t T;
+    int need;
+    select_low_bits<kRowBS>(n, K - nabove, get_key, b1, hist2, warp_sums, &s_d, &s_above, &T,
+                            &need);
+    const int pstar = tied_position_cut<kRowBS>(n, need, T, get_key, get_pos, hist2, warp_sums,
+                                                &s_d, &s_above, &s_n);
+    for (int i = tid; i < n; i += kRowBS) {
+      const uint32_t k = get_key(i);
+      if (k == ~0u) continue;
+      if (k > T || (k == T && get_pos(i) <= pstar)) take(get_pos(i));
+    }
+    __syncthreads();
+    if (use_bits) {
+      // ascending compaction: thread tid owns words [tid * wpt, tid * wpt + wpt)
+      const int wpt = (nwords + kRowBS - 1) / kRowBS;
+      const int w0 = min(tid * wpt, nwords), w1 = min(w0 + wpt, nwords);
+      int c = 0;
+      for (int w = w0; w < w1; ++w) c += __popc(bits[w]);
+      int total;
+      int slot = block_excl_scan<kRowBS>(c, warp_sums, &total);
+      if (tid == 0 && total != K) atomicOr(status, DSA_DEVERR_BATCH);
+      for (int w = w0; w < w1; ++w) {
+        uint32_t m = bits[w];
+        while (m) {
+          const int bit = __ffs(m) - 1;
+          m &= m - 1;
+          if (slot < K) out[slot] = w * 32 + bit;
+          ++slot;
+        }
+      }
+    } else {
+      if (tid == 0 && s_ns != K) atomicOr(status, DSA_DEVERR_BATCH);
+      sort_positions<kRowBS>(sel, K);
+      for (int i = tid; i < K; i += kRowBS) out[i] = sel[i];
+    }
+    __syncthreads();  // the next row reuses the shared buffers
+  }
+}
+
+// Rows beyond 16K positions: fewer than kRowsMin of them are spread over
+// several CTAs each (the three launches above); more get a CTA each.
+constexpr int kRowsMin = 32;
+
 bool use_long_path(const dsa_batch_t& b) {
-  return static_cast<int64_t>(b.num_q) < 2 * 152 && b.max_len > 16384;
+  return b.num_q < kRowsMin && b.max_len > 16384;
 }
 
 size_t round256z(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -607,6 +911,27 @@ cudaError_t launch_cl(const float* scores, const dsa_batch_t& b, int k, int32_t*
   prof_end(kLaunchTopk, stream);
   count_launch(kLaunchTopk);
   return e;
+}
+
+cudaError_t launch_rows(const float* scores, const dsa_batch_t& b, int k, int32_t* idx, int* status,
+                        cudaStream_t stream) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kRowDynBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  int sms = 152;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = static_cast<int>(std::min<int64_t>(b.num_q, sms));
+  prof_begin(stream);
+  topk_rows_kernel<<<grid, kRowBS, kRowDynBytes, stream>>>(scores, to_args(b), k, idx, status);
+  prof_end(kLaunchTopk, stream);
+  count_launch(kLaunchTopk);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -656,14 +981,13 @@ cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_
     count_launch(kLaunchTopk);
     return cudaGetLastError();
   }
-  // Many rows (prefill, chunked prefill): one CTA per row, its row re-read
-  // from L2 per pass (rows up to 16K positions use 256 threads, longer ones
-  // 1024).  Few short rows: a cluster of 8 CTAs per row, each staging its
-  // slice in shared memory once.
-  if (static_cast<int64_t>(b.num_q) >= 2 * 152) {
-    return b.max_len <= 16384 ? launch_cl<1, 256, false>(scores, b, k, idx, status, 0, stream)
-                              : launch_cl<1, 1024, false>(scores, b, k, idx, status, 0, stream);
-  }
+  // Rows beyond 16K positions (kRowsMin or more of them): one persistent CTA
+  // per SM, a row at a time.  Many short rows (prefill): one CTA of 256
+  // threads per row, its row re-read from L2 per pass.  Few short rows: a
+  // cluster of 8 CTAs per row, each staging its slice in shared memory once.
+  if (b.max_len > 16384) return launch_rows(scores, b, k, idx, status, stream);
+  if (static_cast<int64_t>(b.num_q) >= 2 * 152)
+    return launch_cl<1, 256, false>(scores, b, k, idx, status, 0, stream);
   const int64_t slice = ((b.max_len + 7) / 8 + 3) & ~3;
   return launch_cl<8, 1024, true>(scores, b, k, idx, status, static_cast<size_t>(slice) * 4, stream);
 }

@@ -95,6 +95,14 @@ def test_topk_bit_exact_long_rows(values):
 
 
 @pytest.mark.parametrize("values", ["ties", "gauss", "const"])
+def test_topk_bit_exact_many_long_rows(values):
+    # hundreds of rows beyond 16K positions: one persistent CTA per SM, two
+    # reads per row (constant rows overflow the member buffer and rescan);
+    # the second sequence's rows have pos + 1 <= K
+    _topk_case([40000, 1500], [390, 20], 2048, values, 6)
+
+
+@pytest.mark.parametrize("values", ["ties", "gauss", "const"])
 def test_topk_bit_exact_few_short_rows_cluster(values):
     _topk_case([9000, 16000, 3000], [1, 2, 1], 512, values, 5)  # cluster of 8, staged
 
