@@ -42,6 +42,8 @@ DESCR = {
     "decode1m": "1M decode: 4 sequences x 1 query, context 1048576, layers FSSS, H=64, K=2048, "
                 "FP8 E4M3 + Hadamard indexer keys/queries, bf16 KV latent",
     "prefill2k": "profiling case: prefill of 2560 tokens, layers FSSS, H=64, K=2048, bf16",
+    "chunked1k": "profiling case: chunked prefill of 1024 queries after a 131072-token prefix, "
+                 "layers FSSS, H=64, K=2048, bf16",
     "decode8": "profiling case: decode of 8 sequences x 1 query, context U[98304,131072], FSSS, "
                "H=64, K=2048, bf16",
 }
@@ -50,7 +52,7 @@ DESCR = {
 NCU_TRAFFIC = {
     # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch, scaled by
     # tokens to the 8192-token launch (q/out traffic is per token; the kv cache is a few MB)
-    "sparse_mla": {"bytes": 1.0577e+09, "workload": "prefill8k", "src": "4c89d053fc2c247b"},
+    "sparse_mla": {"bytes": 1.0590e+09, "workload": "prefill8k", "src": "0fba8f882d686733"},
 }
 
 
@@ -417,7 +419,8 @@ def main():
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
     if not args.no_cpu and rank == 0 and world == 1:
         nrows = args.cpu_rows or {"tiny": 512, "prefill8k": 48, "decode64": 4, "chunked": 24,
-                                  "decode1m": 1, "prefill2k": 48, "decode8": 4}[args.workload]
+                                  "decode1m": 1, "prefill2k": 48, "decode8": 4,
+                                  "chunked1k": 24}[args.workload]
         rows, host = oracle_sample(args.workload, lay, layers, cfg, fp8, nrows)
         import oracle
         secs = run_oracle(lay, host, rows, cfg, fp8)
@@ -481,7 +484,8 @@ def reference_arm(args):
     lay = synth.workload_layout(args.workload)
     fp8 = bool(cfg.get("fp8"))
     nrows = args.cpu_rows or {"tiny": 64, "prefill8k": 8, "decode64": 1, "chunked": 4,
-                              "decode1m": 1, "prefill2k": 8, "decode8": 1}[args.workload]
+                              "decode1m": 1, "prefill2k": 8, "decode8": 1,
+                              "chunked1k": 4}[args.workload]
     sub, rows, host = reference_inputs(lay, cfg, fp8, nrows)
     for _ in range(args.warmup):
         run_oracle(sub, host, rows, cfg, fp8)

@@ -174,7 +174,7 @@ DSA_API dsa_status_t dsa_indexer_scores(const void* q_idx, const float* q_scale,
  * are -1.  scores is fp32 [num_q, max_len] (only s <= q_pos[t] is read), idx
  * int32 [num_q, k].  1 <= k <= 4096.  The comparison uses the fp32 bit
  * order (NaN ranks above +inf).  ws: dsa_topk_workspace_size (the status
- * block, plus 48 KB of scratch per row for batches of fewer than 304 rows
+ * block, plus 48 KB of scratch per row for batches of fewer than 32 rows
  * longer than 16K positions).
  */
 DSA_API size_t dsa_topk_workspace_size(const dsa_batch_t* b, int32_t k);

@@ -13,8 +13,8 @@ Workloads (all seeded):
 * ``decode64``  64 sequences, one query each, context ~ U[98304, 131072].
 * ``chunked``   4096 new queries after a 131072-token cached prefix, 8 layers.
 * ``decode1m``  4 sequences of 1,048,576 positions, FP8 indexer keys.
-* ``prefill2k`` / ``decode8``: the same shapes at 2560 tokens / 8 sequences,
-  small enough for profiler captures.
+* ``prefill2k`` / ``decode8`` / ``chunked1k``: the same shapes at 2560 tokens /
+  8 sequences / 1024 new queries (4 layers), small enough for profiler captures.
 
 Gaussian workloads draw each vector as N(0, 1)/sqrt(d) with d its own width
 (128 for indexer q/k, 512 for latent parts, 64 for RoPE parts) and head
@@ -47,6 +47,7 @@ WORKLOADS = {
     # smaller cases of the same kernels, sized for profiler captures
     "prefill2k": dict(kind="prefill", T=2560, H=64, K=2048, layers="FSSS"),
     "decode8": dict(kind="decode", B=8, lo=98304, hi=131072, H=64, K=2048, layers="FSSS"),
+    "chunked1k": dict(kind="chunked", prefix=131072, Tq=1024, H=64, K=2048, layers="FSSS"),
 }
 
 
