@@ -179,7 +179,41 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- inputs
-def setup(workload, dev, seed=0):
+def page_caches(lay, layers, block_rows, dev, seed=0):
+    """Move every per-position cache (kv, k_idx, k_scale) into a paged pool:
+    each sequence's blocks of block_rows positions go to a seeded random
+    permutation of physical blocks.  Returns the block table and the
+    physical row of every logical (contiguous) row, on the device."""
+    import numpy as np
+    import torch
+    R = int(block_rows)
+    lens = [int(n) for n in lay.seq_len]
+    nblk = [(n + R - 1) // R for n in lens]
+    bps = (lay.max_len + R - 1) // R
+    total = sum(nblk)
+    ids = np.random.default_rng(5000 + seed).permutation(total)
+    table = np.full((len(lens), bps), -1, np.int32)
+    phys = np.empty(lay.rows, np.int64)  # physical row of every logical (contiguous) row
+    k = 0
+    for b, n in enumerate(lens):
+        table[b, :nblk[b]] = ids[k:k + nblk[b]]
+        s = np.arange(n)
+        phys[int(lay.seq_row0[b]) + s] = table[b, s // R].astype(np.int64) * R + s % R
+        k += nblk[b]
+    phys_d = torch.from_numpy(phys).to(dev)
+    for L in layers:
+        for key in ("kv", "k_idx", "k_scale"):
+            if key in L:
+                src = L[key]
+                dst = torch.zeros((total * R,) + tuple(src.shape[1:]), dtype=src.dtype, device=dev)
+                dst.index_copy_(0, phys_d, src)
+                L[key] = dst
+                del src
+    torch.cuda.synchronize(dev)
+    return table, phys_d
+
+
+def setup(workload, dev, seed=0, paged=0):
     import torch
 
     import dsa_indexer_indexshare_gb300 as dsa
@@ -198,8 +232,14 @@ def setup(workload, dev, seed=0):
                 kc, ks = dsa.dsa_fp8_quantize(L["k_idx"])
                 L.update(q_idx=qc, q_scale=qs, k_idx=kc, k_scale=ks)
         torch.cuda.synchronize(dev)
-    batch = dsa.Batch(lay.q_start, lay.q_pos, lay.seq_row0, lay.max_len, device=dev)
-    return cfg, lay, layers, batch, fp8
+    phys = None
+    if paged:
+        table, phys = page_caches(lay, layers, paged, dev, seed)
+        batch = dsa.Batch(lay.q_start, lay.q_pos, None, lay.max_len, device=dev,
+                          block_table=table, block_rows=paged)
+    else:
+        batch = dsa.Batch(lay.q_start, lay.q_pos, lay.seq_row0, lay.max_len, device=dev)
+    return cfg, lay, layers, batch, fp8, phys
 
 
 def time_steps(run, steps, warmup, flush, stream):
@@ -222,8 +262,9 @@ def time_steps(run, steps, warmup, flush, stream):
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_sample(workload, lay, layers, cfg, fp8, nrows, seed=1):
-    """Host copies of a sampled set of query rows (and the caches they read)."""
+def oracle_sample(workload, lay, layers, cfg, fp8, nrows, seed=1, phys=None):
+    """Host copies of a sampled set of query rows (and the caches they read,
+    in contiguous order: a paged cache is read back through `phys`)."""
     import torch
     rng = np.random.default_rng(seed)
     nq = lay.num_q
@@ -238,6 +279,9 @@ def oracle_sample(workload, lay, layers, cfg, fp8, nrows, seed=1):
     host = []
     rt = torch.as_tensor(rows, device=layers[0]["q_lat"].device)
     for L in layers:
+        if phys is not None:
+            L = {k: (v.index_select(0, phys) if k in ("kv", "k_idx", "k_scale") else v)
+                 for k, v in L.items()}
         d = {"q_lat": hb(L["q_lat"].index_select(0, rt)), "q_rope": hb(L["q_rope"].index_select(0, rt)),
              "kv": hb(L["kv"])}
         if "q_idx" in L:
@@ -273,6 +317,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0)
+    ap.add_argument("--paged", type=int, default=0, metavar="ROWS",
+                    help="paged caches: blocks of ROWS positions (a multiple of 128) in a "
+                         "permuted pool, addressed through a block table")
     args = ap.parse_args()
 
     import torch
@@ -293,7 +340,7 @@ def main():
 
     import dsa_indexer_indexshare_gb300 as dsa
     peaks = load_peaks()
-    cfg, lay, layers, batch, fp8 = setup(args.workload, dev)
+    cfg, lay, layers, batch, fp8, phys = setup(args.workload, dev, paged=args.paged)
     stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.fill_(1)
@@ -395,6 +442,8 @@ def main():
             "config": {"workload": DESCR[args.workload], "global_batch": world * tokens_per_step,
                        "seq_len": int(lay.max_len), "layers": cfg["layers"],
                        "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "kv_layout": (f"paged: blocks of {args.paged} positions, permuted pool, "
+                                     "block table" if args.paged else "contiguous"),
                        "l2": "flushed between steps (256 MiB write, outside the timed events)"},
             "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
             "clocks": clocks, "wall_s_timed": round(wall, 3)}
@@ -421,7 +470,7 @@ def main():
         nrows = args.cpu_rows or {"tiny": 512, "prefill8k": 48, "decode64": 4, "chunked": 24,
                                   "decode1m": 1, "prefill2k": 48, "decode8": 4,
                                   "chunked1k": 24}[args.workload]
-        rows, host = oracle_sample(args.workload, lay, layers, cfg, fp8, nrows)
+        rows, host = oracle_sample(args.workload, lay, layers, cfg, fp8, nrows, phys=phys)
         import oracle
         secs = run_oracle(lay, host, rows, cfg, fp8)
         line["cpu_baseline"] = {"value": round(len(rows) / secs, 3), "unit": UNIT,

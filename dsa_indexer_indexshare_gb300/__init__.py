@@ -37,7 +37,8 @@ class DsaError(RuntimeError):
 class _Batch(ctypes.Structure):
     _fields_ = [("num_seqs", c_int32), ("num_q", c_int32), ("max_q", c_int32),
                 ("max_len", c_int32), ("q_start", c_void_p), ("q_pos", c_void_p),
-                ("seq_row0", c_void_p)]
+                ("seq_row0", c_void_p), ("block_table", c_void_p), ("block_rows", c_int32),
+                ("blocks_per_seq", c_int32)]
 
 
 _PP = POINTER(c_void_p)
@@ -126,9 +127,12 @@ def _need(t, name, dtype=None, device=None, shape=None):
 class Batch:
     """Batch layout (dsa_batch_t): query rows of sequence b are
     [q_start[b], q_start[b+1]); query t sits at position q_pos[t]; position s
-    of sequence b is row seq_row0[b] + s of every per-layer cache."""
+    of sequence b is row seq_row0[b] + s of every per-layer cache, or, with a
+    block table [num_seqs, blocks_per_seq] (paged caches), row
+    block_table[b, s // block_rows] * block_rows + s % block_rows."""
 
-    def __init__(self, q_start, q_pos, seq_row0, max_len: int, device="cuda"):
+    def __init__(self, q_start, q_pos, seq_row0, max_len: int, device="cuda", *,
+                 block_table=None, block_rows: int = 0):
         import numpy as np
         qs = np.asarray(q_start, np.int64)
         self.num_seqs = int(qs.size - 1)
@@ -139,9 +143,21 @@ class Batch:
         self.device = dev
         self.q_start = torch.as_tensor(np.asarray(q_start, np.int32), device=dev)
         self.q_pos = torch.as_tensor(np.asarray(q_pos, np.int32), device=dev)
-        self.seq_row0 = torch.as_tensor(np.asarray(seq_row0, np.int64), device=dev)
+        self.seq_row0 = (torch.as_tensor(np.asarray(seq_row0, np.int64), device=dev)
+                         if seq_row0 is not None else None)
+        if block_table is not None:
+            bt = np.asarray(block_table, np.int32)
+            if bt.ndim != 2 or bt.shape[0] != self.num_seqs:
+                raise ValueError("block_table must be [num_seqs, blocks_per_seq]")
+            self.block_table = torch.as_tensor(np.ascontiguousarray(bt), device=dev)
+            self.block_rows, self.blocks_per_seq = int(block_rows), int(bt.shape[1])
+        else:
+            self.block_table, self.block_rows, self.blocks_per_seq = None, 0, 0
         self._c = _Batch(self.num_seqs, self.num_q, self.max_q, self.max_len,
-                         _ptr(self.q_start), _ptr(self.q_pos), _ptr(self.seq_row0))
+                         _ptr(self.q_start), _ptr(self.q_pos),
+                         _ptr(self.seq_row0) if self.seq_row0 is not None else None,
+                         _ptr(self.block_table) if self.block_table is not None else None,
+                         self.block_rows, self.blocks_per_seq)
 
     @property
     def c(self):

@@ -55,8 +55,18 @@ dsa_status_t check_batch(const dsa_batch_t* b) {
     return fail(DSA_ERR_INVALID_ARG, "max_q must be >= 1 when num_q > 0");
   if (b->max_q > b->num_q) return fail(DSA_ERR_INVALID_ARG, "max_q > num_q");
   if (b->num_seqs > 65535) return fail(DSA_ERR_UNSUPPORTED, "num_seqs > 65535");
-  if (!b->q_start || !b->q_pos || !b->seq_row0)
+  const bool paged = b->block_table != nullptr;
+  if (!b->q_start || !b->q_pos || (!paged && !b->seq_row0))
     return fail(DSA_ERR_INVALID_ARG, "batch arrays must be non-NULL device pointers");
+  if (paged) {
+    if (b->block_rows < 128 || (b->block_rows & (b->block_rows - 1)) != 0)
+      return fail(DSA_ERR_INVALID_ARG, "block_rows=%d must be a power of two >= 128",
+                  b->block_rows);
+    if (b->blocks_per_seq < 1 ||
+        static_cast<int64_t>(b->blocks_per_seq) * b->block_rows < b->max_len)
+      return fail(DSA_ERR_INVALID_ARG, "blocks_per_seq=%d x block_rows=%d does not cover max_len=%d",
+                  b->blocks_per_seq, b->block_rows, b->max_len);
+  }
   return DSA_OK;
 }
 

@@ -17,10 +17,29 @@ struct BatchArgs {
   const int32_t* q_start;
   const int32_t* q_pos;
   const int64_t* seq_row0;
+  const int32_t* block_table;  // paged layout when not null
+  int32_t block_rows, blocks_per_seq;
 };
 
 inline BatchArgs to_args(const dsa_batch_t& b) {
-  return BatchArgs{b.num_seqs, b.num_q, b.max_q, b.max_len, b.q_start, b.q_pos, b.seq_row0};
+  return BatchArgs{b.num_seqs, b.num_q, b.max_q, b.max_len, b.q_start, b.q_pos, b.seq_row0,
+                   b.block_table, b.block_rows, b.blocks_per_seq};
+}
+
+// First cache row of sequence `seq` in the contiguous layout (0 when paged).
+__device__ __forceinline__ int64_t seq_base_row(const BatchArgs& b, int seq) {
+  return b.block_table ? 0 : b.seq_row0[seq];
+}
+
+// Cache row of position s (>= 0) of sequence `seq`; base = seq_base_row(b, seq).
+// Paged layout: the row inside the block the table names, or -1 for a
+// negative block id or a block beyond the table.
+__device__ __forceinline__ int64_t cache_row(const BatchArgs& b, int seq, int64_t base, int s) {
+  if (!b.block_table) return base + s;
+  const int blk = s / b.block_rows;
+  if (blk >= b.blocks_per_seq) return -1;
+  const int32_t id = b.block_table[static_cast<int64_t>(seq) * b.blocks_per_seq + blk];
+  return id < 0 ? -1 : static_cast<int64_t>(id) * b.block_rows + (s - blk * b.block_rows);
 }
 
 // Rows [qs, qe) of sequence `seq`, validated against the batch sizes.  On

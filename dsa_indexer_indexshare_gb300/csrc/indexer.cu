@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
     }
   }
   if (nkb == 0) return;
-  const int64_t row0 = p.b.seq_row0[seq];
+  const int64_t row0 = seq_base_row(p.b, seq);
 
   // ---- shared memory, barriers, TMEM
   const uint32_t sQ = smem_u32(sm + C::OFF_Q);
@@ -184,7 +184,11 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
             !mbar_wait(bar(B_KEMPTY + st), ((i / STAGES) - 1) & 1, abort_flag, p.status, to))
           break;
         mbar_arrive_expect_tx(bar(B_KFULL + st), C::K_BYTES);
-        const int y = static_cast<int>(row0 + s_begin + i * 128);
+        // first cache row of the tile (a tile never straddles a cache block);
+        // an unmapped block loads as zeros (tile fully outside the map)
+        const int64_t ty = cache_row(p.b, seq, row0, s_begin + i * 128);
+        if (ty < 0) atomicOr(p.status, DSA_DEVERR_INDEX);
+        const int y = ty < 0 ? -128 : static_cast<int>(ty);
 #pragma unroll
         for (int ks = 0; ks < C::KSUB; ++ks)
           tma_load_2d(sK + st * C::K_BYTES + ks * C::K_SUB, &kmap, ks * 64, y, bar(B_KFULL + st));
@@ -240,8 +244,8 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
       const int s = s_begin + i * 128 + quarter * 32 + lane;
       float kscale = 1.f;
       if (FP8) {
-        const int64_t kr = row0 + s;
-        kscale = kr < p.k_rows ? p.k_scale[kr] : 0.f;
+        const int64_t kr = cache_row(p.b, seq, row0, s);
+        kscale = (kr >= 0 && kr < p.k_rows) ? p.k_scale[kr] : 0.f;
       }
 #pragma unroll
       for (int nn = 0; nn < C::TOK_PER_WARP; ++nn) {

@@ -57,8 +57,12 @@ extern "C" DSA_API dsa_status_t dsa_indexer_topk_noalloc(
   // Argument checks mirror dsa_indexer_scores + dsa_topk.
   if (!b || !q_idx || !w || !k_idx || !idx) return DSA_ERR_INVALID_ARG;
   if (b->num_seqs < 1 || b->num_q < 0 || b->max_q < 0 || b->max_q > b->num_q ||
-      b->max_len < 128 || b->max_len % 128 != 0 || !b->q_start || !b->q_pos || !b->seq_row0 ||
-      (b->num_q > 0 && b->max_q < 1))
+      b->max_len < 128 || b->max_len % 128 != 0 || !b->q_start || !b->q_pos ||
+      (!b->block_table && !b->seq_row0) || (b->num_q > 0 && b->max_q < 1))
+    return DSA_ERR_INVALID_ARG;
+  if (b->block_table &&
+      (b->block_rows < 128 || (b->block_rows & (b->block_rows - 1)) != 0 || b->blocks_per_seq < 1 ||
+       static_cast<int64_t>(b->blocks_per_seq) * b->block_rows < b->max_len))
     return DSA_ERR_INVALID_ARG;
   if (b->num_seqs > 65535) return DSA_ERR_UNSUPPORTED;
   if (dt != DSA_BF16 && dt != DSA_FP8_E4M3) return DSA_ERR_UNSUPPORTED;

@@ -64,7 +64,10 @@ struct MlaCfg {
   static constexpr int OFF_BAR = (OFF_FLAGS + 4 * 8 + 7) & ~7;
   static constexpr int NBAR = 1 + 4 + 4 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  // the sequence's block-table row (paged caches), when it has <= TAB_MAX entries
+  static constexpr int TAB_MAX = 1024;
+  static constexpr int OFF_TAB = OFF_MISC + 64;
+  static constexpr int SMEM = OFF_TAB + TAB_MAX * 4 + 1024;
   static constexpr int HW = H > 32 ? 32 : H;       // heads per softmax warp
   static constexpr int NSW = 4 * (H / HW);           // softmax warps (two per lane quarter at H=64)
   static constexpr int NT = NSW * 32 + 64;           // + the QK and the P.V issuer warps
@@ -136,7 +139,7 @@ __device__ __forceinline__ void tmem_cols_store(uint32_t taddr, const float (&v)
     tmem_st32(taddr, v);
 }
 
-template <int H, int NSPLIT>
+template <int H, int NSPLIT, bool PAGED>
 __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap qlat_map,
                       const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   const int nvalid = pos < 0 ? 0 : min(p.K, pos + 1);
   const int nb = (nvalid + 127) / 128;
   const int j0 = rank * nb / NSPLIT, j1 = (rank + 1) * nb / NSPLIT;  // this CTA's blocks
-  const int64_t row0 = p.b.seq_row0[seq];
+  const int64_t row0 = seq_base_row(p.b, seq);
   const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.K;
   if (nb == 0) {  // nothing visible: zero output, lse = -inf
     constexpr int DS = 512 / NSPLIT;
@@ -208,6 +211,27 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     fence_mbar_init();
   }
   if (tid < H) m_used[tid] = -INFINITY;
+  // Paged caches: the sequence's block-table row is staged in shared memory
+  // (when short enough) so that the per-key row lookups of the gather and
+  // of the softmax's validity test stay off global memory.
+  int32_t* stab = reinterpret_cast<int32_t*>(sm + C::OFF_TAB);
+  const int bps = p.b.blocks_per_seq;
+  const bool tab_smem = PAGED && bps <= C::TAB_MAX;
+  if (tab_smem)
+    for (int i = tid; i < bps; i += NT) stab[i] = p.b.block_table[static_cast<int64_t>(seq) * bps + i];
+  const int rshift = PAGED ? __ffs(p.b.block_rows) - 1 : 0;  // block_rows is a power of two
+  auto row_of = [&](int e) -> int64_t {  // cache row of selected position e >= 0, -1 if unmapped
+    if constexpr (!PAGED) {
+      return row0 + e;
+    } else {
+      const int blk = e >> rshift;
+      if (blk >= bps) return -1;
+      const int32_t id =
+          tab_smem ? stab[blk] : p.b.block_table[static_cast<int64_t>(seq) * bps + blk];
+      return id < 0 ? -1
+                    : (static_cast<int64_t>(id) << rshift) + (e & (p.b.block_rows - 1));
+    }
+  };
   if (warp == W_PV) {
     tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
     tmem_relinquish();
@@ -317,8 +341,8 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
 #pragma unroll
       for (int c = 0; c < RPT; ++c) {
         const int e = gsel[c];
-        const int64_t rr = row0 + e;
-        const bool ok = e >= 0 && e <= pos && rr < p.kv_rows;
+        const int64_t rr = e >= 0 ? row_of(e) : -1;
+        const bool ok = e >= 0 && e <= pos && rr >= 0 && rr < p.kv_rows;
         if (!ok && e != -1 && kch == 0) atomicOr(p.status, DSA_DEVERR_INDEX);
         grow[c] = ok ? static_cast<int>(rr) : 0;
       }
@@ -360,7 +384,11 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       if (more) fetch_sel(j + 1);  // consumed after P of this block
       if (!mbar_wait(bar(B_S), u & 1, abort_flag, p.status, to)) break;
       tc_fence_after();
-      const bool valid = e >= 0 && e <= pos && row0 + e < p.kv_rows;
+      bool valid = e >= 0 && e <= pos;  // the gather's test, on this thread's key
+      if (valid) {
+        const int64_t rr = row_of(e);
+        valid = rr >= 0 && rr < p.kv_rows;
+      }
       // d = scale*log2(e)*s - m: the exponent of P and the rescale test in one FFMA
       float d[HW];
       tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
@@ -576,11 +604,11 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   }
 }
 
-template <int H, int NSPLIT>
+template <int H, int NSPLIT, bool PAGED>
 cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p,
                        cudaStream_t stream) {
   using C = MlaCfg<H>;
-  auto* kern = sparse_mla_kernel<H, NSPLIT>;
+  auto* kern = sparse_mla_kernel<H, NSPLIT, PAGED>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -610,12 +638,17 @@ cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaPa
 
 template <int H>
 cudaError_t launch_h(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p, int nsplit,
+                     bool paged,
                      cudaStream_t stream) {
   switch (nsplit) {
-    case 1: return launch_mla<H, 1>(ql, qr, p, stream);
-    case 2: return launch_mla<H, 2>(ql, qr, p, stream);
-    case 4: return launch_mla<H, 4>(ql, qr, p, stream);
-    default: return launch_mla<H, 8>(ql, qr, p, stream);
+    case 1: return paged ? launch_mla<H, 1, true>(ql, qr, p, stream)
+                         : launch_mla<H, 1, false>(ql, qr, p, stream);
+    case 2: return paged ? launch_mla<H, 2, true>(ql, qr, p, stream)
+                         : launch_mla<H, 2, false>(ql, qr, p, stream);
+    case 4: return paged ? launch_mla<H, 4, true>(ql, qr, p, stream)
+                         : launch_mla<H, 4, false>(ql, qr, p, stream);
+    default: return paged ? launch_mla<H, 8, true>(ql, qr, p, stream)
+                          : launch_mla<H, 8, false>(ql, qr, p, stream);
   }
 }
 
@@ -650,8 +683,9 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   int nsplit = 1;
   while (nsplit < 8 && nsplit * 2 <= nblk && static_cast<int64_t>(b.num_q) * nsplit * 2 <= 152)
     nsplit *= 2;
-  return heads == 16 ? launch_h<16>(ql, qr, p, nsplit, stream)
-                     : launch_h<64>(ql, qr, p, nsplit, stream);
+  const bool paged = b.block_table != nullptr;
+  return heads == 16 ? launch_h<16>(ql, qr, p, nsplit, paged, stream)
+                     : launch_h<64>(ql, qr, p, nsplit, paged, stream);
 }
 
 }  // namespace dsa

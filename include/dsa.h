@@ -75,7 +75,13 @@ enum {
  * of sequence b are [q_start[b], q_start[b+1]).  Query t sits at absolute
  * position q_pos[t] of its sequence and sees positions 0..q_pos[t] (causal,
  * itself included).  Every per-layer cache (indexer keys, KV latent) stores
- * position s of sequence b at row seq_row0[b] + s.
+ * position s of sequence b at row seq_row0[b] + s (contiguous layout), or,
+ * when block_table is not NULL (paged layout: caches allocated in blocks of
+ * block_rows rows, a sequence's blocks anywhere in the cache), at row
+ *   block_table[b * blocks_per_seq + s / block_rows] * block_rows + s % block_rows.
+ * The paged layout is the block-table cache of PagedAttention, which pages
+ * the compressed 512-d MLA KV ("GLM-5.2 架构深度拆解" CH 4.4); the pages fix no
+ * block format, and this is its plainest form.
  *   num_seqs  >= 1
  *   num_q     >= 0 (0 is a no-op)
  *   max_q     >= the largest query count of one sequence
@@ -83,9 +89,15 @@ enum {
  *   q_start   device int32 [num_seqs + 1], non-decreasing, q_start[0] = 0,
  *             q_start[num_seqs] = num_q
  *   q_pos     device int32 [num_q]
- *   seq_row0  device int64 [num_seqs]
- * A kernel that finds q_start / q_pos inconsistent with these sizes skips the
- * affected rows and raises DSA_ERR_DEVICE_INDEX in the status word.
+ *   seq_row0  device int64 [num_seqs] (contiguous layout; NULL allowed when paged)
+ *   block_table     device int32 [num_seqs * blocks_per_seq] block ids, or NULL
+ *   block_rows      paged layout: rows per block, a power of two >= 128 (so
+ *                   that a 128-position key tile never straddles blocks)
+ *   blocks_per_seq  paged layout: table row stride; blocks_per_seq * block_rows
+ *                   must cover max_len
+ * A kernel that finds q_start / q_pos inconsistent with these sizes, or a
+ * negative block id for a visible position, skips the affected rows and
+ * raises DSA_ERR_DEVICE_INDEX in the status word.
  */
 typedef struct {
   int32_t num_seqs;
@@ -95,6 +107,9 @@ typedef struct {
   const int32_t* q_start;
   const int32_t* q_pos;
   const int64_t* seq_row0;
+  const int32_t* block_table;
+  int32_t block_rows;
+  int32_t blocks_per_seq;
 } dsa_batch_t;
 
 /* ------------------------------------------------------------------ status */

@@ -131,6 +131,34 @@ def row_metadata(q_start, q_pos, seq_row0, rows):
     return row_pos, row_key0
 
 
+def paged_row(block_table, block_rows, seq, s):
+    """Cache row of position s of sequence seq in a paged cache: the table
+    names the block holding positions [j*block_rows, (j+1)*block_rows) of the
+    sequence, and the position keeps its offset inside the block
+    (PagedAttention over the compressed MLA KV, "GLM-5.2 架构深度拆解" CH 4.4).
+    -1 when the table has no block for it (negative id or beyond the table)."""
+    bt = np.asarray(block_table)
+    j = int(s) // int(block_rows)
+    if j >= bt.shape[1] or bt[seq, j] < 0:
+        return -1
+    return int(bt[seq, j]) * int(block_rows) + int(s) % int(block_rows)
+
+
+def logical_cache(paged, block_table, block_rows, seq_lens):
+    """The contiguous cache a paged one stands for: positions 0..seq_lens[b]-1
+    of every sequence b, back to back in sequence order (row seq_row0[b] + s
+    with seq_row0 the running sum of seq_lens, the layout the functions
+    below take).  Row by row through paged_row."""
+    paged = np.asarray(paged)
+    out = np.empty((int(np.sum(seq_lens)),) + paged.shape[1:], paged.dtype)
+    r = 0
+    for b, n in enumerate(seq_lens):
+        for s in range(int(n)):
+            out[r] = paged[paged_row(block_table, block_rows, b, s)]
+            r += 1
+    return out
+
+
 # ---------------------------------------------------------------- the method
 def indexer_scores(q_idx, w, k_idx, rows, row_pos, row_key0, max_len, *, dtype=0,
                    q_scale=None, k_scale=None, Hi=None, Di=None):

@@ -196,6 +196,89 @@ def test_group_tiny_bit_exact_indices(types):
         assert torch.equal(o, outs[l])
 
 
+def _page(lay, arrays, R, seed, spare=3):
+    """Paged copies of per-position cache arrays (rows in the layout's
+    contiguous order): every sequence's blocks of R positions land in a
+    random permutation of physical blocks, with spare blocks left unused.
+    Returns the block table and the paged arrays."""
+    rng = np.random.default_rng(seed)
+    lens = [int(n) for n in lay.seq_len]
+    nblk = [(n + R - 1) // R for n in lens]
+    bps = lay.max_len // R + (lay.max_len % R != 0)
+    total = sum(nblk) + spare
+    ids = rng.permutation(total)
+    table = np.full((len(lens), bps), -1, np.int32)
+    paged = [np.zeros((total * R,) + a.shape[1:], a.dtype) for a in arrays]
+    k = 0
+    for b, n in enumerate(lens):
+        r0 = int(lay.seq_row0[b])
+        for j in range(nblk[b]):
+            table[b, j] = ids[k]
+            m = min(R, n - j * R)
+            for a, pa in zip(arrays, paged):
+                pa[ids[k] * R: ids[k] * R + m] = a[r0 + j * R: r0 + j * R + m]
+            k += 1
+    return table, paged
+
+
+def test_paged_caches_match_contiguous_and_oracle():
+    # two sequences, blocks of 256 positions scattered over a permuted pool
+    lay = synth.make_layout([700, 400], [300, 200])
+    types, H, K, R = "FSSS", 16, 64, 256
+    host = synth.host_layers(lay, types, H, ints=True, seed=21)
+    keys = ["kv", "k_idx"]
+    table = None
+    paged_host = []
+    for l, L in enumerate(host):
+        arrs = [L[k] for k in keys if k in L]
+        table, parr = _page(lay, arrs, R, seed=22)  # same table for every layer
+        P = dict(L)
+        for k, a in zip([k for k in keys if k in L], parr):
+            P[k] = a
+            # the oracle's row map gives back the logical cache
+            assert np.array_equal(oracle.logical_cache(a, table, R, lay.seq_len), L[k])
+        paged_host.append(P)
+    contiguous = make_batch(dsa, lay, DEV)
+    paged = dsa.Batch(lay.q_start, lay.q_pos, None, lay.max_len, device=DEV, block_table=table,
+                      block_rows=R)
+    results = []
+    for hl, batch in ((host, contiguous), (paged_host, paged)):
+        layers = device_layers(hl, DEV)
+        group = dsa.Group(types, layers, k=K, scale=1 / 16, with_lse=True)
+        ws = dsa.workspace(group.workspace_size(batch), DEV)
+        outs, lses, idx = dsa.indexshare_group_forward(group, batch, ws=ws)
+        torch.cuda.synchronize()
+        dsa.status_fetch(ws)
+        results.append(([o.clone() for o in outs], idx.clone()))
+    (oc, ic), (op, ip) = results
+    assert torch.equal(ic, ip)
+    for a, b_ in zip(oc, op):
+        assert torch.equal(a, b_)
+    rows = np.arange(lay.num_q, dtype=np.int32)
+    pos, key0 = rows_meta(lay, rows)
+    ref = oracle.group_forward(types, host, rows, pos, key0, lay.max_len, K, 1 / 16)
+    assert np.array_equal(ip.cpu().numpy(), ref["idx"][-1])
+    for l in range(len(types)):
+        assert_close(op[l].float().cpu().numpy(), ref["out"][l], 2e-2, f"paged layer {l}")
+
+
+def test_paged_fp8_indexer_scores_match_contiguous():
+    lay = synth.make_layout([1500, 2300], [3, 2])
+    host = synth.host_layers(lay, "F", 16, ints=False, seed=23)[0]
+    qc, qs = oracle.fp8_quantize_rows(host["q_idx"].reshape(-1, 128))
+    kc, ks = oracle.fp8_quantize_rows(host["k_idx"])
+    R = 512
+    table, (kcp, ksp) = _page(lay, [kc, ks], R, seed=24)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    qc_d, qs_d, w_d = T(qc.reshape(lay.num_q, 32, 128)), T(qs.reshape(lay.num_q, 32)), T(host["w"])
+    sc = dsa.dsa_indexer_scores(qc_d, w_d, T(kc), make_batch(dsa, lay, DEV), q_scale=qs_d,
+                                k_scale=T(ks))
+    paged = dsa.Batch(lay.q_start, lay.q_pos, None, lay.max_len, device=DEV, block_table=table,
+                      block_rows=R)
+    scp = dsa.dsa_indexer_scores(qc_d, w_d, T(kcp), paged, q_scale=qs_d, k_scale=T(ksp))
+    assert torch.equal(sc, scp)
+
+
 def test_fp8_quantiser_bit_exact():
     rng = np.random.default_rng(12)
     x = rng.standard_normal((4099, 128)).astype(np.float32) / np.sqrt(128)
@@ -259,4 +342,12 @@ def test_host_argument_errors():
         dsa.dsa_sparse_mla_attn(ql, qr, kv, torch.zeros((3, 64), dtype=torch.int32, device=DEV),
                                 batch, scale=1 / 16)
     assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
+    # paged layout: blocks must be a power of two >= 128 and the table must cover max_len
+    for table, rows in (([[0, 1, 2]], 384), ([[0]], 128), ([[0, 1, 2]], 64)):
+        bad = dsa.Batch(lay.q_start, lay.q_pos, None, lay.max_len, device=DEV,
+                        block_table=np.asarray(table, np.int32), block_rows=rows)
+        with pytest.raises(dsa.DsaError) as e:
+            dsa.dsa_indexer_scores(z, torch.zeros((3, 32), device=DEV),
+                                   torch.zeros((300, 128), dtype=torch.bfloat16, device=DEV), bad)
+        assert e.value.status == dsa.DSA_ERR_INVALID_ARG
     del z
