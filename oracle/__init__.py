@@ -58,6 +58,9 @@ def lib():
             L.oracle_hadamard128_f64.argtypes = [vp, vp]
             L.oracle_fwht128_f32.argtypes = [vp]
             L.oracle_fp8_quantize_rows.argtypes = [vp, i64, vp, vp]
+            L.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+            L.oracle_f64_to_bf16.restype = ctypes.c_uint16
+            L.oracle_rope_bf16.argtypes = [vp, vp, i64, ctypes.c_int, ctypes.c_int, vp, vp]
             L.oracle_indexer_scores.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp,
                                                 vp, vp, vp, vp, vp, vp, ctypes.c_int, i64, vp]
             L.oracle_topk.argtypes = [vp, i64, vp, ctypes.c_int, ctypes.c_int, vp]
@@ -117,6 +120,38 @@ def fp8_quantize_rows(x_bf16_bits):
     lib().oracle_fp8_quantize_rows(px, rows, q.ctypes.data_as(ctypes.c_void_p),
                                    s.ctypes.data_as(ctypes.c_void_p))
     return q, s
+
+
+def f64_to_bf16(x: float) -> int:
+    """One fp64 value rounded to a bf16 bit pattern (nearest, ties to even)."""
+    return int(lib().oracle_f64_to_bf16(float(x)))
+
+
+def rope_inv_freq(theta: float, rope_dims: int = 64) -> np.ndarray:
+    """theta^(-2i/rope_dims), i < rope_dims/2: the rotary frequencies of a
+    base theta (8e6 for GLM-5.2, "GLM-5.2 架构深度拆解" CH 1.1)."""
+    return np.power(float(theta), -2.0 * np.arange(rope_dims // 2) / rope_dims)
+
+
+def rope_bf16(x_bf16_bits, pos, inv_freq, rope_dims: int = 64):
+    """Interleaved RoPE of the first rope_dims entries of each row of x (bf16
+    bits, [n, dim]) at positions pos [n], fp64, rounded once to bf16."""
+    x, px = _c(np.asarray(x_bf16_bits).reshape(len(pos), -1), np.uint16)
+    n, dim = x.shape
+    p, pp = _c(pos, np.int32)
+    f, pf = _c(inv_freq, np.float64)
+    assert f.size >= rope_dims // 2
+    out = np.empty_like(x)
+    lib().oracle_rope_bf16(px, pp, n, dim, rope_dims, pf, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def indexer_append(x_bf16_bits, pos, inv_freq, fp8: bool):
+    """What the cache append writes for indexer vectors (rows of 128): RoPE
+    (rounded to bf16), then for FP8 the Hadamard + E4M3 quantiser.  Returns
+    bf16 bits, or (codes, scales)."""
+    r = rope_bf16(x_bf16_bits, pos, inv_freq, 64)
+    return fp8_quantize_rows(r) if fp8 else r
 
 
 # ---------------------------------------------------------------- batch helpers

@@ -145,6 +145,58 @@ void oracle_fp8_quantize_rows(const uint16_t* x, int64_t rows, uint8_t* q, float
   }
 }
 
+/* ------------------------------------------------------------ RoPE */
+
+/* fp64 -> bf16 bit pattern, rounded once to nearest with ties to even: |x|
+ * is scaled by a power of two (exact) so that the bf16 grid of its binade
+ * becomes the integers (bf16 keeps 8 significant bits; below the normal
+ * range the grid spacing stays 2^-133), rounded with rint (default rounding
+ * mode: nearest, ties to even) and scaled back (exact).  Results beyond the
+ * largest finite bf16 become infinity. */
+uint16_t oracle_f64_to_bf16(double x) {
+  if (isnan(x)) return 0x7FC0;
+  const uint16_t sign = signbit(x) ? 0x8000 : 0;
+  const double a = fabs(x);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e); /* a = m * 2^e, 0.5 <= m < 1 */
+  int es = e - 8;
+  if (es < -133) es = -133;
+  const double y = ldexp(rint(ldexp(a, -es)), es);
+  if (y > 3.3895313892515355e38) return sign | 0x7F80;
+  const float f = (float)y; /* exact: y lies on the bf16 grid */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return sign | (uint16_t)(u >> 16);
+}
+
+/* Interleaved rotary embedding ("GLM-5.2 架构深度拆解" CH 7.1 table: indexer
+ * 32 heads x 128 with indexer_rope_interleave; partial RoPE on a 64-d
+ * subspace, interleaved): each vector of width `dim` at position pos[v] has
+ * its entries (2i, 2i+1), i < rope_dims / 2, rotated by the angle
+ * pos[v] * inv_freq[i]:
+ *   y[2i]   = x[2i] cos a - x[2i+1] sin a
+ *   y[2i+1] = x[2i] sin a + x[2i+1] cos a
+ * in fp64 on the exact bf16 inputs, each result rounded once to bf16; the
+ * entries from rope_dims on are copied.  inv_freq[i] = theta^(-2i/rope_dims)
+ * for the model's base theta, given by the caller. */
+void oracle_rope_bf16(const uint16_t* x, const int32_t* pos, int64_t n, int dim, int rope_dims,
+                      const double* inv_freq, uint16_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t v = 0; v < n; ++v) {
+    const uint16_t* xv = x + v * dim;
+    uint16_t* yv = out + v * dim;
+    for (int i = 0; i < rope_dims / 2; ++i) {
+      const double a = (double)pos[v] * inv_freq[i];
+      const double c = cos(a), s = sin(a);
+      const double x0 = bf16_value(xv[2 * i]), x1 = bf16_value(xv[2 * i + 1]);
+      yv[2 * i] = oracle_f64_to_bf16(x0 * c - x1 * s);
+      yv[2 * i + 1] = oracle_f64_to_bf16(x0 * s + x1 * c);
+    }
+    for (int k = rope_dims; k < dim; ++k) yv[k] = xv[k];
+  }
+}
+
 /* ------------------------------------------------------------ indexer */
 
 /* Lightning-indexer scores for the listed query rows.
