@@ -213,6 +213,41 @@ def page_caches(lay, layers, block_rows, dev, seed=0):
     return table, phys_d
 
 
+def make_appends(lay, layers, cfg, fp8, batch, dev, theta=8e6):
+    """Per F layer, the cache-append work of one step's new tokens: the new
+    indexer queries (pre-RoPE, bf16) are rotated (and FP8-quantised) into the
+    layer's q_idx, and the new tokens' keys are rotated (and quantised) into
+    their cache rows.  Returns the calls and the algorithmic bytes they move."""
+    import math
+
+    import torch
+
+    import dsa_indexer_indexshare_gb300 as dsa
+    freq = np.power(float(theta), -2.0 * np.arange(32) / 64)
+    nq = lay.num_q
+    seq = torch.from_numpy(np.repeat(np.arange(lay.num_seqs), np.diff(lay.q_start)).astype(np.int32)).to(dev)
+    ws = dsa.workspace(256, dev)
+    calls = []
+    nbytes = 0.0
+    for l, L in enumerate(layers):
+        if "q_idx" not in L:
+            continue
+        g = torch.Generator(device=dev)
+        g.manual_seed(9000 + l)
+        q_raw = (torch.randn((nq, 32, 128), generator=g, device=dev) / math.sqrt(128)).to(torch.bfloat16)
+        k_new = (torch.randn((nq, 128), generator=g, device=dev) / math.sqrt(128)).to(torch.bfloat16)
+
+        def call(L=L, q_raw=q_raw, k_new=k_new):
+            dsa.dsa_indexer_prepare_queries(q_raw, batch, freq, fp8=fp8, q_out=L["q_idx"],
+                                            q_scale=L.get("q_scale"), ws=ws)
+            dsa.dsa_indexer_append_keys(k_new, seq, batch.q_pos, batch, L["k_idx"], freq,
+                                        k_scale=L.get("k_scale"), ws=ws)
+        calls.append(call)
+        out = 128 + 4 if fp8 else 256  # bytes written per vector
+        nbytes += nq * 32 * (256 + out) + nq * 4 + nq * (256 + out + 8)
+    return calls, nbytes, ws
+
+
 def setup(workload, dev, seed=0, paged=0):
     import torch
 
@@ -317,6 +352,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0)
+    ap.add_argument("--with-append", action="store_true",
+                    help="each step also rotates (and FP8-quantises) the new tokens' indexer "
+                         "queries and appends their keys to the caches of every F layer")
     ap.add_argument("--paged", type=int, default=0, metavar="ROWS",
                     help="paged caches: blocks of ROWS positions (a multiple of 128) in a "
                          "permuted pool, addressed through a block table")
@@ -369,7 +407,14 @@ def main():
         return out
 
     group, ws, idx_buf = make_group(cfg["layers"])
-    run = lambda: dsa.indexshare_group_forward(group, batch, idx_buf, ws=ws)
+    appends, append_bytes, append_ws = ([], 0.0, None)
+    if args.with_append:
+        appends, append_bytes, append_ws = make_appends(lay, layers, cfg, fp8, batch, dev)
+
+    def run():
+        for a in appends:
+            a()
+        dsa.indexshare_group_forward(group, batch, idx_buf, ws=ws)
 
     def barrier():
         if world > 1:
@@ -408,8 +453,13 @@ def main():
 
     # ---- per-kernel roofline (live CUDA events around each launch)
     work = algorithmic(lay, cfg, fp8)
+    if appends:  # two launches (queries, keys) per F layer per step
+        work["append"] = {"flops": 0.0, "bytes": append_bytes / (2 * len(appends))}
+        dsa.status_fetch(append_ws)
     kernels = {}
-    for name in ("indexer", "topk", "sparse_mla"):
+    for name in ("indexer", "topk", "sparse_mla", "append"):
+        if name not in work or name not in prof:
+            continue
         ms, n = prof[name]
         if n == 0:
             continue
@@ -444,6 +494,8 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "kv_layout": (f"paged: blocks of {args.paged} positions, permuted pool, "
                                      "block table" if args.paged else "contiguous"),
+                       "step": ("indexer query RoPE/FP8 + key cache append per F layer, then the "
+                                "group" if args.with_append else "the group forward"),
                        "l2": "flushed between steps (256 MiB write, outside the timed events)"},
             "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
             "clocks": clocks, "wall_s_timed": round(wall, 3)}

@@ -21,7 +21,8 @@ DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE = 0, 1, 2, 3
 DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX = 4, 5, 6
 DSA_BF16, DSA_FP8_E4M3 = 0, 1
 INDEX_HEADS, INDEX_DIM, LATENT, ROPE, KV_ROW = 32, 128, 512, 64, 576
-LAUNCH_KINDS = ("indexer", "topk", "sparse_mla", "combine", "fp8_quantize", "other")
+STATUS_BYTES = 256
+LAUNCH_KINDS = ("indexer", "topk", "sparse_mla", "combine", "fp8_quantize", "append", "other")
 
 STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
                 3: "DSA_ERR_WORKSPACE", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT",
@@ -82,6 +83,11 @@ def _load():
         "indexshare_group_forward": (st, [POINTER(_Group), B, c_void_p, c_void_p, c_size_t,
                                           c_void_p]),
         "dsa_fp8_quantize": (st, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p]),
+        "dsa_indexer_append_keys": (st, [c_void_p, c_void_p, c_void_p, c_int32, B, c_int,
+                                         c_void_p, c_void_p, c_void_p, c_int64, c_void_p,
+                                         c_size_t, c_void_p]),
+        "dsa_indexer_prepare_queries": (st, [c_void_p, B, c_int, c_void_p, c_void_p, c_void_p,
+                                             c_void_p, c_size_t, c_void_p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -378,3 +384,55 @@ def dsa_fp8_quantize(x, codes=None, scale=None, *, stream=None):
     _check(lib.dsa_fp8_quantize(_ptr(x), rows, _ptr(codes), _ptr(scale), _stream(stream, x.device)),
            "dsa_fp8_quantize")
     return codes, scale
+
+
+def _freq(inv_freq):
+    f = (ctypes.c_double * 32)(*[float(v) for v in list(inv_freq)[:32]])
+    if len(list(inv_freq)) < 32:
+        raise ValueError("inv_freq needs 32 entries")
+    return f
+
+
+def dsa_indexer_append_keys(k_new, k_seq, k_pos, batch: Batch, k_cache, inv_freq, *,
+                            k_scale=None, ws=None, stream=None):
+    """RoPE (+ Hadamard + FP8 when k_cache is uint8) of new indexer keys
+    k_new bf16 [n, 128], written at the cache rows of (k_seq, k_pos) in the
+    batch layout.  inv_freq: 32 rotary frequencies (host sequence)."""
+    dev = batch.device
+    _need(k_new, "k_new", torch.bfloat16, dev)
+    n = k_new.numel() // 128
+    _need(k_seq, "k_seq", torch.int32, dev, (n,))
+    _need(k_pos, "k_pos", torch.int32, dev, (n,))
+    _need(k_cache, "k_cache", (torch.bfloat16, torch.uint8), dev)
+    fp8 = k_cache.dtype == torch.uint8
+    if fp8:
+        _need(k_scale, "k_scale", torch.float32, dev, (k_cache.shape[0],))
+    if ws is None:
+        ws = workspace(STATUS_BYTES, dev)
+    _check(lib.dsa_indexer_append_keys(_ptr(k_new), _ptr(k_seq), _ptr(k_pos), n, batch.c,
+                                       DSA_FP8_E4M3 if fp8 else DSA_BF16, _freq(inv_freq),
+                                       _ptr(k_cache), _ptr(k_scale) if fp8 else None,
+                                       k_cache.shape[0], _ptr(ws), ws.numel(),
+                                       _stream(stream, dev)), "dsa_indexer_append_keys")
+    return k_cache
+
+
+def dsa_indexer_prepare_queries(q_new, batch: Batch, inv_freq, *, fp8=False, q_out=None,
+                                q_scale=None, ws=None, stream=None):
+    """RoPE (+ Hadamard + FP8) of the batch's indexer queries q_new bf16
+    [num_q, 32, 128] at q_pos: returns q_out (bf16, or uint8 codes with
+    q_scale fp32 [num_q, 32])."""
+    dev = batch.device
+    _need(q_new, "q_new", torch.bfloat16, dev, (batch.num_q, INDEX_HEADS, INDEX_DIM))
+    if q_out is None:
+        q_out = torch.empty(q_new.shape, dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    if fp8 and q_scale is None:
+        q_scale = torch.empty((batch.num_q, INDEX_HEADS), dtype=torch.float32, device=dev)
+    _need(q_out, "q_out", torch.uint8 if fp8 else torch.bfloat16, dev, tuple(q_new.shape))
+    if ws is None:
+        ws = workspace(STATUS_BYTES, dev)
+    _check(lib.dsa_indexer_prepare_queries(_ptr(q_new), batch.c, DSA_FP8_E4M3 if fp8 else DSA_BF16,
+                                           _freq(inv_freq), _ptr(q_out),
+                                           _ptr(q_scale) if fp8 else None, _ptr(ws), ws.numel(),
+                                           _stream(stream, dev)), "dsa_indexer_prepare_queries")
+    return (q_out, q_scale) if fp8 else q_out

@@ -404,4 +404,44 @@ dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float
   return launch_status(launch_quantize(x, rows, codes, scale, stream), "quantiser launch");
 }
 
+// ------------------------------------------------------------- NEXT-3: cache append
+dsa_status_t dsa_indexer_append_keys(const void* k_new, const int32_t* k_seq,
+                                     const int32_t* k_pos, int32_t n, const dsa_batch_t* b,
+                                     dsa_dtype_t dt, const double* inv_freq, void* k_cache,
+                                     float* k_scale, int64_t k_rows, void* ws, size_t ws_bytes,
+                                     dsa_stream_t stream) {
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (n < 0) return fail(DSA_ERR_INVALID_ARG, "n < 0");
+  if (dt != DSA_BF16 && dt != DSA_FP8_E4M3) return fail(DSA_ERR_UNSUPPORTED, "dtype");
+  if (!inv_freq) return fail(DSA_ERR_INVALID_ARG, "inv_freq (32 host doubles) is required");
+  if (n > 0 && (!k_new || !k_seq || !k_pos || !k_cache || (dt == DSA_FP8_E4M3 && !k_scale)))
+    return fail(DSA_ERR_INVALID_ARG, "k_new, k_seq, k_pos, k_cache (and k_scale for FP8) are required");
+  if (n > 0 && (!aligned16(k_new) || !aligned16(k_cache)))
+    return fail(DSA_ERR_INVALID_ARG, "k_new and k_cache must be 16-byte aligned");
+  if (k_rows < 1) return fail(DSA_ERR_INVALID_ARG, "k_rows < 1");
+  if (dsa_status_t s = check_ws(ws, ws_bytes, kStatusBytes)) return s;
+  return launch_status(launch_rope_append(k_new, n, 1, k_pos, k_seq, *b, inv_freq,
+                                          dt == DSA_FP8_E4M3, k_cache, k_scale, k_rows,
+                                          static_cast<int*>(ws), stream),
+                       "append launch");
+}
+
+dsa_status_t dsa_indexer_prepare_queries(const void* q_new, const dsa_batch_t* b, dsa_dtype_t dt,
+                                         const double* inv_freq, void* q_out, float* q_scale,
+                                         void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (dt != DSA_BF16 && dt != DSA_FP8_E4M3) return fail(DSA_ERR_UNSUPPORTED, "dtype");
+  if (!inv_freq) return fail(DSA_ERR_INVALID_ARG, "inv_freq (32 host doubles) is required");
+  if (b->num_q > 0 && (!q_new || !q_out || (dt == DSA_FP8_E4M3 && !q_scale)))
+    return fail(DSA_ERR_INVALID_ARG, "q_new, q_out (and q_scale for FP8) are required");
+  if (b->num_q > 0 && (!aligned16(q_new) || !aligned16(q_out)))
+    return fail(DSA_ERR_INVALID_ARG, "q_new and q_out must be 16-byte aligned");
+  if (dsa_status_t s = check_ws(ws, ws_bytes, kStatusBytes)) return s;
+  const int64_t nv = static_cast<int64_t>(b->num_q) * DSA_INDEX_HEADS;
+  return launch_status(launch_rope_append(q_new, nv, DSA_INDEX_HEADS, b->q_pos, nullptr, *b,
+                                          inv_freq, dt == DSA_FP8_E4M3, q_out, q_scale, nv,
+                                          static_cast<int*>(ws), stream),
+                       "query preparation launch");
+}
+
 }  // extern "C"

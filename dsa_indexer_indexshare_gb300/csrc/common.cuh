@@ -75,7 +75,7 @@ void prof_end(int which, cudaStream_t stream);
 uint64_t wait_timeout_ns();
 
 enum LaunchKind { kLaunchIndexer = 0, kLaunchTopk, kLaunchMla, kLaunchCombine, kLaunchQuant,
-                  kLaunchOther, kNumLaunchKinds };
+                  kLaunchAppend, kLaunchOther, kNumLaunchKinds };
 
 // Launchers (return a CUDA error code; argument checks are done by api.cu).
 cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float* w,
@@ -90,6 +90,13 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
                               const dsa_batch_t& b, void* out, float* lse, void* ws_extra,
                               size_t ws_extra_bytes, int* status, cudaStream_t stream);
+// RoPE (+ Hadamard + FP8) of n indexer vectors; vector v at position
+// pos_of[v / group], written to the cache row of (seq_of[v / group], pos)
+// (seq_of set) or to row v.  inv_freq: 32 host doubles.
+cudaError_t launch_rope_append(const void* x, int64_t n, int group, const int32_t* pos_of,
+                               const int32_t* seq_of, const dsa_batch_t& b, const double* inv_freq,
+                               bool fp8, void* out, float* out_scale, int64_t out_rows, int* status,
+                               cudaStream_t stream);
 cudaError_t launch_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
                             cudaStream_t stream);
 cudaError_t launch_selftest_wait(int* status, cudaStream_t stream);

@@ -20,15 +20,10 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
   return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
 
-__global__ void __launch_bounds__(256) fp8_quant_kernel(const uint16_t* __restrict__ x,
-                                                        int64_t rows, uint8_t* __restrict__ codes,
-                                                        float* __restrict__ scale) {
-  const int lane = threadIdx.x & 31;
-  const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  const uint2 raw = *reinterpret_cast<const uint2*>(x + r * 128 + lane * 4);
-  float v[4] = {bf16_bits_to_float(raw.x & 0xFFFF), bf16_bits_to_float(raw.x >> 16),
-                bf16_bits_to_float(raw.y & 0xFFFF), bf16_bits_to_float(raw.y >> 16)};
+// Hadamard rotation + FP8 quantisation of one 128-vector held by a warp
+// (lane l: elements 4l .. 4l+3), codes and scale stored at the given row.
+__device__ __forceinline__ void hadamard_quant_store(float (&v)[4], int lane, uint8_t* codes_row,
+                                                     float* scale_slot) {
   // h = 1: (0,1), (2,3)
   {
     const float a0 = v[0], b0 = v[1], a1 = v[2], b1 = v[3];
@@ -71,8 +66,102 @@ __global__ void __launch_bounds__(256) fp8_quant_kernel(const uint16_t* __restri
     const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(__fdiv_rn(v[k], sc), __NV_SATFINITE, __NV_E4M3);
     packed |= static_cast<uint32_t>(c) << (8 * k);
   }
-  *reinterpret_cast<uint32_t*>(codes + r * 128 + lane * 4) = packed;
-  if (lane == 0) scale[r] = sc;
+  *reinterpret_cast<uint32_t*>(codes_row + lane * 4) = packed;
+  if (lane == 0) *scale_slot = sc;
+}
+
+__global__ void __launch_bounds__(256) fp8_quant_kernel(const uint16_t* __restrict__ x,
+                                                        int64_t rows, uint8_t* __restrict__ codes,
+                                                        float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const uint2 raw = *reinterpret_cast<const uint2*>(x + r * 128 + lane * 4);
+  float v[4] = {bf16_bits_to_float(raw.x & 0xFFFF), bf16_bits_to_float(raw.x >> 16),
+                bf16_bits_to_float(raw.y & 0xFFFF), bf16_bits_to_float(raw.y >> 16)};
+  hadamard_quant_store(v, lane, codes + r * 128, scale + r);
+}
+
+// fp64 -> bf16 bits, one rounding to nearest (ties to even).  The double is
+// first narrowed to fp32 with round-to-odd (toward zero, then the lowest bit
+// set when anything was dropped), then the fp32 value is rounded to bf16
+// with ties to even; because fp32 keeps 16 more bits than bf16, this double
+// rounding equals the single correct rounding (the round-to-odd argument).
+__device__ __forceinline__ uint16_t f64_to_bf16_bits(double x) {
+  if (x != x) return 0x7FC0;
+  const float fz = __double2float_rz(x);
+  uint32_t u = __float_as_uint(fz);
+  if (static_cast<double>(fz) != x) u |= 1u;  // sticky: inexact narrowing
+  if ((u & 0x7F800000u) == 0x7F800000u) return static_cast<uint16_t>(u >> 16);  // +-inf
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+struct RopeFreq {
+  double f[32];  // theta^(-2i/64), the rotary frequencies of the first 64 dims
+};
+
+// Indexer cache append / query preparation ("GLM-5.2 架构深度拆解" CH 7.1:
+// interleaved RoPE of the indexer vectors; then the FP8 per-block quantiser
+// above).  Warp w takes the `group` vectors w*group .. w*group+group-1 (of
+// the 32 heads of a query, or one key), all at position pos_of[w / split]
+// (`split` warps share a position), so the fp64 sin/cos of the 32 angles
+// pos * f[i] are computed once per warp.  The pairs (2i, 2i+1) of the first 64 entries are
+// rotated in fp64 and rounded once to bf16 (lanes 0..15 hold them), entries
+// 64.. are copied; the result is stored as bf16 or, FP8, Hadamard-rotated and
+// quantised.  Destination row: the cache row of (seq_of[w], pos) in the batch
+// layout when seq_of is set (keys), else the vector's index (queries).
+template <bool FP8>
+__global__ void __launch_bounds__(256) rope_append_kernel(
+    const uint16_t* __restrict__ x, int64_t npos, int group, int split,
+    const int32_t* __restrict__ pos_of,
+    const int32_t* __restrict__ seq_of, BatchArgs b, RopeFreq rf, uint16_t* __restrict__ out_bf16,
+    uint8_t* __restrict__ out_codes, float* __restrict__ out_scale, int64_t out_rows, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (w >= npos) return;
+  const int pos = pos_of[w / split];
+  int64_t row0 = w * group;
+  if (seq_of) {
+    const int seq = seq_of[w / split];
+    row0 = (seq >= 0 && seq < b.num_seqs && pos >= 0)
+               ? cache_row(b, seq, seq_base_row(b, seq), pos)
+               : -1;
+  }
+  if (pos < 0 || row0 < 0 || row0 + group > out_rows) {  // uniform over the warp
+    if (lane == 0) atomicOr(status, DSA_DEVERR_INDEX);
+    return;
+  }
+  double sn[2] = {0.0, 0.0}, cs[2] = {1.0, 1.0};
+  if (lane < 16) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) sincos(static_cast<double>(pos) * rf.f[2 * lane + q], &sn[q], &cs[q]);
+  }
+#pragma unroll 1
+  for (int k = 0; k < group; ++k) {
+    const int64_t v = w * group + k, row = row0 + k;
+    const uint2 raw = *reinterpret_cast<const uint2*>(x + v * 128 + lane * 4);
+    uint16_t h[4] = {static_cast<uint16_t>(raw.x & 0xFFFF), static_cast<uint16_t>(raw.x >> 16),
+                     static_cast<uint16_t>(raw.y & 0xFFFF), static_cast<uint16_t>(raw.y >> 16)};
+    if (lane < 16) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const double x0 = bf16_bits_to_float(h[2 * q]), x1 = bf16_bits_to_float(h[2 * q + 1]);
+        h[2 * q] = f64_to_bf16_bits(__dsub_rn(__dmul_rn(x0, cs[q]), __dmul_rn(x1, sn[q])));
+        h[2 * q + 1] = f64_to_bf16_bits(__dadd_rn(__dmul_rn(x0, sn[q]), __dmul_rn(x1, cs[q])));
+      }
+    }
+    if constexpr (!FP8) {
+      uint2 o;
+      o.x = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
+      o.y = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16);
+      *reinterpret_cast<uint2*>(out_bf16 + row * 128 + lane * 4) = o;
+    } else {
+      float vv[4] = {bf16_bits_to_float(h[0]), bf16_bits_to_float(h[1]),
+                     bf16_bits_to_float(h[2]), bf16_bits_to_float(h[3])};
+      hadamard_quant_store(vv, lane, out_codes + row * 128, out_scale + row);
+    }
+  }
 }
 
 // One CTA waits on an mbarrier that nothing arrives on; the bounded wait
@@ -101,6 +190,34 @@ cudaError_t launch_quantize(const void* x, int64_t rows, uint8_t* codes, float* 
       static_cast<const uint16_t*>(x), rows, codes, scale);
   prof_end(kLaunchQuant, stream);
   count_launch(kLaunchQuant);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_append(const void* x, int64_t n, int group, const int32_t* pos_of,
+                               const int32_t* seq_of, const dsa_batch_t& b, const double* inv_freq,
+                               bool fp8, void* out, float* out_scale, int64_t out_rows, int* status,
+                               cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  RopeFreq rf;
+  for (int i = 0; i < 32; ++i) rf.f[i] = inv_freq[i];
+  // few positions (decode): split a position's vectors over up to 8 warps
+  // (each recomputes the 32 sin/cos), so that more warps are in flight
+  int split = 1;
+  while (split < 8 && group % (split * 2) == 0 && (n / group) * split * 2 <= 8 * 152) split *= 2;
+  group /= split;
+  const int64_t npos = n / group;
+  const int64_t blocks = (npos + 7) / 8;
+  prof_begin(stream);
+  if (fp8)
+    rope_append_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(x), npos, group, split, pos_of, seq_of, to_args(b), rf, nullptr,
+        static_cast<uint8_t*>(out), out_scale, out_rows, status);
+  else
+    rope_append_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(x), npos, group, split, pos_of, seq_of, to_args(b), rf,
+        static_cast<uint16_t*>(out), nullptr, nullptr, out_rows, status);
+  prof_end(kLaunchAppend, stream);
+  count_launch(kLaunchAppend);
   return cudaGetLastError();
 }
 

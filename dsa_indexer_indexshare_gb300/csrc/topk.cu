@@ -591,15 +591,15 @@ __global__ void __launch_bounds__(kFinBS) topk_finish_kernel(const float* __rest
 // ------------------------------------------------------------------ many long rows
 // Many long rows (chunked prefill: thousands of rows of 128K+ positions).
 // One CTA per SM loops over rows and normally reads each row from HBM once:
-//  1. a 12-bit histogram of the order keys of the row's first kPrefix
-//     positions gives a cutoff bin that leaves about twice the prefix's share
-//     of K above it;
+//  1. a 12-bit histogram of the order keys of kPrefix positions sampled in
+//     16 runs spread over the row gives a cutoff bin that leaves about 1.5
+//     times the sample's share of K above it;
 //  2. one pass over the row keeps every key in a bin >= the cutoff, with its
 //     position, in shared memory.  With at least K keys kept (and none
 //     dropped) the k-th largest key is >= the cutoff, so every key the
 //     selection needs is kept, and the threshold bin (the one holding the
 //     k-th largest key) follows from a histogram of the kept keys;
-//  3. otherwise (an unrepresentative prefix, or a buffer overflow from many
+//  3. otherwise (an unrepresentative sample, or a buffer overflow from many
 //     equal keys) the whole row is histogrammed and a second pass collects
 //     the positions above the threshold bin and its members.
 // The threshold bin's members are resolved as in the finish kernel above,
@@ -615,11 +615,11 @@ constexpr int kHCopies = 8;
 constexpr int kHStride = kHBins + 4;                      // words between histogram copies
 constexpr int kRegionA = kHCopies * kHStride;             // words: copies, later hist + bitmap
 constexpr int kBitWords = 28672;                          // bitmap: rows up to 917,504 positions
-constexpr int kSeg = 256;                                 // buffered keys per warp
+constexpr int kSeg = 352;                                 // buffered keys per warp
 constexpr int kRowCand = kRowWarps * kSeg;                // buffer slots (warp segments)
-constexpr int kPrefix = 16384;      // positions whose histogram sets the capture cutoff
+constexpr int kPrefix = 16384;      // sampled positions whose histogram sets the capture cutoff
 constexpr int kPrefixSlack = 64;
-constexpr int kRowDynBytes = (kRegionA + 2 * kRowCand) * 4;  // 196,736 B: one CTA per SM
+constexpr int kRowDynBytes = (kRegionA + 2 * kRowCand) * 4;  // 221,312 B: one CTA per SM
 static_assert(kHBins + kBitWords <= kRegionA, "merged histogram + bitmap fit the copies' space");
 
 // Visit positions [0, hi) of a row: f(s, order key, valid) for every
@@ -681,7 +681,7 @@ __global__ void __launch_bounds__(kRowBS, 1) topk_rows_kernel(const float* __res
   };
   // warp-segmented buffer: slot i holds an entry when i % kSeg < its warp's count
   auto buf_key = [&](int i) -> uint32_t {
-    return (i & (kSeg - 1)) < s_wcnt[i / kSeg] ? ckey[i] : ~0u;
+    return (i % kSeg) < s_wcnt[i / kSeg] ? ckey[i] : ~0u;
   };
 #pragma unroll 1
   for (int t = blockIdx.x; t < b.num_q; t += gridDim.x) {
@@ -701,18 +701,34 @@ __global__ void __launch_bounds__(kRowBS, 1) topk_rows_kernel(const float* __res
       s_cut = 0;  // no bin found below: keep everything (overflows, second pass)
     }
     __syncthreads();
-    // ---- pass 1a: histogram of the row's first kPrefix positions; a cutoff
-    // bin leaving about twice the prefix's share of K above it follows
+    // ---- pass 1a: histogram of a sample of kPrefix positions, 16 runs of
+    // kPrefix/16 spread evenly over the row (the whole row when shorter), so
+    // that scores that drift with position are sampled everywhere; a cutoff
+    // bin leaving about 1.5 times the sample's share of K above it follows
     const int P0 = min(len, kPrefix);
+    {
+      constexpr int kRun = kPrefix / 16;
+      const bool whole = len <= kPrefix;
+      const int stride = (len / 16) & ~3;  // run starts stay float4-aligned
+#pragma unroll 4
+      for (int v = tid * 4; v < P0; v += kRowBS * 4) {
+        const int s = whole ? v : (v / kRun) * stride + (v % kRun);
+        const float4 x = *reinterpret_cast<const float4*>(row + s);
+        atomicAdd(&hmine[order_key(x.x) >> 20], 1u);
+        if (s + 1 < len) atomicAdd(&hmine[order_key(x.y) >> 20], 1u);
+        if (s + 2 < len) atomicAdd(&hmine[order_key(x.z) >> 20], 1u);
+        if (s + 3 < len) atomicAdd(&hmine[order_key(x.w) >> 20], 1u);
+      }
+    }
     auto count = [&](int, float x, bool valid) {
       if (valid) atomicAdd(&hmine[order_key(x) >> 20], 1u);
     };
-    scan_row<kRowBS, 4>(row, P0, count);
     __syncthreads();
     sum_copies();
     __syncthreads();
     const int need_p =
-        static_cast<int>(2 * static_cast<int64_t>(K) * P0 / len) + kPrefixSlack;
+        static_cast<int>(3 * static_cast<int64_t>(K) * P0 / (2 * static_cast<int64_t>(len))) +
+        kPrefixSlack;
     threshold_bin<kRowBS>(hist, need_p, warp_sums, &s_cut, &s_d);
     const uint32_t cut = static_cast<uint32_t>(s_cut);
     // ---- pass 1b: every key of the row in a bin >= cut into this warp's

@@ -280,6 +280,45 @@ DSA_API dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_ba
 DSA_API dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
                               dsa_stream_t stream);
 
+/* ------------------------------------------------------------------ NEXT-3: cache append */
+
+/*
+ * The step just before a1 for new tokens: interleaved RoPE of the indexer
+ * vectors ("GLM-5.2 架构深度拆解" CH 7.1: indexer 32 heads x 128 with
+ * indexer_rope_interleave; partial RoPE on a 64-d subspace, interleaved;
+ * CH 1.1: rope_theta 8,000,000), then, for the FP8 indexer, the quantiser of
+ * dsa_fp8_quantize.  Entries (2i, 2i+1), i < 32, of a 128-vector at position
+ * p are rotated by the angle p * inv_freq[i]:
+ *   y[2i] = x[2i] cos a - x[2i+1] sin a,  y[2i+1] = x[2i] sin a + x[2i+1] cos a
+ * computed in fp64 on the bf16 inputs and rounded once to bf16 (nearest,
+ * ties to even); entries 64..127 are copied.  inv_freq: 32 host doubles,
+ * theta^(-2i/64) for the model's base theta (passed in so that every
+ * implementation rotates by the same angles).
+ *
+ * dsa_indexer_append_keys: n new keys, k_new bf16 [n, 128]; key i belongs to
+ * sequence k_seq[i] at position k_pos[i] (device int32 [n]) and is written at
+ * that position's cache row in the batch layout (contiguous or paged):
+ * k_cache bf16 [k_rows, 128], or E4M3 codes uint8 [k_rows, 128] with
+ * k_scale fp32 [k_rows] for dt = FP8.  A key whose row is outside
+ * [0, k_rows) (or unmapped) is skipped and raises DSA_ERR_DEVICE_INDEX.
+ *
+ * dsa_indexer_prepare_queries: q_new bf16 [num_q, 32, 128], every head of
+ * query t rotated at q_pos[t]; q_out bf16 [num_q, 32, 128], or E4M3 codes
+ * with q_scale fp32 [num_q, 32].
+ *
+ * Inputs and outputs must not overlap; pointers to vectors 16-byte aligned.
+ * ws: the status block (dsa_status_bytes()).
+ */
+DSA_API dsa_status_t dsa_indexer_append_keys(const void* k_new, const int32_t* k_seq,
+                                     const int32_t* k_pos, int32_t n, const dsa_batch_t* b,
+                                     dsa_dtype_t dt, const double* inv_freq, void* k_cache,
+                                     float* k_scale, int64_t k_rows, void* ws, size_t ws_bytes,
+                                     dsa_stream_t stream);
+DSA_API dsa_status_t dsa_indexer_prepare_queries(const void* q_new, const dsa_batch_t* b,
+                                         dsa_dtype_t dt, const double* inv_freq, void* q_out,
+                                         float* q_scale, void* ws, size_t ws_bytes,
+                                         dsa_stream_t stream);
+
 /* ------------------------------------------------------------------ no workspace */
 
 /*

@@ -94,3 +94,36 @@ def test_launch_counters_and_timeout_setter(dsa):
     dsa.launch_counts_reset()
     assert set(dsa.launch_counts().values()) == {0}
     dsa.set_wait_timeout_ns(2_000_000_000)
+
+
+def test_append_and_paged_argument_errors_without_a_device(dsa):
+    L = dsa.lib
+    fake = ctypes.c_void_p(4096)
+    b = _batch(dsa)
+    freq = (ctypes.c_double * 32)(*([1.0] * 32))
+    # no rotary frequencies
+    assert L.dsa_indexer_append_keys(fake, fake, fake, 4, ctypes.byref(b), dsa.DSA_BF16, None, fake,
+                                     None, 100, fake, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    assert b"inv_freq" in L.dsa_last_error_string()
+    # negative count, unknown dtype, FP8 without scales, misaligned keys
+    assert L.dsa_indexer_append_keys(fake, fake, fake, -1, ctypes.byref(b), dsa.DSA_BF16, freq,
+                                     fake, None, 100, fake, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_indexer_append_keys(fake, fake, fake, 4, ctypes.byref(b), 7, freq, fake, None, 100,
+                                     fake, 256, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_indexer_append_keys(fake, fake, fake, 4, ctypes.byref(b), dsa.DSA_FP8_E4M3, freq,
+                                     fake, None, 100, fake, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_indexer_append_keys(ctypes.c_void_p(4100), fake, fake, 4, ctypes.byref(b),
+                                     dsa.DSA_BF16, freq, fake, None, 100, fake, 256,
+                                     None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_indexer_prepare_queries(fake, ctypes.byref(b), dsa.DSA_FP8_E4M3, freq, fake, None,
+                                         fake, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    # paged layout: block size not a power of two >= 128, table too short for max_len
+    for rows, per_seq in ((384, 4), (64, 4), (128, 1)):
+        pb = dsa._Batch(1, 4, 4, 256, fake, fake, None, fake, rows, per_seq)
+        assert L.dsa_topk(fake, ctypes.byref(pb), 16, fake, fake, 256,
+                          None) == dsa.DSA_ERR_INVALID_ARG
+    # a paged batch needs no seq_row0; a contiguous one does
+    ok = dsa._Batch(1, 0, 0, 256, fake, fake, None, fake, 128, 2)
+    assert L.dsa_topk(fake, ctypes.byref(ok), 16, fake, fake, 256, None) == dsa.DSA_OK
+    nob = dsa._Batch(1, 0, 0, 256, fake, fake, None)
+    assert L.dsa_topk(fake, ctypes.byref(nob), 16, fake, fake, 256, None) == dsa.DSA_ERR_INVALID_ARG
