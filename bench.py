@@ -473,6 +473,17 @@ def main():
     ktot = sum(v["ms_per_launch"] * v["launches"] for v in kernels.values())
     for v in kernels.values():
         v["share"] = round(v["ms_per_launch"] * v["launches"] / ktot, 4) if ktot else None
+    # HBM-bound (decode) groups: the index scan and the sparse gathers of the
+    # step together, algorithmic bytes over their summed launch times
+    scan_gather = None
+    if all(kernels.get(k, {}).get("bound") == "hbm" for k in ("indexer", "sparse_mla")):
+        byt = sum(work[k]["bytes"] * kernels[k]["launches"] for k in ("indexer", "sparse_mla"))
+        sec = sum(kernels[k]["ms_per_launch"] * kernels[k]["launches"] / 1e3
+                  for k in ("indexer", "sparse_mla"))
+        ach = byt / sec / 1e9
+        scan_gather = {"achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                       "frac": round(ach / peaks["hbm"], 4),
+                       "what": "indexer scans + sparse-MLA gathers of the timed steps"}
     top = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"])
     tk = kernels[top]
     traffic = None
@@ -498,6 +509,7 @@ def main():
                                 "group" if args.with_append else "the group forward"),
                        "l2": "flushed between steps (256 MiB write, outside the timed events)"},
             "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
+            "scan_gather_hbm": scan_gather,
             "clocks": clocks, "wall_s_timed": round(wall, 3)}
 
     # ---- IndexShare ablation: every layer runs its own indexer
