@@ -524,9 +524,59 @@ __device__ void sort_positions(int32_t* buf, int K) {
   }
 }
 
-__global__ void __launch_bounds__(kFinBS) topk_finish_kernel(const float* __restrict__ scores,
+// Write the positions marked in bits[0, nwords) to out[0, K) in ascending
+// order.  Each warp owns a contiguous segment of words and reads it 32
+// consecutive words at a time (no bank conflicts), a warp prefix sum placing
+// each lane's positions; warp segments are ordered by a scan of their counts.
+// Flags DSA_DEVERR_BATCH when the bitmap does not hold exactly K positions.
+// Ends with a CTA barrier.
+template <int BS>
+__device__ void bitmap_compact(const uint32_t* bits, int nwords, int K, int32_t* out,
+                               int* warp_sums, int* status) {
+  constexpr int NW = BS / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (nwords + NW - 1) / NW;
+  const int w0 = min(warp * per, nwords), w1 = min(w0 + per, nwords);
+  int cnt = 0;
+  for (int w = w0 + lane; w < w1; w += 32) cnt += __popc(bits[w]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  __syncthreads();  // warp_sums may still be read by the caller's last scan
+  if (lane == 0) warp_sums[warp] = cnt;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int i = 0; i < NW; ++i) {
+    const int v = warp_sums[i];
+    base += i < warp ? v : 0;
+    total += v;
+  }
+  if (threadIdx.x == 0 && total != K) atomicOr(status, DSA_DEVERR_BATCH);
+  for (int c0 = w0; c0 < w1; c0 += 32) {
+    const int w = c0 + lane;
+    uint32_t m = w < w1 ? bits[w] : 0u;
+    const int n = __popc(m);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int slot = base + incl - n;
+    while (m) {
+      const int bit = __ffs(m) - 1;
+      m &= m - 1;
+      if (slot < K) out[slot] = w * 32 + bit;
+      ++slot;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kFinBS, 1) topk_finish_kernel(const float* __restrict__ scores,
                                                              BatchArgs b, int K, LongScratch ws,
-                                                             int32_t* idx, int* status) {
+                                                             int32_t* idx, int* status,
+                                                             int dyn_words) {
   __shared__ int hist2[2048];
   __shared__ int warp_sums[32];
   __shared__ int s_d, s_above, s_n;
@@ -582,10 +632,25 @@ __global__ void __launch_bounds__(kFinBS) topk_finish_kernel(const float* __rest
     }
   }
   __syncthreads();
-  // ascending order
-  for (int i = tid; i < K; i += kFinBS) sorted[i] = out[i];
-  sort_positions<kFinBS>(sorted, K);
-  for (int i = tid; i < K; i += kFinBS) out[i] = sorted[i];
+  // ascending order: the K positions marked in a bitmap over the row (in the
+  // candidate arrays' space, no longer needed) and compacted in order by one
+  // prefix scan; rows beyond the bitmap's reach are sorted instead
+  const int nwords = (len + 31) >> 5;
+  if (nwords <= dyn_words) {
+    uint32_t* bits = fin_dyn;
+    for (int i = tid; i < nwords; i += kFinBS) bits[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < K; i += kFinBS) {
+      const int p = out[i];
+      if (p >= 0 && p < len) atomicOr(&bits[p >> 5], 1u << (p & 31));
+    }
+    __syncthreads();
+    bitmap_compact<kFinBS>(bits, nwords, K, out, warp_sums, status);
+  } else {
+    for (int i = tid; i < K; i += kFinBS) sorted[i] = out[i];
+    sort_positions<kFinBS>(sorted, K);
+    for (int i = tid; i < K; i += kFinBS) out[i] = sorted[i];
+  }
 }
 
 // ------------------------------------------------------------------ many long rows
@@ -859,23 +924,7 @@ __global__ void __launch_bounds__(kRowBS, 1) topk_rows_kernel(const float* __res
     }
     __syncthreads();
     if (use_bits) {
-      // ascending compaction: thread tid owns words [tid * wpt, tid * wpt + wpt)
-      const int wpt = (nwords + kRowBS - 1) / kRowBS;
-      const int w0 = min(tid * wpt, nwords), w1 = min(w0 + wpt, nwords);
-      int c = 0;
-      for (int w = w0; w < w1; ++w) c += __popc(bits[w]);
-      int total;
-      int slot = block_excl_scan<kRowBS>(c, warp_sums, &total);
-      if (tid == 0 && total != K) atomicOr(status, DSA_DEVERR_BATCH);
-      for (int w = w0; w < w1; ++w) {
-        uint32_t m = bits[w];
-        while (m) {
-          const int bit = __ffs(m) - 1;
-          m &= m - 1;
-          if (slot < K) out[slot] = w * 32 + bit;
-          ++slot;
-        }
-      }
+      bitmap_compact<kRowBS>(bits, nwords, K, out, warp_sums, status);
     } else {
       if (tid == 0 && s_ns != K) atomicOr(status, DSA_DEVERR_BATCH);
       sort_positions<kRowBS>(sel, K);
@@ -979,18 +1028,23 @@ cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_
     prof_begin(stream);
     topk_hist_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws);
     topk_select_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws, idx);
+    // dynamic shared memory: the candidate arrays, or the row's position
+    // bitmap when larger (up to 200 KB: with the static 8 KB, inside 227 KB)
+    const size_t bitmap_bytes = ((static_cast<size_t>(b.max_len) + 31) / 32) * 4;
+    const size_t fin_bytes = std::max<size_t>(kFinDynBytes, std::min<size_t>(bitmap_bytes, 200 << 10));
     {
       static int configured_device = -1;
       int dev = 0;
       cudaGetDevice(&dev);
       if (configured_device != dev) {
         e = cudaFuncSetAttribute(topk_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kFinDynBytes);
+                                 200 << 10);
         if (e != cudaSuccess) return e;
         configured_device = dev;
       }
     }
-    topk_finish_kernel<<<b.num_q, kFinBS, kFinDynBytes, stream>>>(scores, a, k, ws, idx, status);
+    topk_finish_kernel<<<b.num_q, kFinBS, fin_bytes, stream>>>(scores, a, k, ws, idx, status,
+                                                                static_cast<int>(fin_bytes / 4));
     prof_end(kLaunchTopk, stream);
     count_launch(kLaunchTopk);
     count_launch(kLaunchTopk);
