@@ -61,6 +61,8 @@ def lib():
             L.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
             L.oracle_f64_to_bf16.restype = ctypes.c_uint16
             L.oracle_rope_bf16.argtypes = [vp, vp, i64, ctypes.c_int, ctypes.c_int, vp, vp]
+            L.oracle_kv_fp8_quantize.argtypes = [vp, i64, vp]
+            L.oracle_kv_fp8_dequantize.argtypes = [vp, i64, vp]
             L.oracle_indexer_scores.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp,
                                                 vp, vp, vp, vp, vp, vp, ctypes.c_int, i64, vp]
             L.oracle_topk.argtypes = [vp, i64, vp, ctypes.c_int, ctypes.c_int, vp]
@@ -152,6 +154,26 @@ def indexer_append(x_bf16_bits, pos, inv_freq, fp8: bool):
     bf16 bits, or (codes, scales)."""
     r = rope_bf16(x_bf16_bits, pos, inv_freq, 64)
     return fp8_quantize_rows(r) if fp8 else r
+
+
+def kv_fp8_quantize(kv_bf16_bits):
+    """bf16 KV rows [rows, 576] -> FP8 KV rows uint8 [rows, 656]: four groups
+    of 128 latent dims as E4M3 codes, four fp32 scales, the bf16 RoPE key."""
+    x, px = _c(np.asarray(kv_bf16_bits).reshape(-1, 576), np.uint16)
+    rows = x.shape[0]
+    out = np.empty((rows, 656), np.uint8)
+    lib().oracle_kv_fp8_quantize(px, rows, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def kv_fp8_dequantize(kv_fp8):
+    """FP8 KV rows uint8 [rows, 656] -> the bf16 rows [rows, 576] (bits) the
+    attention reads: code * scale rounded once to bf16, the RoPE key as is."""
+    x, px = _c(np.asarray(kv_fp8).reshape(-1, 656), np.uint8)
+    rows = x.shape[0]
+    out = np.empty((rows, 576), np.uint16)
+    lib().oracle_kv_fp8_dequantize(px, rows, out.ctypes.data_as(ctypes.c_void_p))
+    return out
 
 
 # ---------------------------------------------------------------- batch helpers

@@ -197,6 +197,55 @@ void oracle_rope_bf16(const uint16_t* x, const int32_t* pos, int64_t n, int dim,
   }
 }
 
+/* ------------------------------------------------------------ FP8 KV latent */
+
+/* FP8 KV cache row (656 bytes per position; "GLM-5.2 / 总览" config table:
+ * per-token per-layer KV cache BF16 = 1152 B, FP8 ~656 B per-group): the
+ * 512-d latent as E4M3 codes in four groups of 128 dims, each with its own
+ * fp32 scale amax/448 (1 for an all-zero group), then the 64-d RoPE key kept
+ * in bf16:  bytes [0, 512) codes, [512, 528) four fp32 scales,
+ * [528, 656) 64 bf16.  Codes are decided in fp32 (x / scale, E4M3 round to
+ * nearest even, saturating), as by the quantiser that writes the cache. */
+void oracle_kv_fp8_quantize(const uint16_t* kv, int64_t rows, uint8_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* x = kv + r * 576;
+    uint8_t* o = out + r * 656;
+    for (int g = 0; g < 4; ++g) {
+      float amax = 0.0f;
+      for (int j = 0; j < 128; ++j) {
+        const float m = fabsf((float)bf16_value(x[128 * g + j]));
+        if (m > amax) amax = m;
+      }
+      volatile float sc = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+      memcpy(o + 512 + 4 * g, (const void*)&sc, 4);
+      for (int j = 0; j < 128; ++j) {
+        volatile float y = (float)bf16_value(x[128 * g + j]) / sc;
+        o[128 * g + j] = oracle_e4m3_encode(y);
+      }
+    }
+    memcpy(o + 528, x + 512, 128);
+  }
+}
+
+/* The bf16 row the attention reads from an FP8 KV row: latent value =
+ * code * scale, the exact product (4 + 24 significant bits, exact in fp64)
+ * rounded once to bf16; the RoPE key as stored. */
+void oracle_kv_fp8_dequantize(const uint8_t* in, int64_t rows, uint16_t* kv) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint8_t* o = in + r * 656;
+    uint16_t* x = kv + r * 576;
+    for (int g = 0; g < 4; ++g) {
+      float sc;
+      memcpy(&sc, o + 512 + 4 * g, 4);
+      for (int j = 0; j < 128; ++j)
+        x[128 * g + j] = oracle_f64_to_bf16(oracle_e4m3_decode(o[128 * g + j]) * (double)sc);
+    }
+    memcpy(x + 512, o + 528, 128);
+  }
+}
+
 /* ------------------------------------------------------------ indexer */
 
 /* Lightning-indexer scores for the listed query rows.
