@@ -168,7 +168,8 @@ def kv_fp8_quantize(kv_bf16_bits):
 
 def kv_fp8_dequantize(kv_fp8):
     """FP8 KV rows uint8 [rows, 656] -> the bf16 rows [rows, 576] (bits) the
-    attention reads: code * scale rounded once to bf16, the RoPE key as is."""
+    attention reads: the fp32 product code * scale rounded to bf16, the RoPE
+    key as is."""
     x, px = _c(np.asarray(kv_fp8).reshape(-1, 656), np.uint8)
     rows = x.shape[0]
     out = np.empty((rows, 576), np.uint16)

@@ -229,8 +229,9 @@ void oracle_kv_fp8_quantize(const uint16_t* kv, int64_t rows, uint8_t* out) {
 }
 
 /* The bf16 row the attention reads from an FP8 KV row: latent value =
- * code * scale, the exact product (4 + 24 significant bits, exact in fp64)
- * rounded once to bf16; the RoPE key as stored. */
+ * code * scale formed as an fp32 product (the scale's precision; round to
+ * nearest even), then rounded to the bf16 the attention multiplies; the RoPE
+ * key as stored. */
 void oracle_kv_fp8_dequantize(const uint8_t* in, int64_t rows, uint16_t* kv) {
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r) {
@@ -239,8 +240,10 @@ void oracle_kv_fp8_dequantize(const uint8_t* in, int64_t rows, uint16_t* kv) {
     for (int g = 0; g < 4; ++g) {
       float sc;
       memcpy(&sc, o + 512 + 4 * g, 4);
-      for (int j = 0; j < 128; ++j)
-        x[128 * g + j] = oracle_f64_to_bf16(oracle_e4m3_decode(o[128 * g + j]) * (double)sc);
+      for (int j = 0; j < 128; ++j) {
+        volatile float prod = (float)oracle_e4m3_decode(o[128 * g + j]) * sc;
+        x[128 * g + j] = oracle_f64_to_bf16((double)prod);
+      }
     }
     memcpy(x + 512, o + 528, 128);
   }

@@ -82,3 +82,30 @@ def test_error_bound_and_group_maximum():
     codes = q[:, :512].reshape(50, 4, 128)
     top = np.take_along_axis(codes, i[:, :, None], axis=2)[:, :, 0]
     assert ((top & 0x7F) == 0x7E).all()
+
+
+def _row(codes, scales):
+    """An FP8 KV row built by hand: codes at dims 0.., the four group scales,
+    a zero RoPE key."""
+    r = np.zeros((1, 656), np.uint8)
+    r[0, :len(codes)] = codes
+    r[0, 512:528] = np.asarray(scales, np.float32).view(np.uint8)
+    return r
+
+
+def test_dequantisation_rounds_the_fp32_product():
+    # code 0x3D = 1.625, scale 1 + 20165 * 2^-23 (exact in fp32): the exact
+    # product is 1.625 + (2^15 + 1/8) * 2^-23, just above the midpoint
+    # 1.625 + 2^-8 of the bf16 values 0x3FD0 / 0x3FD1.  The fp32 product
+    # rounds down onto that midpoint, which rounds to the even 0x3FD0 (a
+    # single rounding of the exact product would give 0x3FD1).
+    s = np.float32(1 + 20165 * 2.0 ** -23)
+    assert float(s) == 1 + 20165 * 2.0 ** -23
+    assert np.float32(1.625) * s == np.float32(1.625 + 2.0 ** -8)
+    d = oracle.kv_fp8_dequantize(_row([0x3D, 0xBD, 0x38], [s, 1, 1, 1]))[0]
+    assert d[0] == 0x3FD0 and d[1] == 0xBFD0
+    # 1.0 * s: fp32-exact, then s rounds to bf16 1.0 (0x3F80); zero codes stay zero
+    assert d[2] == 0x3F80 and (d[3:512] == 0).all()
+    # a product with no rounding at either step keeps every bit
+    d2 = oracle.kv_fp8_dequantize(_row([0x7E, 0x01], [2.0 ** -3, 1, 1, 1]))[0]
+    assert d2[0] == 0x4260 and d2[1] == 0x3980  # 448/8 = 56, 2^-9 / 8 = 2^-12
