@@ -79,7 +79,7 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------- algorithmic work
-def algorithmic(lay, cfg, fp8):
+def algorithmic(lay, cfg, fp8, kv_row_bytes=1152):
     """Per-launch algorithmic FLOPs / bytes of each kernel for this layout."""
     pos = lay.q_pos.astype(np.int64)
     vis = pos + 1
@@ -98,7 +98,7 @@ def algorithmic(lay, cfg, fp8):
     # distinct cache rows a launch must read: per sequence, at most its length
     rows_read = sum(min(int(nvalid[lay.q_start[b]:lay.q_start[b + 1]].sum()), int(seq_len[b]))
                     for b in range(lay.num_seqs))
-    mla_bytes = rows_read * 1152 + lay.num_q * H * (576 + 512) * 2
+    mla_bytes = rows_read * kv_row_bytes + lay.num_q * H * (576 + 512) * 2
     return {"indexer": {"flops": idx_flops, "bytes": float(idx_bytes)},
             "topk": {"flops": 0.0, "bytes": float(topk_bytes)},
             "sparse_mla": {"flops": mla_flops, "bytes": float(mla_bytes)}}
@@ -248,7 +248,7 @@ def make_appends(lay, layers, cfg, fp8, batch, dev, theta=8e6):
     return calls, nbytes, ws
 
 
-def setup(workload, dev, seed=0, paged=0):
+def setup(workload, dev, seed=0, paged=0, kv_fp8=False):
     import torch
 
     import dsa_indexer_indexshare_gb300 as dsa
@@ -266,6 +266,10 @@ def setup(workload, dev, seed=0, paged=0):
                 qc, qs = dsa.dsa_fp8_quantize(L["q_idx"])
                 kc, ks = dsa.dsa_fp8_quantize(L["k_idx"])
                 L.update(q_idx=qc, q_scale=qs, k_idx=kc, k_scale=ks)
+        torch.cuda.synchronize(dev)
+    if kv_fp8:  # FP8 KV latent rows (656 B) from the library's quantiser
+        for L in layers:
+            L["kv"] = dsa.dsa_kv_fp8_quantize(L["kv"])
         torch.cuda.synchronize(dev)
     phys = None
     if paged:
@@ -317,8 +321,13 @@ def oracle_sample(workload, lay, layers, cfg, fp8, nrows, seed=1, phys=None):
         if phys is not None:
             L = {k: (v.index_select(0, phys) if k in ("kv", "k_idx", "k_scale") else v)
                  for k, v in L.items()}
+        if L["kv"].dtype == torch.uint8:  # FP8 KV rows: the oracle reads their dequantised rows
+            import oracle
+            kv_host = oracle.kv_fp8_dequantize(L["kv"].cpu().numpy())
+        else:
+            kv_host = hb(L["kv"])
         d = {"q_lat": hb(L["q_lat"].index_select(0, rt)), "q_rope": hb(L["q_rope"].index_select(0, rt)),
-             "kv": hb(L["kv"])}
+             "kv": kv_host}
         if "q_idx" in L:
             if fp8:
                 d.update(q_idx=L["q_idx"].index_select(0, rt).cpu().numpy(),
@@ -355,6 +364,9 @@ def main():
     ap.add_argument("--with-append", action="store_true",
                     help="each step also rotates (and FP8-quantises) the new tokens' indexer "
                          "queries and appends their keys to the caches of every F layer")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="FP8 KV latent caches (656-byte rows: E4M3 latent in four scaled groups, "
+                         "bf16 RoPE key)")
     ap.add_argument("--paged", type=int, default=0, metavar="ROWS",
                     help="paged caches: blocks of ROWS positions (a multiple of 128) in a "
                          "permuted pool, addressed through a block table")
@@ -378,7 +390,8 @@ def main():
 
     import dsa_indexer_indexshare_gb300 as dsa
     peaks = load_peaks()
-    cfg, lay, layers, batch, fp8, phys = setup(args.workload, dev, paged=args.paged)
+    cfg, lay, layers, batch, fp8, phys = setup(args.workload, dev, paged=args.paged,
+                                               kv_fp8=args.kv_fp8)
     stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.fill_(1)
@@ -452,7 +465,7 @@ def main():
     value = replica_throughput(tokens_per_step, args.steps, world, total_ms)
 
     # ---- per-kernel roofline (live CUDA events around each launch)
-    work = algorithmic(lay, cfg, fp8)
+    work = algorithmic(lay, cfg, fp8, 656 if args.kv_fp8 else 1152)
     if appends:  # two launches (queries, keys) per F layer per step
         work["append"] = {"flops": 0.0, "bytes": append_bytes / (2 * len(appends))}
         dsa.status_fetch(append_ws)
@@ -505,6 +518,8 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "kv_layout": (f"paged: blocks of {args.paged} positions, permuted pool, "
                                      "block table" if args.paged else "contiguous"),
+                       "kv_dtype": ("FP8 E4M3 latent, 656-byte rows" if args.kv_fp8
+                                    else "bf16, 1152-byte rows"),
                        "step": ("indexer query RoPE/FP8 + key cache append per F layer, then the "
                                 "group" if args.with_append else "the group forward"),
                        "l2": "flushed between steps (256 MiB write, outside the timed events)"},

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libdsa.so")
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE = 0, 1, 2, 3
 DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX = 4, 5, 6
 DSA_BF16, DSA_FP8_E4M3 = 0, 1
-INDEX_HEADS, INDEX_DIM, LATENT, ROPE, KV_ROW = 32, 128, 512, 64, 576
+INDEX_HEADS, INDEX_DIM, LATENT, ROPE, KV_ROW, KV_ROW_FP8 = 32, 128, 512, 64, 576, 656
 STATUS_BYTES = 256
 LAUNCH_KINDS = ("indexer", "topk", "sparse_mla", "combine", "fp8_quantize", "append", "other")
 
@@ -50,7 +50,7 @@ class _Group(ctypes.Structure):
                 ("scale", c_float), ("idx_dtype", c_int), ("kv_rows", c_int64),
                 ("k_rows", c_int64), ("q_lat", _PP), ("q_rope", _PP), ("kv", _PP), ("out", _PP),
                 ("lse", _PP), ("q_idx", _PP), ("q_scale", _PP), ("w", _PP), ("k_idx", _PP),
-                ("k_scale", _PP)]
+                ("k_scale", _PP), ("kv_dtype", c_int)]
 
 
 def _load():
@@ -83,6 +83,10 @@ def _load():
         "indexshare_group_forward": (st, [POINTER(_Group), B, c_void_p, c_void_p, c_size_t,
                                           c_void_p]),
         "dsa_fp8_quantize": (st, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p]),
+        "dsa_kv_fp8_quantize": (st, [c_void_p, c_int64, c_void_p, c_void_p]),
+        "dsa_sparse_mla_attn_fp8kv": (st, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p,
+                                           c_int32, c_int32, c_float, B, c_void_p, c_void_p,
+                                           c_void_p, c_size_t, c_void_p]),
         "dsa_indexer_append_keys": (st, [c_void_p, c_void_p, c_void_p, c_int32, B, c_int,
                                          c_void_p, c_void_p, c_void_p, c_int64, c_void_p,
                                          c_size_t, c_void_p]),
@@ -265,14 +269,16 @@ def dsa_topk(scores, batch: Batch, k: int, idx=None, *, ws=None, stream=None):
 
 def dsa_sparse_mla_attn(q_lat, q_rope, kv, idx, batch: Batch, *, scale: float, out=None,
                         lse=None, with_lse=True, ws=None, stream=None):
-    """Sparse absorbed-MLA attention: (out [num_q, H, 512] bf16, lse [num_q, H] fp32)."""
+    """Sparse absorbed-MLA attention: (out [num_q, H, 512] bf16, lse [num_q, H] fp32).
+    kv: bf16 [rows, 576], or FP8 rows uint8 [rows, 656] (dsa_kv_fp8_quantize)."""
     dev = batch.device
     H = q_lat.shape[1]
     _need(q_lat, "q_lat", torch.bfloat16, dev, (batch.num_q, H, LATENT))
     _need(q_rope, "q_rope", torch.bfloat16, dev, (batch.num_q, H, ROPE))
-    _need(kv, "kv", torch.bfloat16, dev)
-    if kv.dim() != 2 or kv.shape[1] != KV_ROW:
-        raise ValueError("kv must be [rows, 576]")
+    _need(kv, "kv", (torch.bfloat16, torch.uint8), dev)
+    kv_fp8 = kv.dtype == torch.uint8
+    if kv.dim() != 2 or kv.shape[1] != (KV_ROW_FP8 if kv_fp8 else KV_ROW):
+        raise ValueError("kv must be bf16 [rows, 576] or uint8 [rows, 656]")
     _need(idx, "idx", torch.int32, dev)
     k = idx.shape[1]
     if out is None:
@@ -282,10 +288,25 @@ def dsa_sparse_mla_attn(q_lat, q_rope, kv, idx, batch: Batch, *, scale: float, o
         lse = torch.empty((batch.num_q, H), dtype=torch.float32, device=dev)
     if ws is None:
         ws = workspace(lib.dsa_sparse_mla_workspace_size(batch.c, H, k), dev)
-    _check(lib.dsa_sparse_mla_attn(_ptr(q_lat), _ptr(q_rope), _ptr(kv), kv.shape[0], _ptr(idx), k,
-                                   H, float(scale), batch.c, _ptr(out), _ptr(lse), _ptr(ws),
-                                   ws.numel(), _stream(stream, dev)), "dsa_sparse_mla_attn")
+    fn = lib.dsa_sparse_mla_attn_fp8kv if kv_fp8 else lib.dsa_sparse_mla_attn
+    _check(fn(_ptr(q_lat), _ptr(q_rope), _ptr(kv), kv.shape[0], _ptr(idx), k, H, float(scale),
+              batch.c, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream, dev)),
+           "dsa_sparse_mla_attn")
     return out, lse
+
+
+def dsa_kv_fp8_quantize(kv, out=None, *, stream=None):
+    """bf16 KV rows [rows, 576] -> FP8 KV rows uint8 [rows, 656] (four E4M3
+    groups of 128 latent dims with fp32 scales, then the bf16 RoPE key)."""
+    _need(kv, "kv", torch.bfloat16)
+    if kv.dim() != 2 or kv.shape[1] != KV_ROW:
+        raise ValueError("kv must be [rows, 576]")
+    if out is None:
+        out = torch.empty((kv.shape[0], KV_ROW_FP8), dtype=torch.uint8, device=kv.device)
+    _need(out, "out", torch.uint8, kv.device, (kv.shape[0], KV_ROW_FP8))
+    _check(lib.dsa_kv_fp8_quantize(_ptr(kv), kv.shape[0], _ptr(out), _stream(stream, kv.device)),
+           "dsa_kv_fp8_quantize")
+    return out
 
 
 class Group:
@@ -309,7 +330,9 @@ class Group:
         for l, L in enumerate(layers):
             _need(L["q_lat"], f"q_lat[{l}]", torch.bfloat16, dev, (num_q, H, LATENT))
             _need(L["q_rope"], f"q_rope[{l}]", torch.bfloat16, dev, (num_q, H, ROPE))
-            _need(L["kv"], f"kv[{l}]", torch.bfloat16, dev, (first["kv"].shape[0], KV_ROW))
+            kv_fp8 = first["kv"].dtype == torch.uint8
+            _need(L["kv"], f"kv[{l}]", torch.uint8 if kv_fp8 else torch.bfloat16, dev,
+                  (first["kv"].shape[0], KV_ROW_FP8 if kv_fp8 else KV_ROW))
             if layer_types[l] == "F":
                 _need(L["q_idx"], f"q_idx[{l}]", idx_t.dtype, dev, (num_q, INDEX_HEADS, INDEX_DIM))
                 _need(L["w"], f"w[{l}]", torch.float32, dev, (num_q, INDEX_HEADS))
@@ -340,7 +363,8 @@ class Group:
         self._c = _Group(self._types, H, k, float(scale), self.idx_dtype, kv_rows, k_rows,
                          cast(a["q_lat"]), cast(a["q_rope"]), cast(a["kv"]), cast(a["out"]),
                          cast(a["lse"]), cast(a["q_idx"]), cast(a["q_scale"]), cast(a["w"]),
-                         cast(a["k_idx"]), cast(a["k_scale"]))
+                         cast(a["k_idx"]), cast(a["k_scale"]),
+                         DSA_FP8_E4M3 if first["kv"].dtype == torch.uint8 else DSA_BF16)
         self.k = k
         self.device = dev
         self.num_q = num_q

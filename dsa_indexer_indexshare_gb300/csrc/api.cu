@@ -321,6 +321,22 @@ dsa_status_t dsa_sparse_mla_attn(const void* q_lat, const void* q_rope, const vo
                        "sparse MLA launch");
 }
 
+dsa_status_t dsa_sparse_mla_attn_fp8kv(const void* q_lat, const void* q_rope, const void* kv8,
+                                       int64_t kv_rows, const int32_t* idx, int32_t k,
+                                       int32_t heads, float scale, const dsa_batch_t* b, void* out,
+                                       float* lse, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (dsa_status_t s = check_mla_args(q_lat, q_rope, kv8, kv_rows, idx, k, heads, scale, b, out)) return s;
+  if (heads != 64) return fail(DSA_ERR_UNSUPPORTED, "FP8 KV rows: heads must be 64");
+  const size_t need = dsa_sparse_mla_workspace_size(b, heads, k);
+  if (dsa_status_t s = check_ws(ws, ws_bytes, need)) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  return launch_status(launch_sparse_mla(q_lat, q_rope, kv8, kv_rows, idx, k, heads, scale, *b,
+                                         out, lse, wsb + kStatusBytes, need - kStatusBytes,
+                                         static_cast<int*>(ws), stream, true),
+                       "sparse MLA (FP8 KV) launch");
+}
+
 // ------------------------------------------------------------- a6: group
 size_t dsa_group_workspace_size(const dsa_group_t* g, const dsa_batch_t* b) {
   if (!g || !b) return kStatusBytes;
@@ -367,6 +383,9 @@ dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b
   uint8_t* topk_scratch = wsb + kStatusBytes + score_bytes;
   const size_t topk_bytes = round256(topk_scratch_bytes(*b, g->k));
   const bool fp8 = g->idx_dtype == DSA_FP8_E4M3;
+  const bool kv_fp8 = g->kv_dtype == DSA_FP8_E4M3;
+  if (g->kv_dtype != DSA_BF16 && !kv_fp8) return fail(DSA_ERR_UNSUPPORTED, "kv_dtype");
+  if (kv_fp8 && g->heads != 64) return fail(DSA_ERR_UNSUPPORTED, "FP8 KV rows: heads must be 64");
   for (int l = 0; l < nl; ++l) {
     if (g->layer_types[l] == 'F') {
       // F layer: candidate scoring, then top-K into the shared index buffer
@@ -385,7 +404,7 @@ dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b
     if (dsa_status_t s = launch_status(
             launch_sparse_mla(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, idx_buf, g->k,
                               g->heads, g->scale, *b, g->out[l], g->lse ? g->lse[l] : nullptr,
-                              wsb + kStatusBytes, need - kStatusBytes, status, stream),
+                              wsb + kStatusBytes, need - kStatusBytes, status, stream, kv_fp8),
             "sparse MLA launch"))
       return s;
   }
@@ -402,6 +421,16 @@ dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float
     return fail(DSA_ERR_INVALID_ARG, "x and codes must be 16-byte aligned");
   if (rows > (int64_t(1) << 34)) return fail(DSA_ERR_UNSUPPORTED, "rows too large");
   return launch_status(launch_quantize(x, rows, codes, scale, stream), "quantiser launch");
+}
+
+// ------------------------------------------------------------- NEXT-2: FP8 KV rows
+dsa_status_t dsa_kv_fp8_quantize(const void* kv, int64_t rows, uint8_t* out, dsa_stream_t stream) {
+  if (rows < 0) return fail(DSA_ERR_INVALID_ARG, "rows < 0");
+  if (rows > 0 && (!kv || !out)) return fail(DSA_ERR_INVALID_ARG, "kv and out are required");
+  if (rows > 0 && (!aligned16(kv) || !aligned16(out)))
+    return fail(DSA_ERR_INVALID_ARG, "kv and out must be 16-byte aligned");
+  if (rows > (int64_t(1) << 33)) return fail(DSA_ERR_UNSUPPORTED, "rows too large");
+  return launch_status(launch_kv_fp8_quantize(kv, rows, out, stream), "KV quantiser launch");
 }
 
 // ------------------------------------------------------------- NEXT-3: cache append

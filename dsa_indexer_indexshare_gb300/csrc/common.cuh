@@ -89,7 +89,8 @@ size_t mla_workspace_bytes(const dsa_batch_t& b, int heads, int k);
 cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void* kv,
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
                               const dsa_batch_t& b, void* out, float* lse, void* ws_extra,
-                              size_t ws_extra_bytes, int* status, cudaStream_t stream);
+                              size_t ws_extra_bytes, int* status, cudaStream_t stream,
+                              bool kv_fp8 = false);
 // RoPE (+ Hadamard + FP8) of n indexer vectors; vector v at position
 // pos_of[v / group], written to the cache row of (seq_of[v / group], pos)
 // (seq_of set) or to row v.  inv_freq: 32 host doubles.
@@ -97,6 +98,8 @@ cudaError_t launch_rope_append(const void* x, int64_t n, int group, const int32_
                                const int32_t* seq_of, const dsa_batch_t& b, const double* inv_freq,
                                bool fp8, void* out, float* out_scale, int64_t out_rows, int* status,
                                cudaStream_t stream);
+cudaError_t launch_kv_fp8_quantize(const void* kv, int64_t rows, uint8_t* out,
+                                   cudaStream_t stream);
 cudaError_t launch_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
                             cudaStream_t stream);
 cudaError_t launch_selftest_wait(int* status, cudaStream_t stream);

@@ -164,6 +164,52 @@ __global__ void __launch_bounds__(256) rope_append_kernel(
   }
 }
 
+// FP8 KV latent rows ("GLM-5.2 / 总览" config table: FP8 KV ~656 B per token
+// and layer, per-group): warp r quantises bf16 row r [576] into 656 bytes,
+// the 512 latent dims as E4M3 codes in four groups of 128 (lane l: dims
+// 16l .. 16l+15, group l / 8), each group scaled by amax/448 (fp32; 1 for
+// an all-zero group), then the four fp32 scales, then the 64 bf16 RoPE dims.
+__global__ void __launch_bounds__(256) kv_fp8_quant_kernel(const uint16_t* __restrict__ kv,
+                                                           int64_t rows,
+                                                           uint8_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const uint16_t* x = kv + r * 576;
+  uint8_t* o = out + r * 656;
+  const uint4 a = *reinterpret_cast<const uint4*>(x + lane * 16);
+  const uint4 b2 = *reinterpret_cast<const uint4*>(x + lane * 16 + 8);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+  float v[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[2 * k] = bf16_bits_to_float(static_cast<uint16_t>(w[k] & 0xFFFF));
+    v[2 * k + 1] = bf16_bits_to_float(static_cast<uint16_t>(w[k] >> 16));
+    amax = fmaxf(amax, fmaxf(fabsf(v[2 * k]), fabsf(v[2 * k + 1])));
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  uint32_t packed[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t pk = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_fp8_storage_t c =
+          __nv_cvt_float_to_fp8(__fdiv_rn(v[4 * k + j], sc), __NV_SATFINITE, __NV_E4M3);
+      pk |= static_cast<uint32_t>(c) << (8 * j);
+    }
+    packed[k] = pk;
+  }
+  *reinterpret_cast<uint4*>(o + lane * 16) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  if ((lane & 7) == 0) *reinterpret_cast<float*>(o + 512 + 4 * (lane >> 3)) = sc;
+  if (lane < 8)
+    *reinterpret_cast<uint4*>(o + 528 + lane * 16) =
+        *reinterpret_cast<const uint4*>(x + 512 + lane * 8);
+}
+
 // One CTA waits on an mbarrier that nothing arrives on; the bounded wait
 // gives up, records the timeout and the kernel returns normally.
 __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
@@ -218,6 +264,18 @@ cudaError_t launch_rope_append(const void* x, int64_t n, int group, const int32_
         static_cast<uint16_t*>(out), nullptr, nullptr, out_rows, status);
   prof_end(kLaunchAppend, stream);
   count_launch(kLaunchAppend);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_fp8_quantize(const void* kv, int64_t rows, uint8_t* out,
+                                   cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks = (rows + 7) / 8;
+  prof_begin(stream);
+  kv_fp8_quant_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(kv), rows, out);
+  prof_end(kLaunchQuant, stream);
+  count_launch(kLaunchQuant);
   return cudaGetLastError();
 }
 

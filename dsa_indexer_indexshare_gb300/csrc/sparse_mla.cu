@@ -36,6 +36,8 @@
 // queued MMAs have drained, so one issuer waiting for gathered data would
 // empty the tensor pipe every time.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 
@@ -65,9 +67,12 @@ struct MlaCfg {
   static constexpr int NBAR = 1 + 4 + 4 + 4;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // the sequence's block-table row (paged caches), when it has <= TAB_MAX entries
-  static constexpr int TAB_MAX = 1024;
-  static constexpr int OFF_TAB = OFF_MISC + 64;
-  static constexpr int SMEM = OFF_TAB + TAB_MAX * 4 + 1024;
+  static constexpr int TAB_MAX = 512;
+  static constexpr int OFF_TAB = (OFF_MISC + 64 + 15) & ~15;
+  // FP8 KV rows: the block's 128 x 4 fp32 group scales (16-byte cp.async targets)
+  static constexpr int OFF_KSC = OFF_TAB + TAB_MAX * 4;
+  static constexpr int SMEM = OFF_KSC + 128 * 16 + 1024;
+  static_assert(OFF_KSC % 16 == 0, "cp.async destinations need 16-byte alignment");
   static constexpr int HW = H > 32 ? 32 : H;       // heads per softmax warp
   static constexpr int NSW = 4 * (H / HW);           // softmax warps (two per lane quarter at H=64)
   static constexpr int NT = NSW * 32 + 64;           // + the QK and the P.V issuer warps
@@ -83,6 +88,7 @@ struct MlaCfg {
 struct MlaParams {
   BatchArgs b;
   const uint16_t* kv;  // [kv_rows, 576] bf16
+  const uint8_t* kv8;  // or FP8 rows [kv_rows, 656]: 512 E4M3, 4 fp32 group scales, 64 bf16
   int64_t kv_rows;
   const int32_t* idx;
   int K;
@@ -139,7 +145,19 @@ __device__ __forceinline__ void tmem_cols_store(uint32_t taddr, const float (&v)
     tmem_st32(taddr, v);
 }
 
-template <int H, int NSPLIT, bool PAGED>
+// bf16 bits of four E4M3 codes (one 32-bit word, lowest byte first) times
+// their group scale: the codes widen exactly to fp16 then fp32, the fp32
+// products round to nearest even (two lanes per packed multiply), and each
+// narrows to bf16 with round to nearest even.
+__device__ __forceinline__ uint2 scaled_e4m3x4_to_bf16x4(uint32_t w, float2 sc2) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
+  const __nv_bfloat162 a = __float22bfloat162_rn(__fmul2_rn(__half22float2(__half2(lo)), sc2));
+  const __nv_bfloat162 b = __float22bfloat162_rn(__fmul2_rn(__half22float2(__half2(hi)), sc2));
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+
+template <int H, int NSPLIT, bool PAGED, bool KV8>
 __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap qlat_map,
                       const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
@@ -355,6 +373,68 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
                      "l"(kvk + static_cast<int64_t>(grow[c]) * 576 + 64 * i)
                      : "memory");
     };
+    // ---- FP8 KV rows: a group's codes (128 keys x 128 dims, 16 KB) are staged
+    // unswizzled in its second sub-tile, its rows' scales in a 2 KB area,
+    // then the threads that copied them expand them in place to the swizzled
+    // bf16 operand layout (the 8 threads of a row share a warp, so warp
+    // barriers order the reads of the codes before the writes over them).
+    const uint32_t sKsc = smem_u32(sm + C::OFF_KSC);
+    auto issue8 = [&](int g) {
+      const uint32_t dst = sC + (2 * g + 1) * C::CSUB + rb * 128 + kch * 16;
+#pragma unroll
+      for (int c = 0; c < RPT; ++c)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + c * GROW * 128),
+                     "l"(p.kv8 + static_cast<int64_t>(grow[c]) * 656 + 128 * g + kch * 16)
+                     : "memory");
+      if (g == 0 && kch == 0) {
+#pragma unroll
+        for (int c = 0; c < RPT; ++c)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sKsc + (rb + GROW * c) * 16),
+                       "l"(p.kv8 + static_cast<int64_t>(grow[c]) * 656 + 512)
+                       : "memory");
+      }
+      if (g == 3) {  // the RoPE key, bf16 as stored, into its swizzled sub-tile
+        const uint32_t rdst = gdst0 + 8 * C::CSUB;
+#pragma unroll
+        for (int c = 0; c < RPT; ++c)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(rdst + c * GROW * 128),
+                       "l"(p.kv8 + static_cast<int64_t>(grow[c]) * 656 + 528 + kch * 16)
+                       : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    auto convert8 = [&](int g, int pending) {  // pending: younger copy groups still allowed
+      if (pending == 0)
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+      else if (pending == 1)
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+      else if (pending == 2)
+        asm volatile("cp.async.wait_group 2;" ::: "memory");
+      else
+        asm volatile("cp.async.wait_group 3;" ::: "memory");
+#pragma unroll
+      for (int c = 0; c < RPT; ++c) {
+        const int r = rb + GROW * c;
+        // every code of row r is read (by its 8 threads, one warp) before any
+        // of them writes over it; rows of other c are disjoint
+        __syncwarp();
+        const uint4 cv = *reinterpret_cast<const uint4*>(sm + C::OFF_C + (2 * g + 1) * C::CSUB +
+                                                         r * 128 + kch * 16);
+        const float sc = *reinterpret_cast<const float*>(sm + C::OFF_KSC + r * 16 + 4 * g);
+        __syncwarp();
+        const float2 s2 = make_float2(sc, sc);
+        const uint2 o01 = scaled_e4m3x4_to_bf16x4(cv.x, s2), o23 = scaled_e4m3x4_to_bf16x4(cv.y, s2);
+        const uint2 o45 = scaled_e4m3x4_to_bf16x4(cv.z, s2), o67 = scaled_e4m3x4_to_bf16x4(cv.w, s2);
+        // dims 128g + 16kch .. +15: sub-tile 2g + kch/4, 16-byte chunks 2(kch%4), 2(kch%4)+1
+        uint8_t* tile = sm + C::OFF_C + (2 * g + (kch >> 2)) * C::CSUB + r * 128;
+        const int ch = 2 * (kch & 3);
+        *reinterpret_cast<uint4*>(tile + ((ch ^ (r & 7)) << 4)) = make_uint4(o01.x, o01.y, o23.x, o23.y);
+        *reinterpret_cast<uint4*>(tile + (((ch + 1) ^ (r & 7)) << 4)) =
+            make_uint4(o45.x, o45.y, o67.x, o67.y);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_CFULL + g));
+    };
     // CFULL(g) completes once every copy this thread issued so far has landed
     auto signal = [&](int g) {
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(B_CFULL + g))
@@ -363,12 +443,19 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     if (j0 < j1) {
       fetch_sel(j0);
       resolve_rows();
+      if constexpr (KV8) {
 #pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        issue(2 * g);
-        issue(2 * g + 1);
-        if (g == 3) issue(8);
-        signal(g);
+        for (int g = 0; g < 4; ++g) issue8(g);
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) convert8(g, 3 - g);
+      } else {
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          issue(2 * g);
+          issue(2 * g + 1);
+          if (g == 3) issue(8);
+          signal(g);
+        }
       }
     }
 
@@ -489,16 +576,23 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         bool alive = true;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          if (!mbar_wait(bar(B_CFREE + c), u & 1, abort_flag, p.status, to)) {
+          const bool freed = mbar_wait(bar(B_CFREE + c), u & 1, abort_flag, p.status, to);
+          if (!(KV8 ? __all_sync(0xffffffffu, freed) : freed)) {
             alive = false;
             break;
           }
-          issue(2 * c);
-          issue(2 * c + 1);
-          if (c == 3) issue(8);
-          signal(c);
+          if constexpr (KV8) {
+            issue8(c);
+            if (c > 0) convert8(c - 1, 1);
+          } else {
+            issue(2 * c);
+            issue(2 * c + 1);
+            if (c == 3) issue(8);
+            signal(c);
+          }
         }
         if (!alive) break;
+        if constexpr (KV8) convert8(3, 0);
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -604,11 +698,11 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   }
 }
 
-template <int H, int NSPLIT, bool PAGED>
+template <int H, int NSPLIT, bool PAGED, bool KV8>
 cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p,
                        cudaStream_t stream) {
   using C = MlaCfg<H>;
-  auto* kern = sparse_mla_kernel<H, NSPLIT, PAGED>;
+  auto* kern = sparse_mla_kernel<H, NSPLIT, PAGED, KV8>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -636,19 +730,18 @@ cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaPa
   return e;
 }
 
-template <int H>
+template <int H, bool KV8>
 cudaError_t launch_h(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p, int nsplit,
-                     bool paged,
-                     cudaStream_t stream) {
+                     bool paged, cudaStream_t stream) {
   switch (nsplit) {
-    case 1: return paged ? launch_mla<H, 1, true>(ql, qr, p, stream)
-                         : launch_mla<H, 1, false>(ql, qr, p, stream);
-    case 2: return paged ? launch_mla<H, 2, true>(ql, qr, p, stream)
-                         : launch_mla<H, 2, false>(ql, qr, p, stream);
-    case 4: return paged ? launch_mla<H, 4, true>(ql, qr, p, stream)
-                         : launch_mla<H, 4, false>(ql, qr, p, stream);
-    default: return paged ? launch_mla<H, 8, true>(ql, qr, p, stream)
-                          : launch_mla<H, 8, false>(ql, qr, p, stream);
+    case 1: return paged ? launch_mla<H, 1, true, KV8>(ql, qr, p, stream)
+                         : launch_mla<H, 1, false, KV8>(ql, qr, p, stream);
+    case 2: return paged ? launch_mla<H, 2, true, KV8>(ql, qr, p, stream)
+                         : launch_mla<H, 2, false, KV8>(ql, qr, p, stream);
+    case 4: return paged ? launch_mla<H, 4, true, KV8>(ql, qr, p, stream)
+                         : launch_mla<H, 4, false, KV8>(ql, qr, p, stream);
+    default: return paged ? launch_mla<H, 8, true, KV8>(ql, qr, p, stream)
+                          : launch_mla<H, 8, false, KV8>(ql, qr, p, stream);
   }
 }
 
@@ -659,7 +752,7 @@ size_t mla_workspace_bytes(const dsa_batch_t&, int, int) { return 0; }
 cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void* kv,
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
                               const dsa_batch_t& b, void* out, float* lse, void*, size_t,
-                              int* status, cudaStream_t stream) {
+                              int* status, cudaStream_t stream, bool kv_fp8) {
   if (b.num_q == 0) return cudaSuccess;
   CUtensorMap ql, qr;
   const uint64_t qrows = static_cast<uint64_t>(b.num_q) * heads;
@@ -668,7 +761,8 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
     return cudaErrorInvalidValue;
   MlaParams p{};
   p.b = to_args(b);
-  p.kv = static_cast<const uint16_t*>(kv);
+  p.kv = kv_fp8 ? nullptr : static_cast<const uint16_t*>(kv);
+  p.kv8 = kv_fp8 ? static_cast<const uint8_t*>(kv) : nullptr;
   p.kv_rows = kv_rows;
   p.idx = idx;
   p.K = k;
@@ -684,8 +778,12 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   while (nsplit < 8 && nsplit * 2 <= nblk && static_cast<int64_t>(b.num_q) * nsplit * 2 <= 152)
     nsplit *= 2;
   const bool paged = b.block_table != nullptr;
-  return heads == 16 ? launch_h<16>(ql, qr, p, nsplit, paged, stream)
-                     : launch_h<64>(ql, qr, p, nsplit, paged, stream);
+  if (kv_fp8) {  // FP8 KV rows: the model's 64 heads only
+    if (heads != 64) return cudaErrorNotSupported;
+    return launch_h<64, true>(ql, qr, p, nsplit, paged, stream);
+  }
+  return heads == 16 ? launch_h<16, false>(ql, qr, p, nsplit, paged, stream)
+                     : launch_h<64, false>(ql, qr, p, nsplit, paged, stream);
 }
 
 }  // namespace dsa

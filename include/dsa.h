@@ -257,6 +257,8 @@ typedef struct {
   const float* const* w;
   const void* const* k_idx;
   const float* const* k_scale;
+  dsa_dtype_t kv_dtype; /* DSA_BF16: kv[l] bf16 [kv_rows, 576]; DSA_FP8_E4M3: FP8 rows
+                           uint8 [kv_rows, 656] (see dsa_kv_fp8_quantize; heads 64) */
 } dsa_group_t;
 
 DSA_API size_t dsa_group_workspace_size(const dsa_group_t* g, const dsa_batch_t* b);
@@ -279,6 +281,31 @@ DSA_API dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_ba
  */
 DSA_API dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
                               dsa_stream_t stream);
+
+/* ------------------------------------------------------------------ NEXT-2: FP8 KV latent */
+
+/*
+ * FP8 KV cache rows ("GLM-5.2 / 总览" config table: per-token per-layer KV
+ * cache BF16 = 1152 bytes, FP8 ~656 bytes per-group): 656 bytes per position,
+ *   [0, 512)    the 512-d latent as E4M3 codes, in four groups of 128 dims
+ *   [512, 528)  the four groups' fp32 scales, amax/448 (1 for an all-zero group)
+ *   [528, 656)  the 64-d RoPE key, bf16 as given
+ * Codes are E4M3(x / scale), computed in fp32, round to nearest even,
+ * saturating.  dsa_kv_fp8_quantize writes such rows from bf16 rows
+ * kv [rows, 576] (out uint8 [rows, 656]; both 16-byte aligned).
+ *
+ * dsa_sparse_mla_attn_fp8kv: dsa_sparse_mla_attn over an FP8 cache
+ * (kv8 uint8 [kv_rows, 656], heads = 64); each gathered latent value is
+ * code * scale rounded once to bf16, then the attention is the bf16 one.
+ * The group call takes such caches with dsa_group_t.kv_dtype = DSA_FP8_E4M3.
+ */
+DSA_API dsa_status_t dsa_kv_fp8_quantize(const void* kv, int64_t rows, uint8_t* out,
+                                 dsa_stream_t stream);
+DSA_API dsa_status_t dsa_sparse_mla_attn_fp8kv(const void* q_lat, const void* q_rope,
+                                       const void* kv8, int64_t kv_rows, const int32_t* idx,
+                                       int32_t k, int32_t heads, float scale,
+                                       const dsa_batch_t* b, void* out, float* lse, void* ws,
+                                       size_t ws_bytes, dsa_stream_t stream);
 
 /* ------------------------------------------------------------------ NEXT-3: cache append */
 
