@@ -40,7 +40,7 @@ DESCR = {
     "chunked": "chunked prefill: 4096 queries after a 131072-token prefix, layers FSSSFSSS, H=64, "
                "K=2048, bf16",
     "decode1m": "1M decode: 4 sequences x 1 query, context 1048576, layers FSSS, H=64, K=2048, "
-                "FP8 E4M3 + Hadamard indexer keys/queries, bf16 KV latent",
+                "FP8 E4M3 + Hadamard indexer keys/queries",
     "prefill2k": "profiling case: prefill of 2560 tokens, layers FSSS, H=64, K=2048, bf16",
     "chunked1k": "profiling case: chunked prefill of 1024 queries after a 131072-token prefix, "
                  "layers FSSS, H=64, K=2048, bf16",
@@ -511,7 +511,7 @@ def main():
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" + ("+fp8-indexer" if fp8 else ""),
+            "dtype": "bf16" + ("+fp8-indexer" if fp8 else "") + ("+fp8-kv" if args.kv_fp8 else ""),
             "data": "synthetic (seeded N(0,1)/sqrt(d) bf16, device-resident)",
             "config": {"workload": DESCR[args.workload], "global_batch": world * tokens_per_step,
                        "seq_len": int(lay.max_len), "layers": cfg["layers"],
