@@ -296,7 +296,8 @@ DSA_API dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* code
  *
  * dsa_sparse_mla_attn_fp8kv: dsa_sparse_mla_attn over an FP8 cache
  * (kv8 uint8 [kv_rows, 656], heads = 64); each gathered latent value is
- * code * scale rounded once to bf16, then the attention is the bf16 one.
+ * the fp32 product code * scale (round to nearest even) narrowed to bf16
+ * (round to nearest even), then the attention is the bf16 one.
  * The group call takes such caches with dsa_group_t.kv_dtype = DSA_FP8_E4M3.
  */
 DSA_API dsa_status_t dsa_kv_fp8_quantize(const void* kv, int64_t rows, uint8_t* out,

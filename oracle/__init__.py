@@ -217,6 +217,93 @@ def logical_cache(paged, block_table, block_rows, seq_lens):
     return out
 
 
+# ---------------------------------------------------------------- hot / cold KV
+def hot_state(num_seqs, hot_slots, max_len):
+    """An empty hot buffer: slot_pos [S, hot] (position held, -1 empty),
+    slot_stamp [S, hot] (last step that used the slot, -1 never) and
+    pos_slot [S, max_len] (slot holding each position, -1 none)."""
+    return {"slot_pos": np.full((num_seqs, hot_slots), -1, np.int32),
+            "slot_stamp": np.full((num_seqs, hot_slots), -1, np.int32),
+            "pos_slot": np.full((num_seqs, max_len), -1, np.int32)}
+
+
+def hot_plan(idx, q_start, q_pos, state, step, hot_slots):
+    """One step of the HiSparse-style hot buffer ("GLM-5.2 / 总览" glossary
+    entry HiSparse: a GPU "hot" KV of 6144 slots, the full KV in CPU pinned
+    memory, rows swapped in on demand after the DSA top-K).
+
+    Per sequence b, over the valid entries e = idx[t, k] (0 <= e <= q_pos[t])
+    of its queries, taken query by query and slot by slot:
+      1. a resident position (pos_slot[e] >= 0) is a hit: its slot's stamp
+         becomes `step`;
+      2. the other positions are misses, kept in order of first appearance;
+      3. the m misses need m slots: among the slots whose stamp is below
+         `step` (not used at this step), the m least recently used ones
+         (smallest stamp, then lowest slot index); more misses than such
+         slots is an overflow: the sequence changes no slot and all its rows
+         are -1;
+      4. the chosen slots, taken in increasing slot index, receive the misses
+         in order: the slot's old position (if any) leaves, the miss enters,
+         the stamp becomes `step`; (position, slot) goes on the fetch list;
+      5. rows[t, k] = b * hot_slots + pos_slot[e] (-1 for -1 padding and for
+         invalid entries).
+    `step` must exceed every step used before with this state.  Returns
+    (new state, rows [Nq, K] int32, fetch list per sequence, set of errors
+    among {"index", "overflow"})."""
+    st = {key: np.array(v, copy=True) for key, v in state.items()}
+    idx = np.asarray(idx)
+    q_start = np.asarray(q_start)
+    q_pos = np.asarray(q_pos)
+    nq, K = idx.shape
+    max_len = st["pos_slot"].shape[1]
+    rows = np.full((nq, K), -1, np.int32)
+    fetch, errors = [], set()
+    for b in range(len(q_start) - 1):
+        sp, ss, ps = st["slot_pos"][b], st["slot_stamp"][b], st["pos_slot"][b]
+        entries = []
+        for t in range(int(q_start[b]), int(q_start[b + 1])):
+            for k in range(K):
+                e = int(idx[t, k])
+                if e == -1:
+                    continue
+                if e < 0 or e > int(q_pos[t]) or e >= max_len:
+                    errors.add("index")
+                    continue
+                entries.append((t, k, e))
+        misses, seen = [], set()
+        for _, _, e in entries:
+            if ps[e] >= 0:
+                ss[ps[e]] = step
+            elif e not in seen:
+                seen.add(e)
+                misses.append(e)
+        free = [s for s in range(hot_slots) if ss[s] < step]
+        if len(misses) > len(free):
+            errors.add("overflow")
+            fetch.append([])
+            continue
+        lru = sorted(free, key=lambda s: (int(ss[s]), s))[:len(misses)]
+        moves = []
+        for e, s in zip(misses, sorted(lru)):
+            if sp[s] >= 0:
+                ps[sp[s]] = -1
+            ps[e], sp[s], ss[s] = s, e, step
+            moves.append((e, s))
+        fetch.append(moves)
+        for t, k, e in entries:
+            rows[t, k] = b * hot_slots + ps[e]
+    return st, rows, fetch, errors
+
+
+def hot_fetch(fetch, cold_kv, cold_row, hot_kv, hot_slots):
+    """Swap-in: for every (position e, slot s) of sequence b's fetch list,
+    hot_kv[b * hot_slots + s] = cold_kv[cold_row(b, e)] (in place)."""
+    for b, moves in enumerate(fetch):
+        for e, s in moves:
+            hot_kv[b * hot_slots + s] = cold_kv[cold_row(b, e)]
+    return hot_kv
+
+
 # ---------------------------------------------------------------- the method
 def indexer_scores(q_idx, w, k_idx, rows, row_pos, row_key0, max_len, *, dtype=0,
                    q_scale=None, k_scale=None, Hi=None, Di=None):
