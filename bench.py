@@ -281,7 +281,7 @@ def setup(workload, dev, seed=0, paged=0, kv_fp8=False):
     return cfg, lay, layers, batch, fp8, phys
 
 
-def time_steps(run, steps, warmup, flush, stream):
+def time_steps(run, steps, warmup, flush, stream, after=None):
     import torch
     for _ in range(warmup):
         run()
@@ -295,9 +295,123 @@ def time_steps(run, steps, warmup, flush, stream):
         run()
         b.record(stream)
         evs.append((a, b))
+        if after is not None:
+            after()  # bookkeeping outside the timed events
         flush()  # outside the timed events: L2 is cold at every step
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in evs]
+
+
+# ---------------------------------------------------------------- hot / cold KV
+class HotMode:
+    """--hot SLOTS: every layer's cache moves to pinned host memory (the cold
+    store, read by the GPU over NVLink-C2C); each layer keeps SLOTS hot rows
+    per sequence in HBM; one HotState per F layer.  Each step runs
+    indexshare_group_forward_hot with the next step number; with
+    --hot-rotate R the F layers' indexer queries cycle through R seeded sets."""
+
+    def __init__(self, dsa, args, cfg, lay, layers, batch, fp8, dev):
+        import math
+
+        import torch
+        self.dsa, self.lay, self.dev, self.slots = dsa, lay, dev, int(args.hot)
+        self.rotate = max(1, int(args.hot_rotate))
+        self.row_bytes = 656 if args.kv_fp8 else 1152
+        types = cfg["layers"]
+        self.cold = []
+        for L in layers:  # device cache -> pinned host memory, then the hot rows replace it
+            h = torch.empty(L["kv"].shape, dtype=L["kv"].dtype, pin_memory=True)
+            h.copy_(L["kv"])
+            self.cold.append(h)
+            shape = (lay.num_seqs * self.slots, L["kv"].shape[1])
+            L["kv"] = torch.zeros(shape, dtype=h.dtype, device=dev)
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        self.spans = [dsa.HotState(lay.num_seqs, self.slots, lay.max_len, dev) for c in types if c == "F"]
+        self.hg = dsa.HotGroup(self.spans, self.cold, num_q=lay.num_q, k=cfg["K"], device=dev)
+        self.groups = []
+        for r in range(self.rotate):
+            ls = [dict(L) for L in layers]
+            if r > 0:
+                g = torch.Generator(device=dev)
+                g.manual_seed(7000 + r)
+                for L in ls:
+                    if "q_idx" in L:
+                        q = (torch.randn((lay.num_q, 32, 128), generator=g, device=dev)
+                             / math.sqrt(128)).to(torch.bfloat16)
+                        if fp8:
+                            qc, qs = dsa.dsa_fp8_quantize(q)
+                            L.update(q_idx=qc, q_scale=qs)
+                        else:
+                            L["q_idx"] = q
+            self.groups.append(dsa.Group(types, ls, k=cfg["K"], scale=1 / 16))
+        self.ws = dsa.workspace(self.groups[0].workspace_size(batch), dev)
+        self.idx_buf = torch.empty((lay.num_q, cfg["K"]), dtype=torch.int32, device=dev)
+        self.batch = batch
+        self.n = 0
+        self.fetched = torch.zeros((), dtype=torch.int64, device=dev)
+        self.selected = int(np.minimum(lay.q_pos.astype(np.int64) + 1, cfg["K"]).sum()) * len(self.spans)
+        self.c2c_gbs = self.measure_c2c()
+
+    def step(self):
+        g = self.groups[self.n % self.rotate]
+        self.dsa.indexshare_group_forward_hot(g, self.batch, self.hg, self.n, self.idx_buf, ws=self.ws)
+        self.n += 1
+
+    def count_reset(self):
+        self.fetched.zero_()
+
+    def count(self):
+        for s in self.spans:
+            self.fetched += s.fetch_count.sum()
+
+    def measure_c2c(self):
+        """Host -> device copy rate from pinned memory (1 GiB, copy engine)."""
+        import torch
+        h = self.cold[0].view(torch.uint8).reshape(-1)
+        n = min(h.numel(), 1 << 30)
+        d = torch.empty(n, dtype=torch.uint8, device=self.dev)
+        for _ in range(2):
+            d.copy_(h[:n], non_blocking=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(4):
+            d.copy_(h[:n], non_blocking=True)
+        b.record()
+        torch.cuda.synchronize(self.dev)
+        return round(4 * n / (a.elapsed_time(b) / 1e3) / 1e9, 1)
+
+    def work(self, steps, prof):
+        """Algorithmic bytes per launch of the hot kernels: the plan reads the
+        index buffer and writes the rows; the swap-in reads the fetched rows
+        from host memory (one launch per F span)."""
+        fetched = float(self.fetched.item())
+        self.fetched_total = fetched
+        per_span_layers = len(self.cold) / max(1, len(self.spans))
+        nfetch = max(1, prof.get("hot_fetch", (0, 0))[1])
+        nplan = max(1, prof.get("hot_plan", (0, 0))[1])
+        K = self.idx_buf.shape[1]
+        plan_bytes = float(self.lay.num_q * K * 8) * len(self.spans) * steps / nplan
+        fetch_bytes = fetched * per_span_layers * self.row_bytes / nfetch
+        return {"hot_plan": {"flops": 0.0, "bytes": plan_bytes},
+                "hot_fetch": {"flops": 0.0, "bytes": fetch_bytes}}
+
+    def describe(self):
+        return (f"hot/cold: {self.slots} hot rows per sequence and layer in HBM, the full caches "
+                f"({self.row_bytes} B rows) in pinned host memory read over NVLink-C2C; "
+                f"{self.rotate} rotating indexer query set(s)")
+
+    def summary(self, steps, kernels=None):
+        fetched = getattr(self, "fetched_total", float(self.fetched.item()))
+        sel = self.selected * steps
+        fk = (kernels or {}).get("hot_fetch")
+        return {"swap_in_gbs": fk["achieved"] if fk else None,
+                "swap_in_frac_of_h2d_copy": fk["frac"] if fk else None,
+                "slots": self.slots, "rotate": self.rotate, "selected_rows": sel,
+                "fetched_rows": int(fetched), "hit_rate": round(1 - fetched / sel, 4) if sel else None,
+                "fetched_bytes_per_step": int(fetched * len(self.cold) / max(1, len(self.spans))
+                                              * self.row_bytes / steps),
+                "h2d_copy_gbs": self.c2c_gbs}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -367,6 +481,12 @@ def main():
     ap.add_argument("--kv-fp8", action="store_true",
                     help="FP8 KV latent caches (656-byte rows: E4M3 latent in four scaled groups, "
                          "bf16 RoPE key)")
+    ap.add_argument("--hot", type=int, default=0, metavar="SLOTS",
+                    help="hot/cold KV: SLOTS hot rows per sequence in HBM per layer, the full "
+                         "caches in pinned host memory, missing rows swapped in every step")
+    ap.add_argument("--hot-rotate", type=int, default=1, metavar="R",
+                    help="with --hot: step i uses the i mod R-th of R indexer query sets, so "
+                         "R > 1 changes the selected rows from step to step")
     ap.add_argument("--paged", type=int, default=0, metavar="ROWS",
                     help="paged caches: blocks of ROWS positions (a multiple of 128) in a "
                          "permuted pool, addressed through a block table")
@@ -419,7 +539,13 @@ def main():
             out.append(d)
         return out
 
-    group, ws, idx_buf = make_group(cfg["layers"])
+    hot = None
+    if args.hot:
+        hot = HotMode(dsa, args, cfg, lay, layers, batch, fp8, dev)
+        group, ws, idx_buf = hot.groups[0], hot.ws, hot.idx_buf
+        args.no_ablation = args.no_e2e = args.no_cpu = True  # those legs read device caches
+    else:
+        group, ws, idx_buf = make_group(cfg["layers"])
     appends, append_bytes, append_ws = ([], 0.0, None)
     if args.with_append:
         appends, append_bytes, append_ws = make_appends(lay, layers, cfg, fp8, batch, dev)
@@ -427,7 +553,10 @@ def main():
     def run():
         for a in appends:
             a()
-        dsa.indexshare_group_forward(group, batch, idx_buf, ws=ws)
+        if hot is not None:
+            hot.step()
+        else:
+            dsa.indexshare_group_forward(group, batch, idx_buf, ws=ws)
 
     def barrier():
         if world > 1:
@@ -451,7 +580,10 @@ def main():
     time.sleep(0.3)
     barrier()
     wall0 = time.perf_counter()
-    times = time_steps(run, args.steps, 0, flush, stream)
+    if hot is not None:
+        hot.count_reset()
+    times = time_steps(run, args.steps, 0, flush, stream,
+                       after=hot.count if hot is not None else None)
     barrier()
     wall = time.perf_counter() - wall0
     clocks = clk.stop()
@@ -469,15 +601,20 @@ def main():
     if appends:  # two launches (queries, keys) per F layer per step
         work["append"] = {"flops": 0.0, "bytes": append_bytes / (2 * len(appends))}
         dsa.status_fetch(append_ws)
+    if hot is not None:
+        work.update(hot.work(args.steps, prof))
     kernels = {}
-    for name in ("indexer", "topk", "sparse_mla", "append"):
+    for name in ("indexer", "topk", "sparse_mla", "append", "hot_plan", "hot_fetch"):
         if name not in work or name not in prof:
             continue
         ms, n = prof[name]
         if n == 0:
             continue
         avg_s = ms / n / 1e3
-        bound, peak, unit = kernel_bound(name, work[name], peaks, fp8)
+        if name == "hot_fetch":  # reads over NVLink-C2C: against the measured host->device copy
+            bound, peak, unit = "c2c", hot.c2c_gbs, "GB/s"
+        else:
+            bound, peak, unit = kernel_bound(name, work[name], peaks, fp8)
         ach = (work[name]["flops"] / avg_s / 1e12) if bound == "tensor" else (
             work[name]["bytes"] / avg_s / 1e9)
         kernels[name] = {"launches": n, "ms_per_launch": round(ms / n, 4), "share": None,
@@ -497,7 +634,10 @@ def main():
         scan_gather = {"achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
                        "frac": round(ach / peaks["hbm"], 4),
                        "what": "indexer scans + sparse-MLA gathers of the timed steps"}
-    top = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"])
+    # the dominant on-GPU kernel (the hot swap-in is bound by the host link and
+    # reported in "hot")
+    top = max((k for k in kernels if not k.startswith("hot_")),
+              key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"])
     tk = kernels[top]
     traffic = None
     if top in NCU_TRAFFIC and NCU_TRAFFIC[top].get("src") == kernel_src_hash(KSRC[top]) and \
@@ -516,7 +656,8 @@ def main():
             "config": {"workload": DESCR[args.workload], "global_batch": world * tokens_per_step,
                        "seq_len": int(lay.max_len), "layers": cfg["layers"],
                        "parallelism": "replicas" if world > 1 else "single-gpu",
-                       "kv_layout": (f"paged: blocks of {args.paged} positions, permuted pool, "
+                       "kv_layout": (hot.describe() if hot is not None else
+                                     f"paged: blocks of {args.paged} positions, permuted pool, "
                                      "block table" if args.paged else "contiguous"),
                        "kv_dtype": ("FP8 E4M3 latent, 656-byte rows" if args.kv_fp8
                                     else "bf16, 1152-byte rows"),
@@ -525,6 +666,7 @@ def main():
                        "l2": "flushed between steps (256 MiB write, outside the timed events)"},
             "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
             "scan_gather_hbm": scan_gather,
+            "hot": hot.summary(args.steps, kernels) if hot is not None else None,
             "clocks": clocks, "wall_s_timed": round(wall, 3)}
 
     # ---- IndexShare ablation: every layer runs its own indexer

@@ -18,15 +18,17 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdsa.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE = 0, 1, 2, 3
-DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX = 4, 5, 6
+DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_DEVICE_INDEX, DSA_ERR_HOT_OVERFLOW = 4, 5, 6, 7
 DSA_BF16, DSA_FP8_E4M3 = 0, 1
 INDEX_HEADS, INDEX_DIM, LATENT, ROPE, KV_ROW, KV_ROW_FP8 = 32, 128, 512, 64, 576, 656
 STATUS_BYTES = 256
-LAUNCH_KINDS = ("indexer", "topk", "sparse_mla", "combine", "fp8_quantize", "append", "other")
+LAUNCH_KINDS = ("indexer", "topk", "sparse_mla", "combine", "fp8_quantize", "append", "hot_plan",
+                "hot_fetch", "other")
+HOT_MAX_SLOTS = 16384
 
 STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
                 3: "DSA_ERR_WORKSPACE", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT",
-                6: "DSA_ERR_DEVICE_INDEX"}
+                6: "DSA_ERR_DEVICE_INDEX", 7: "DSA_ERR_HOT_OVERFLOW"}
 
 
 class DsaError(RuntimeError):
@@ -51,6 +53,17 @@ class _Group(ctypes.Structure):
                 ("k_rows", c_int64), ("q_lat", _PP), ("q_rope", _PP), ("kv", _PP), ("out", _PP),
                 ("lse", _PP), ("q_idx", _PP), ("q_scale", _PP), ("w", _PP), ("k_idx", _PP),
                 ("k_scale", _PP), ("kv_dtype", c_int)]
+
+
+class _Hot(ctypes.Structure):
+    _fields_ = [("hot_slots", c_int32), ("max_pos", c_int32), ("slot_pos", c_void_p),
+                ("slot_stamp", c_void_p), ("pos_slot", c_void_p), ("fetch_pos", c_void_p),
+                ("fetch_slot", c_void_p), ("fetch_count", c_void_p)]
+
+
+class _HotGroup(ctypes.Structure):
+    _fields_ = [("spans", POINTER(_Hot)), ("n_spans", c_int32), ("cold_kv", _PP),
+                ("cold_rows", c_int64), ("step", c_int32), ("rows", c_void_p)]
 
 
 def _load():
@@ -92,6 +105,15 @@ def _load():
                                          c_size_t, c_void_p]),
         "dsa_indexer_prepare_queries": (st, [c_void_p, B, c_int, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_size_t, c_void_p]),
+        "dsa_hot_plan": (st, [c_void_p, c_int32, B, POINTER(_Hot), c_int32, c_void_p, c_void_p,
+                              c_size_t, c_void_p]),
+        "dsa_hot_fetch": (st, [POINTER(_Hot), B, c_int32, _PP, c_int64, _PP, c_int, c_void_p,
+                               c_size_t, c_void_p]),
+        "dsa_sparse_mla_attn_rows": (st, [c_void_p, c_void_p, c_void_p, c_int64, c_int, c_void_p,
+                                          c_int32, c_int32, c_float, B, c_void_p, c_void_p,
+                                          c_void_p, c_size_t, c_void_p]),
+        "indexshare_group_forward_hot": (st, [POINTER(_Group), B, POINTER(_HotGroup), c_void_p,
+                                              c_void_p, c_size_t, c_void_p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -460,3 +482,150 @@ def dsa_indexer_prepare_queries(q_new, batch: Batch, inv_freq, *, fp8=False, q_o
                                            _ptr(q_scale) if fp8 else None, _ptr(ws), ws.numel(),
                                            _stream(stream, dev)), "dsa_indexer_prepare_queries")
     return (q_out, q_scale) if fp8 else q_out
+
+
+# ---------------------------------------------------------------- hot / cold KV
+def _cold(t, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be page-locked host memory (pin_memory) or a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class HotState:
+    """Hot-buffer state of one index span (dsa_hot_t) on the device: slot ->
+    position, slot stamps, position -> slot for positions < max_pos, and the
+    last plan's fetch lists."""
+
+    def __init__(self, num_seqs: int, hot_slots: int, max_pos: int, device="cuda"):
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.num_seqs, self.hot_slots, self.max_pos, self.device = num_seqs, hot_slots, max_pos, dev
+        self.slot_pos = torch.full((num_seqs, hot_slots), -1, **i32)
+        self.slot_stamp = torch.full((num_seqs, hot_slots), -1, **i32)
+        self.pos_slot = torch.full((num_seqs, max_pos), -1, **i32)
+        self.fetch_pos = torch.zeros((num_seqs, hot_slots), **i32)
+        self.fetch_slot = torch.zeros((num_seqs, hot_slots), **i32)
+        self.fetch_count = torch.zeros((num_seqs,), **i32)
+        self._c = _Hot(hot_slots, max_pos, *[_ptr(t) for t in (
+            self.slot_pos, self.slot_stamp, self.pos_slot, self.fetch_pos, self.fetch_slot,
+            self.fetch_count)])
+
+    @property
+    def c(self):
+        return ctypes.byref(self._c)
+
+    def fetch_lists(self):
+        """[(position, slot), ...] per sequence of the last plan (host copy)."""
+        n = self.fetch_count.cpu().tolist()
+        fp, fs = self.fetch_pos.cpu(), self.fetch_slot.cpu()
+        return [list(zip(fp[b, :n[b]].tolist(), fs[b, :n[b]].tolist())) for b in range(self.num_seqs)]
+
+
+def dsa_hot_plan(idx, batch: Batch, state: HotState, step: int, rows=None, *, ws=None, stream=None):
+    """One step of the hot buffer: returns rows int32 [num_q, k], the hot row
+    of every valid index entry (-1 elsewhere); the state's fetch lists name
+    the rows to swap in."""
+    dev = batch.device
+    _need(idx, "idx", torch.int32, dev)
+    k = idx.shape[1]
+    if rows is None:
+        rows = torch.empty((batch.num_q, k), dtype=torch.int32, device=dev)
+    _need(rows, "rows", torch.int32, dev, (batch.num_q, k))
+    if ws is None:
+        ws = workspace(STATUS_BYTES, dev)
+    _check(lib.dsa_hot_plan(_ptr(idx), k, batch.c, state.c, int(step), _ptr(rows), _ptr(ws),
+                            ws.numel(), _stream(stream, dev)), "dsa_hot_plan")
+    return rows
+
+
+def dsa_hot_fetch(state: HotState, batch: Batch, cold_kv, hot_kv, *, ws=None, stream=None):
+    """Swap in the last plan's rows for every layer: hot_kv[l] (device, bf16
+    [num_seqs * hot_slots, 576] or uint8 [.., 656]) from cold_kv[l] (pinned host
+    memory, the batch's cache layout)."""
+    dev = batch.device
+    n = len(cold_kv)
+    if len(hot_kv) != n:
+        raise ValueError("one hot array per cold cache")
+    fp8 = cold_kv[0].dtype == torch.uint8
+    row = KV_ROW_FP8 if fp8 else KV_ROW
+    for l in range(n):
+        _cold(cold_kv[l], f"cold_kv[{l}]")
+        _need(hot_kv[l], f"hot_kv[{l}]", cold_kv[0].dtype, dev,
+              (state.num_seqs * state.hot_slots, row))
+        if cold_kv[l].dtype != cold_kv[0].dtype or tuple(cold_kv[l].shape) != tuple(cold_kv[0].shape):
+            raise ValueError("cold caches must share dtype and shape")
+    if ws is None:
+        ws = workspace(STATUS_BYTES, dev)
+    cold = (c_void_p * n)(*[t.data_ptr() for t in cold_kv])
+    hot = (c_void_p * n)(*[t.data_ptr() for t in hot_kv])
+    _check(lib.dsa_hot_fetch(state.c, batch.c, n, ctypes.cast(cold, _PP), cold_kv[0].shape[0],
+                             ctypes.cast(hot, _PP), DSA_FP8_E4M3 if fp8 else DSA_BF16, _ptr(ws),
+                             ws.numel(), _stream(stream, dev)), "dsa_hot_fetch")
+    return hot_kv
+
+
+def dsa_sparse_mla_attn_rows(q_lat, q_rope, kv, rows, batch: Batch, *, scale: float, out=None,
+                             lse=None, with_lse=True, ws=None, stream=None):
+    """dsa_sparse_mla_attn whose index entries are absolute kv rows (e.g. the
+    hot rows of dsa_hot_plan)."""
+    dev = batch.device
+    H = q_lat.shape[1]
+    _need(q_lat, "q_lat", torch.bfloat16, dev, (batch.num_q, H, LATENT))
+    _need(q_rope, "q_rope", torch.bfloat16, dev, (batch.num_q, H, ROPE))
+    _need(kv, "kv", (torch.bfloat16, torch.uint8), dev)
+    fp8 = kv.dtype == torch.uint8
+    if kv.dim() != 2 or kv.shape[1] != (KV_ROW_FP8 if fp8 else KV_ROW):
+        raise ValueError("kv must be bf16 [rows, 576] or uint8 [rows, 656]")
+    _need(rows, "rows", torch.int32, dev)
+    k = rows.shape[1]
+    if out is None:
+        out = torch.empty((batch.num_q, H, LATENT), dtype=torch.bfloat16, device=dev)
+    if lse is None and with_lse:
+        lse = torch.empty((batch.num_q, H), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(lib.dsa_sparse_mla_workspace_size(batch.c, H, k), dev)
+    _check(lib.dsa_sparse_mla_attn_rows(_ptr(q_lat), _ptr(q_rope), _ptr(kv), kv.shape[0],
+                                        DSA_FP8_E4M3 if fp8 else DSA_BF16, _ptr(rows), k, H,
+                                        float(scale), batch.c, _ptr(out), _ptr(lse), _ptr(ws),
+                                        ws.numel(), _stream(stream, dev)), "dsa_sparse_mla_attn_rows")
+    return out, lse
+
+
+class HotGroup:
+    """Hot / cold arguments of indexshare_group_forward_hot (dsa_hot_group_t):
+    one HotState per F layer, the layers' cold caches in pinned host memory
+    (the group's layers[l]["kv"] are then the hot arrays)."""
+
+    def __init__(self, spans, cold_kv, *, num_q: int, k: int, device="cuda"):
+        self.spans = list(spans)
+        self.cold_kv = list(cold_kv)
+        for l, t in enumerate(self.cold_kv):
+            _cold(t, f"cold_kv[{l}]")
+        self.rows = torch.empty((num_q, k), dtype=torch.int32, device=device)
+        self._spans = (_Hot * len(self.spans))(*[s._c for s in self.spans])
+        self._cold = (c_void_p * len(self.cold_kv))(*[t.data_ptr() for t in self.cold_kv])
+        self._c = _HotGroup(ctypes.cast(self._spans, POINTER(_Hot)), len(self.spans),
+                            ctypes.cast(self._cold, _PP), self.cold_kv[0].shape[0], 0,
+                            _ptr(self.rows))
+
+
+def indexshare_group_forward_hot(group: Group, batch: Batch, hot: HotGroup, step: int,
+                                 idx_buf=None, *, ws=None, stream=None):
+    """indexshare_group_forward over hot buffers: per F layer, select, plan the
+    span's hot buffer, swap in its missing rows for every layer of the span,
+    and attend over hot rows.  Returns (outs, lses, idx_buf)."""
+    dev = batch.device
+    if idx_buf is None:
+        idx_buf = torch.empty((batch.num_q, group.k), dtype=torch.int32, device=dev)
+    _need(idx_buf, "idx_buf", torch.int32, dev, (batch.num_q, group.k))
+    if ws is None:
+        ws = workspace(group.workspace_size(batch), dev)
+    hot._c.step = int(step)
+    _check(lib.indexshare_group_forward_hot(group.c, batch.c, ctypes.byref(hot._c), _ptr(idx_buf),
+                                            _ptr(ws), ws.numel(), _stream(stream, dev)),
+           "indexshare_group_forward_hot")
+    return group.outs, group.lses, idx_buf

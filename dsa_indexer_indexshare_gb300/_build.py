@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdsa.so")
-SOURCES = ["api.cu", "indexer.cu", "topk.cu", "sparse_mla.cu", "quant.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "indexer.cu", "topk.cu", "sparse_mla.cu", "quant.cu", "noalloc.cu", "hot.cu"]
 HEADERS = ["common.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -115,6 +115,72 @@ dsa_status_t check_mla_args(const void* q_lat, const void* q_rope, const void* k
 
 dsa_status_t launch_status(cudaError_t e, const char* where) { return cuda_status(e, where); }
 
+dsa_status_t check_hot(const dsa_hot_t* h, const dsa_batch_t* b) {
+  if (!h) return fail(DSA_ERR_INVALID_ARG, "hot state is NULL");
+  if (h->hot_slots < 1 || h->hot_slots > DSA_HOT_MAX_SLOTS)
+    return fail(DSA_ERR_UNSUPPORTED, "hot_slots=%d (supported: 1..%d)", h->hot_slots,
+                static_cast<int>(DSA_HOT_MAX_SLOTS));
+  if (h->max_pos < b->max_len)
+    return fail(DSA_ERR_INVALID_ARG, "hot state max_pos=%d < batch max_len=%d", h->max_pos, b->max_len);
+  if (static_cast<int64_t>(b->num_seqs) * h->hot_slots > (int64_t(1) << 31) - 1)
+    return fail(DSA_ERR_UNSUPPORTED, "num_seqs * hot_slots >= 2^31");
+  if (!h->slot_pos || !h->slot_stamp || !h->pos_slot || !h->fetch_pos || !h->fetch_slot ||
+      !h->fetch_count)
+    return fail(DSA_ERR_INVALID_ARG, "hot state arrays must be non-NULL device pointers");
+  return DSA_OK;
+}
+
+// The layer string and every layer's arguments of a group call (the batch is
+// checked by the caller).
+dsa_status_t check_group(const dsa_group_t* g, const dsa_batch_t* b, const int32_t* idx_buf) {
+  if (!g->layer_types || g->layer_types[0] != 'F')
+    return fail(DSA_ERR_INVALID_ARG, "layer_types must start with F");
+  const int nl = static_cast<int>(strlen(g->layer_types));
+  if (nl > 4096) return fail(DSA_ERR_INVALID_ARG, "layer_types too long");
+  for (int l = 0; l < nl; ++l)
+    if (g->layer_types[l] != 'F' && g->layer_types[l] != 'S')
+      return fail(DSA_ERR_INVALID_ARG, "layer_types[%d] = '%c' (want F or S)", l, g->layer_types[l]);
+  if (!g->q_lat || !g->q_rope || !g->kv || !g->out || !idx_buf)
+    return fail(DSA_ERR_INVALID_ARG, "q_lat, q_rope, kv, out arrays and idx_buf are required");
+  for (int l = 0; l < nl; ++l) {
+    if (dsa_status_t s = check_mla_args(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, idx_buf,
+                                        g->k, g->heads, g->scale, b, g->out[l]))
+      return s;
+    if (g->layer_types[l] == 'F') {
+      if (!g->q_idx || !g->w || !g->k_idx ||
+          (g->idx_dtype == DSA_FP8_E4M3 && (!g->q_scale || !g->k_scale)))
+        return fail(DSA_ERR_INVALID_ARG, "F layer %d: indexer arrays missing", l);
+      if (dsa_status_t s = check_indexer_args(g->q_idx[l], g->q_scale ? g->q_scale[l] : nullptr,
+                                              g->w[l], g->k_idx[l],
+                                              g->k_scale ? g->k_scale[l] : nullptr, g->k_rows,
+                                              g->idx_dtype))
+        return s;
+    }
+  }
+  if (g->kv_dtype != DSA_BF16 && g->kv_dtype != DSA_FP8_E4M3)
+    return fail(DSA_ERR_UNSUPPORTED, "kv_dtype %d", g->kv_dtype);
+  if (g->kv_dtype == DSA_FP8_E4M3 && g->heads != 64)
+    return fail(DSA_ERR_UNSUPPORTED, "FP8 KV rows: heads must be 64");
+  return DSA_OK;
+}
+
+// A pointer the device can dereference: device, managed or page-locked host
+// memory (its device address returned); pageable host memory is refused.
+dsa_status_t device_view(const void* p, const char* what, int l, const void** dev) {
+  if (!p) return fail(DSA_ERR_INVALID_ARG, "%s[%d] is NULL", what, l);
+  if (!aligned16(p)) return fail(DSA_ERR_INVALID_ARG, "%s[%d] must be 16-byte aligned", what, l);
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DSA_ERR_INVALID_ARG, "%s[%d]: not memory CUDA knows", what, l);
+  }
+  if ((a.type != cudaMemoryTypeHost && a.type != cudaMemoryTypeDevice &&
+       a.type != cudaMemoryTypeManaged) || !a.devicePointer)
+    return fail(DSA_ERR_INVALID_ARG, "%s[%d]: pageable host memory (page-lock it first)", what, l);
+  *dev = a.devicePointer;
+  return DSA_OK;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------- host helpers
@@ -220,6 +286,8 @@ dsa_status_t dsa_status_fetch(void* d_ws, dsa_stream_t stream, int32_t* raw_bits
   if (bits & DSA_DEVERR_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a bounded wait in a kernel ran out");
   if (bits & (DSA_DEVERR_INDEX | DSA_DEVERR_BATCH))
     return fail(DSA_ERR_DEVICE_INDEX, "a kernel found an index or batch entry out of range (bits %d)", bits);
+  if (bits & DSA_DEVERR_HOT_OVERFLOW)
+    return fail(DSA_ERR_HOT_OVERFLOW, "a sequence selected more positions than its hot buffer has free slots");
   return DSA_OK;
 }
 
@@ -350,30 +418,8 @@ dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b
                                       void* ws, size_t ws_bytes, dsa_stream_t stream) {
   if (!g) return fail(DSA_ERR_INVALID_ARG, "group is NULL");
   if (dsa_status_t s = check_batch(b)) return s;
-  if (!g->layer_types || g->layer_types[0] != 'F')
-    return fail(DSA_ERR_INVALID_ARG, "layer_types must start with F");
+  if (dsa_status_t s = check_group(g, b, idx_buf)) return s;
   const int nl = static_cast<int>(strlen(g->layer_types));
-  if (nl > 4096) return fail(DSA_ERR_INVALID_ARG, "layer_types too long");
-  for (int l = 0; l < nl; ++l)
-    if (g->layer_types[l] != 'F' && g->layer_types[l] != 'S')
-      return fail(DSA_ERR_INVALID_ARG, "layer_types[%d] = '%c' (want F or S)", l, g->layer_types[l]);
-  if (!g->q_lat || !g->q_rope || !g->kv || !g->out || !idx_buf)
-    return fail(DSA_ERR_INVALID_ARG, "q_lat, q_rope, kv, out arrays and idx_buf are required");
-  for (int l = 0; l < nl; ++l) {
-    if (dsa_status_t s = check_mla_args(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, idx_buf,
-                                        g->k, g->heads, g->scale, b, g->out[l]))
-      return s;
-    if (g->layer_types[l] == 'F') {
-      if (!g->q_idx || !g->w || !g->k_idx ||
-          (g->idx_dtype == DSA_FP8_E4M3 && (!g->q_scale || !g->k_scale)))
-        return fail(DSA_ERR_INVALID_ARG, "F layer %d: indexer arrays missing", l);
-      if (dsa_status_t s = check_indexer_args(g->q_idx[l], g->q_scale ? g->q_scale[l] : nullptr,
-                                              g->w[l], g->k_idx[l],
-                                              g->k_scale ? g->k_scale[l] : nullptr, g->k_rows,
-                                              g->idx_dtype))
-        return s;
-    }
-  }
   const size_t need = dsa_group_workspace_size(g, b);
   if (dsa_status_t s = check_ws(ws, ws_bytes, need)) return s;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -384,8 +430,6 @@ dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b
   const size_t topk_bytes = round256(topk_scratch_bytes(*b, g->k));
   const bool fp8 = g->idx_dtype == DSA_FP8_E4M3;
   const bool kv_fp8 = g->kv_dtype == DSA_FP8_E4M3;
-  if (g->kv_dtype != DSA_BF16 && !kv_fp8) return fail(DSA_ERR_UNSUPPORTED, "kv_dtype");
-  if (kv_fp8 && g->heads != 64) return fail(DSA_ERR_UNSUPPORTED, "FP8 KV rows: heads must be 64");
   for (int l = 0; l < nl; ++l) {
     if (g->layer_types[l] == 'F') {
       // F layer: candidate scoring, then top-K into the shared index buffer
@@ -411,6 +455,143 @@ dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b
   return DSA_OK;
 }
 
+// ------------------------------------------------------------- hot / cold KV
+dsa_status_t dsa_hot_plan(const int32_t* idx, int32_t k, const dsa_batch_t* b, const dsa_hot_t* h,
+                          int32_t step, int32_t* rows, void* ws, size_t ws_bytes,
+                          dsa_stream_t stream) {
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (dsa_status_t s = check_hot(h, b)) return s;
+  if (k < 1 || k > 4096) return fail(DSA_ERR_UNSUPPORTED, "k=%d (supported: 1..4096)", k);
+  if (step < 0) return fail(DSA_ERR_INVALID_ARG, "step < 0");
+  if (b->num_q > 0 && (!idx || !rows)) return fail(DSA_ERR_INVALID_ARG, "idx and rows are required");
+  if (static_cast<int64_t>(b->num_q) * k > (int64_t(1) << 31) - 4)
+    return fail(DSA_ERR_UNSUPPORTED, "num_q * k >= 2^31");
+  if (dsa_status_t s = check_ws(ws, ws_bytes, kStatusBytes)) return s;
+  return launch_status(launch_hot_plan(idx, k, *b, *h, step, rows, static_cast<int*>(ws), stream),
+                       "hot plan launch");
+}
+
+namespace {
+dsa_status_t hot_fetch_impl(const dsa_hot_t* h, const dsa_batch_t* b, int32_t layers,
+                            const void* const* cold_kv, int64_t cold_rows, void* const* hot_kv,
+                            dsa_dtype_t kv_dtype, int* status, cudaStream_t stream) {
+  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_FP8_E4M3) return fail(DSA_ERR_UNSUPPORTED, "kv_dtype");
+  if (layers < 0 || layers > 4096) return fail(DSA_ERR_INVALID_ARG, "layers=%d", layers);
+  if (layers == 0) return DSA_OK;
+  if (!cold_kv || !hot_kv) return fail(DSA_ERR_INVALID_ARG, "cold_kv and hot_kv are required");
+  if (cold_rows < 1) return fail(DSA_ERR_INVALID_ARG, "cold_rows < 1");
+  std::vector<const void*> cold(static_cast<size_t>(layers));
+  for (int l = 0; l < layers; ++l) {
+    if (dsa_status_t s = device_view(cold_kv[l], "cold_kv", l, &cold[l])) return s;
+    if (!hot_kv[l] || !aligned16(hot_kv[l]))
+      return fail(DSA_ERR_INVALID_ARG, "hot_kv[%d] must be a 16-byte aligned device pointer", l);
+  }
+  const int row_bytes = kv_dtype == DSA_FP8_E4M3 ? DSA_KV_ROW_BYTES_FP8 : DSA_KV_ROW_BYTES;
+  return launch_status(launch_hot_fetch(*h, *b, layers, cold.data(), cold_rows, hot_kv, row_bytes,
+                                        status, stream),
+                       "hot fetch launch");
+}
+}  // namespace
+
+dsa_status_t dsa_hot_fetch(const dsa_hot_t* h, const dsa_batch_t* b, int32_t layers,
+                           const void* const* cold_kv, int64_t cold_rows, void* const* hot_kv,
+                           dsa_dtype_t kv_dtype, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (dsa_status_t s = check_hot(h, b)) return s;
+  if (dsa_status_t s = check_ws(ws, ws_bytes, kStatusBytes)) return s;
+  return hot_fetch_impl(h, b, layers, cold_kv, cold_rows, hot_kv, kv_dtype, static_cast<int*>(ws),
+                        stream);
+}
+
+dsa_status_t dsa_sparse_mla_attn_rows(const void* q_lat, const void* q_rope, const void* kv,
+                                      int64_t kv_rows, dsa_dtype_t kv_dtype, const int32_t* rows,
+                                      int32_t k, int32_t heads, float scale, const dsa_batch_t* b,
+                                      void* out, float* lse, void* ws, size_t ws_bytes,
+                                      dsa_stream_t stream) {
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (dsa_status_t s = check_mla_args(q_lat, q_rope, kv, kv_rows, rows, k, heads, scale, b, out)) return s;
+  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_FP8_E4M3) return fail(DSA_ERR_UNSUPPORTED, "kv_dtype");
+  const bool kv_fp8 = kv_dtype == DSA_FP8_E4M3;
+  if (kv_fp8 && heads != 64) return fail(DSA_ERR_UNSUPPORTED, "FP8 KV rows: heads must be 64");
+  const size_t need = dsa_sparse_mla_workspace_size(b, heads, k);
+  if (dsa_status_t s = check_ws(ws, ws_bytes, need)) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  return launch_status(launch_sparse_mla(q_lat, q_rope, kv, kv_rows, rows, k, heads, scale, *b, out,
+                                         lse, wsb + kStatusBytes, need - kStatusBytes,
+                                         static_cast<int*>(ws), stream, kv_fp8, true),
+                       "sparse MLA (rows) launch");
+}
+
+dsa_status_t indexshare_group_forward_hot(const dsa_group_t* g, const dsa_batch_t* b,
+                                          const dsa_hot_group_t* hot, int32_t* idx_buf, void* ws,
+                                          size_t ws_bytes, dsa_stream_t stream) {
+  if (!g) return fail(DSA_ERR_INVALID_ARG, "group is NULL");
+  if (!hot) return fail(DSA_ERR_INVALID_ARG, "hot group is NULL");
+  if (dsa_status_t s = check_batch(b)) return s;
+  if (dsa_status_t s = check_group(g, b, idx_buf)) return s;
+  const int nl = static_cast<int>(strlen(g->layer_types));
+  int nf = 0;
+  for (int l = 0; l < nl; ++l) nf += g->layer_types[l] == 'F';
+  if (hot->n_spans != nf || !hot->spans)
+    return fail(DSA_ERR_INVALID_ARG, "hot->n_spans=%d, layer_types has %d F layers", hot->n_spans, nf);
+  if (!hot->rows || !hot->cold_kv) return fail(DSA_ERR_INVALID_ARG, "hot->rows and hot->cold_kv are required");
+  if (hot->step < 0) return fail(DSA_ERR_INVALID_ARG, "hot->step < 0");
+  for (int i = 0; i < nf; ++i) {
+    if (dsa_status_t s = check_hot(&hot->spans[i], b)) return s;
+    if (g->kv_rows < static_cast<int64_t>(b->num_seqs) * hot->spans[i].hot_slots)
+      return fail(DSA_ERR_INVALID_ARG, "kv_rows=%lld < num_seqs * hot_slots of span %d",
+                  static_cast<long long>(g->kv_rows), i);
+  }
+  if (static_cast<int64_t>(b->num_q) * g->k > (int64_t(1) << 31) - 4)
+    return fail(DSA_ERR_UNSUPPORTED, "num_q * k >= 2^31");
+  const size_t need = dsa_group_workspace_size(g, b);
+  if (dsa_status_t s = check_ws(ws, ws_bytes, need)) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  int* status = static_cast<int*>(ws);
+  float* scores = reinterpret_cast<float*>(wsb + kStatusBytes);
+  const size_t score_bytes = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4);
+  uint8_t* topk_scratch = wsb + kStatusBytes + score_bytes;
+  const size_t topk_bytes = round256(topk_scratch_bytes(*b, g->k));
+  const bool fp8 = g->idx_dtype == DSA_FP8_E4M3;
+  const bool kv_fp8 = g->kv_dtype == DSA_FP8_E4M3;
+  int span = -1;
+  for (int l = 0; l < nl; ++l) {
+    if (g->layer_types[l] == 'F') {
+      ++span;
+      if (dsa_status_t s = launch_status(
+              launch_indexer(g->q_idx[l], fp8 ? g->q_scale[l] : nullptr, g->w[l], g->k_idx[l],
+                             fp8 ? g->k_scale[l] : nullptr, g->k_rows, fp8, *b, scores, false,
+                             status, stream),
+              "indexer launch"))
+        return s;
+      if (dsa_status_t s = launch_status(launch_topk(scores, *b, g->k, idx_buf, status,
+                                                     topk_scratch, topk_bytes, stream),
+                                         "top-K launch"))
+        return s;
+      // one plan for the span, then the span's missing rows for all of its layers
+      const dsa_hot_t& h = hot->spans[span];
+      if (dsa_status_t s = launch_status(
+              launch_hot_plan(idx_buf, g->k, *b, h, hot->step, hot->rows, status, stream),
+              "hot plan launch"))
+        return s;
+      int l1 = l + 1;
+      while (l1 < nl && g->layer_types[l1] == 'S') ++l1;
+      if (dsa_status_t s = hot_fetch_impl(&h, b, l1 - l, hot->cold_kv + l, hot->cold_rows,
+                                          const_cast<void* const*>(g->kv + l), g->kv_dtype, status,
+                                          stream))
+        return s;
+    }
+    if (dsa_status_t s = launch_status(
+            launch_sparse_mla(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, hot->rows, g->k,
+                              g->heads, g->scale, *b, g->out[l], g->lse ? g->lse[l] : nullptr,
+                              wsb + kStatusBytes, need - kStatusBytes, status, stream, kv_fp8,
+                              true),
+            "sparse MLA launch"))
+      return s;
+  }
+  return DSA_OK;
+}
+
 // ------------------------------------------------------------- a7: FP8 quantiser
 dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
                               dsa_stream_t stream) {
@@ -423,7 +604,7 @@ dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float
   return launch_status(launch_quantize(x, rows, codes, scale, stream), "quantiser launch");
 }
 
-// ------------------------------------------------------------- NEXT-2: FP8 KV rows
+// ------------------------------------------------------------- FP8 KV rows
 dsa_status_t dsa_kv_fp8_quantize(const void* kv, int64_t rows, uint8_t* out, dsa_stream_t stream) {
   if (rows < 0) return fail(DSA_ERR_INVALID_ARG, "rows < 0");
   if (rows > 0 && (!kv || !out)) return fail(DSA_ERR_INVALID_ARG, "kv and out are required");
@@ -433,7 +614,7 @@ dsa_status_t dsa_kv_fp8_quantize(const void* kv, int64_t rows, uint8_t* out, dsa
   return launch_status(launch_kv_fp8_quantize(kv, rows, out, stream), "KV quantiser launch");
 }
 
-// ------------------------------------------------------------- NEXT-3: cache append
+// ------------------------------------------------------------- indexer cache append
 dsa_status_t dsa_indexer_append_keys(const void* k_new, const int32_t* k_seq,
                                      const int32_t* k_pos, int32_t n, const dsa_batch_t* b,
                                      dsa_dtype_t dt, const double* inv_freq, void* k_cache,

@@ -75,7 +75,7 @@ void prof_end(int which, cudaStream_t stream);
 uint64_t wait_timeout_ns();
 
 enum LaunchKind { kLaunchIndexer = 0, kLaunchTopk, kLaunchMla, kLaunchCombine, kLaunchQuant,
-                  kLaunchAppend, kLaunchOther, kNumLaunchKinds };
+                  kLaunchAppend, kLaunchHot, kLaunchFetch, kLaunchOther, kNumLaunchKinds };
 
 // Launchers (return a CUDA error code; argument checks are done by api.cu).
 cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float* w,
@@ -90,7 +90,14 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
                               const dsa_batch_t& b, void* out, float* lse, void* ws_extra,
                               size_t ws_extra_bytes, int* status, cudaStream_t stream,
-                              bool kv_fp8 = false);
+                              bool kv_fp8 = false, bool direct_rows = false);
+// Hot / cold KV: the plan of one step (one CTA per sequence) and the swap-in
+// of its fetch lists for `layers` layers from host-resident cold caches.
+cudaError_t launch_hot_plan(const int32_t* idx, int k, const dsa_batch_t& b, const dsa_hot_t& h,
+                            int step, int32_t* rows, int* status, cudaStream_t stream);
+cudaError_t launch_hot_fetch(const dsa_hot_t& h, const dsa_batch_t& b, int layers,
+                             const void* const* cold, int64_t cold_rows, void* const* hot,
+                             int row_bytes, int* status, cudaStream_t stream);
 // RoPE (+ Hadamard + FP8) of n indexer vectors; vector v at position
 // pos_of[v / group], written to the cache row of (seq_of[v / group], pos)
 // (seq_of set) or to row v.  inv_freq: 32 host doubles.

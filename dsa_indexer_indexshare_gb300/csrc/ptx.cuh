@@ -18,6 +18,7 @@ enum : int {
   DSA_DEVERR_TIMEOUT = 1,     // a bounded wait ran out
   DSA_DEVERR_INDEX = 2,       // an index entry outside [-1, q_pos]
   DSA_DEVERR_BATCH = 4,       // q_start / q_pos inconsistent with the sizes
+  DSA_DEVERR_HOT_OVERFLOW = 8,  // more misses than unused hot slots
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

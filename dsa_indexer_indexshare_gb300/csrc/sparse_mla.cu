@@ -90,6 +90,7 @@ struct MlaParams {
   const uint16_t* kv;  // [kv_rows, 576] bf16
   const uint8_t* kv8;  // or FP8 rows [kv_rows, 656]: 512 E4M3, 4 fp32 group scales, 64 bf16
   int64_t kv_rows;
+  int direct;  // index entries are absolute kv rows (no causal test), not positions
   const int32_t* idx;
   int K;
   float scale_log2;
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   const int nvalid = pos < 0 ? 0 : min(p.K, pos + 1);
   const int nb = (nvalid + 127) / 128;
   const int j0 = rank * nb / NSPLIT, j1 = (rank + 1) * nb / NSPLIT;  // this CTA's blocks
-  const int64_t row0 = seq_base_row(p.b, seq);
+  const int64_t row0 = p.direct ? 0 : seq_base_row(p.b, seq);
   const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.K;
   if (nb == 0) {  // nothing visible: zero output, lse = -inf
     constexpr int DS = 512 / NSPLIT;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       for (int c = 0; c < RPT; ++c) {
         const int e = gsel[c];
         const int64_t rr = e >= 0 ? row_of(e) : -1;
-        const bool ok = e >= 0 && e <= pos && rr >= 0 && rr < p.kv_rows;
+        const bool ok = e >= 0 && (p.direct || e <= pos) && rr >= 0 && rr < p.kv_rows;
         if (!ok && e != -1 && kch == 0) atomicOr(p.status, DSA_DEVERR_INDEX);
         grow[c] = ok ? static_cast<int>(rr) : 0;
       }
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       if (more) fetch_sel(j + 1);  // consumed after P of this block
       if (!mbar_wait(bar(B_S), u & 1, abort_flag, p.status, to)) break;
       tc_fence_after();
-      bool valid = e >= 0 && e <= pos;  // the gather's test, on this thread's key
+      bool valid = e >= 0 && (p.direct || e <= pos);  // the gather's test, on this thread's key
       if (valid) {
         const int64_t rr = row_of(e);
         valid = rr >= 0 && rr < p.kv_rows;
@@ -752,7 +753,7 @@ size_t mla_workspace_bytes(const dsa_batch_t&, int, int) { return 0; }
 cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void* kv,
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
                               const dsa_batch_t& b, void* out, float* lse, void*, size_t,
-                              int* status, cudaStream_t stream, bool kv_fp8) {
+                              int* status, cudaStream_t stream, bool kv_fp8, bool direct_rows) {
   if (b.num_q == 0) return cudaSuccess;
   CUtensorMap ql, qr;
   const uint64_t qrows = static_cast<uint64_t>(b.num_q) * heads;
@@ -764,6 +765,7 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   p.kv = kv_fp8 ? nullptr : static_cast<const uint16_t*>(kv);
   p.kv8 = kv_fp8 ? static_cast<const uint8_t*>(kv) : nullptr;
   p.kv_rows = kv_rows;
+  p.direct = direct_rows ? 1 : 0;
   p.idx = idx;
   p.K = k;
   p.scale_log2 = scale * kLog2e;
@@ -777,7 +779,7 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   int nsplit = 1;
   while (nsplit < 8 && nsplit * 2 <= nblk && static_cast<int64_t>(b.num_q) * nsplit * 2 <= 152)
     nsplit *= 2;
-  const bool paged = b.block_table != nullptr;
+  const bool paged = b.block_table != nullptr && !direct_rows;
   if (kv_fp8) {  // FP8 KV rows: the model's 64 heads only
     if (heads != 64) return cudaErrorNotSupported;
     return launch_h<64, true>(ql, qr, p, nsplit, paged, stream);

@@ -56,7 +56,9 @@ typedef enum {
   DSA_ERR_WORKSPACE = 3,   /* workspace null or smaller than the matching *_workspace_size */
   DSA_ERR_CUDA = 4,        /* a CUDA runtime call failed (see dsa_last_error_string) */
   DSA_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel ran out */
-  DSA_ERR_DEVICE_INDEX = 6 /* device: an index outside [-1, q_pos], or bad batch arrays */
+  DSA_ERR_DEVICE_INDEX = 6, /* device: an index outside [-1, q_pos], or bad batch arrays */
+  DSA_ERR_HOT_OVERFLOW = 7  /* device: a sequence selected more distinct positions than its
+                               hot buffer has slots free at this step */
 } dsa_status_t;
 
 typedef enum { DSA_BF16 = 0, DSA_FP8_E4M3 = 1 } dsa_dtype_t;
@@ -67,7 +69,10 @@ enum {
   DSA_INDEX_DIM = 128,  /* indexer width; one shared 128-d key per position */
   DSA_LATENT = 512,     /* MLA KV latent */
   DSA_ROPE = 64,        /* MLA RoPE key */
-  DSA_KV_ROW = 576      /* latent + RoPE key, one cache row */
+  DSA_KV_ROW = 576,     /* latent + RoPE key, one cache row */
+  DSA_KV_ROW_BYTES = 1152,     /* bytes of a bf16 KV row */
+  DSA_KV_ROW_BYTES_FP8 = 656,  /* bytes of an FP8 KV row (dsa_kv_fp8_quantize) */
+  DSA_HOT_MAX_SLOTS = 16384    /* largest hot buffer per sequence (dsa_hot_t) */
 };
 
 /*
@@ -131,7 +136,8 @@ DSA_API dsa_status_t dsa_status_fetch(void* d_ws, dsa_stream_t stream, int32_t* 
 
 /* Per-kernel launch counters kept by the host side of the library (for
  * tests and benchmarks): counts[0] indexer, [1] top-K, [2] sparse MLA,
- * [3] split combine, [4] FP8 quantiser, [5] other.  `n` is the length of
+ * [3] split combine, [4] FP8 quantisers, [5] indexer cache append, [6] hot
+ * buffer plan, [7] hot buffer swap-in, [8] other.  `n` is the length of
  * `counts`; returns how many counters exist. */
 DSA_API int dsa_launch_counts(uint64_t* counts, int n);
 DSA_API void dsa_launch_counts_reset(void);
@@ -282,7 +288,7 @@ DSA_API dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_ba
 DSA_API dsa_status_t dsa_fp8_quantize(const void* x, int64_t rows, uint8_t* codes, float* scale,
                               dsa_stream_t stream);
 
-/* ------------------------------------------------------------------ NEXT-2: FP8 KV latent */
+/* ------------------------------------------------------------------ FP8 KV latent */
 
 /*
  * FP8 KV cache rows ("GLM-5.2 / 总览" config table: per-token per-layer KV
@@ -308,7 +314,7 @@ DSA_API dsa_status_t dsa_sparse_mla_attn_fp8kv(const void* q_lat, const void* q_
                                        const dsa_batch_t* b, void* out, float* lse, void* ws,
                                        size_t ws_bytes, dsa_stream_t stream);
 
-/* ------------------------------------------------------------------ NEXT-3: cache append */
+/* ------------------------------------------------------------------ indexer cache append */
 
 /*
  * The step just before a1 for new tokens: interleaved RoPE of the indexer
@@ -346,6 +352,108 @@ DSA_API dsa_status_t dsa_indexer_prepare_queries(const void* q_new, const dsa_ba
                                          dsa_dtype_t dt, const double* inv_freq, void* q_out,
                                          float* q_scale, void* ws, size_t ws_bytes,
                                          dsa_stream_t stream);
+
+/* ------------------------------------------------------------------ hot / cold KV */
+
+/*
+ * A GPU "hot" buffer of KV rows in front of the full cache kept in host
+ * memory ("GLM-5.2 / 总览" glossary entry HiSparse: 6144 hot KV slots on the
+ * GPU, the full KV in CPU pinned memory, rows swapped in on demand after the
+ * DSA top-K; config table: a 1M-token context's KV held by a GPU hot buffer
+ * plus a CPU cold store).  One state per index span (an F layer and the S
+ * layers that read its index buffer: they select the same positions, so one
+ * plan serves every layer of the span).  All arrays are device int32,
+ * caller-owned:
+ *   slot_pos    [num_seqs, hot_slots]  position held by each slot, -1 empty
+ *   slot_stamp  [num_seqs, hot_slots]  last step that used the slot, -1 never
+ *   pos_slot    [num_seqs, max_pos]    slot holding each position, -1 none
+ *   fetch_pos, fetch_slot [num_seqs, hot_slots], fetch_count [num_seqs]:
+ *               the last plan's swap-in list, per sequence
+ * Initialise slot_pos, slot_stamp and pos_slot to -1 (every byte 0xFF).
+ * max_pos >= the batch's max_len; 1 <= hot_slots <= DSA_HOT_MAX_SLOTS;
+ * num_seqs * hot_slots < 2^31.  The hot KV of a layer is a device array of
+ * num_seqs * hot_slots rows (bf16 [.., 576] or FP8 [.., 656]); position s of
+ * sequence b, once resident in slot j, is hot row b * hot_slots + j.
+ */
+typedef struct {
+  int32_t hot_slots;
+  int32_t max_pos;
+  int32_t* slot_pos;
+  int32_t* slot_stamp;
+  int32_t* pos_slot;
+  int32_t* fetch_pos;
+  int32_t* fetch_slot;
+  int32_t* fetch_count;
+} dsa_hot_t;
+
+/*
+ * dsa_hot_plan: one step of the hot buffer for the index buffer idx
+ * (int32 [num_q, k], positions, -1 padding).  Per sequence, over the valid
+ * entries (0 <= s <= q_pos[t]) of its queries, query by query and slot by
+ * slot: a resident position is a hit and its slot's stamp becomes `step`;
+ * the other positions are misses, in order of first appearance; the misses
+ * take the least recently used slots among those not used at this step
+ * (smallest stamp, then lowest slot index), handed out in increasing slot
+ * index; each chosen slot drops its old position and records (position,
+ * slot) on the fetch list.  rows (int32 [num_q, k], device) receives the
+ * hot row of every valid entry and -1 elsewhere.  `step` >= 0 must exceed
+ * every step used before with this state.  A sequence with more misses than
+ * unused slots changes no slot, gets rows -1 and raises
+ * DSA_ERR_HOT_OVERFLOW; an entry outside [-1, q_pos] is skipped and raises
+ * DSA_ERR_DEVICE_INDEX (both in the workspace's status word).
+ *
+ * dsa_hot_fetch: the swap-in of the last plan's fetch lists for `layers`
+ * layers: hot_kv[l][b * hot_slots + slot] = cold_kv[l][row of (b, position)]
+ * with the batch's cache layout (seq_row0 or block table) addressing the cold
+ * caches of cold_rows rows.  cold_kv[l] is host memory the device can read
+ * (page-locked: cudaHostAlloc / cudaMallocHost, or cudaHostRegister'ed;
+ * device memory is accepted too); pageable memory returns
+ * DSA_ERR_INVALID_ARG.  The kernel reads it directly (NVLink-C2C on Grace),
+ * no staging copies.  Rows are 1152 bytes (kv_dtype DSA_BF16) or 656
+ * (DSA_FP8_E4M3); all pointers 16-byte aligned.
+ *
+ * dsa_sparse_mla_attn_rows: dsa_sparse_mla_attn (or _fp8kv, by kv_dtype)
+ * whose index entries are absolute rows of kv (e.g. the hot rows of
+ * dsa_hot_plan) instead of positions: entry r >= 0 reads kv row r, -1 is
+ * padding; rows outside [0, kv_rows) are skipped and raise
+ * DSA_ERR_DEVICE_INDEX.  The batch supplies the query rows and positions.
+ */
+DSA_API dsa_status_t dsa_hot_plan(const int32_t* idx, int32_t k, const dsa_batch_t* b,
+                                  const dsa_hot_t* h, int32_t step, int32_t* rows, void* ws,
+                                  size_t ws_bytes, dsa_stream_t stream);
+DSA_API dsa_status_t dsa_hot_fetch(const dsa_hot_t* h, const dsa_batch_t* b, int32_t layers,
+                                   const void* const* cold_kv, int64_t cold_rows,
+                                   void* const* hot_kv, dsa_dtype_t kv_dtype, void* ws,
+                                   size_t ws_bytes, dsa_stream_t stream);
+DSA_API dsa_status_t dsa_sparse_mla_attn_rows(const void* q_lat, const void* q_rope,
+                                              const void* kv, int64_t kv_rows,
+                                              dsa_dtype_t kv_dtype, const int32_t* rows,
+                                              int32_t k, int32_t heads, float scale,
+                                              const dsa_batch_t* b, void* out, float* lse,
+                                              void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * indexshare_group_forward_hot: indexshare_group_forward over hot buffers.
+ * g->kv[l] are the layers' HOT KV arrays (kv_rows = num_seqs * hot_slots of
+ * every span), hot->cold_kv[l] their full caches in host memory.  Each F
+ * layer scores and selects as usual into idx_buf, then plans its span
+ * (hot->spans[i] for the i-th F layer of layer_types, hot->n_spans of them),
+ * swaps in the span's missing rows for all of its layers at once and every
+ * layer of the span attends over its hot rows (hot->rows: device int32
+ * [num_q, k] scratch).  Errors as for the calls above.
+ */
+typedef struct {
+  const dsa_hot_t* spans;
+  int32_t n_spans;
+  const void* const* cold_kv;
+  int64_t cold_rows;
+  int32_t step;
+  int32_t* rows;
+} dsa_hot_group_t;
+
+DSA_API dsa_status_t indexshare_group_forward_hot(const dsa_group_t* g, const dsa_batch_t* b,
+                                                  const dsa_hot_group_t* hot, int32_t* idx_buf,
+                                                  void* ws, size_t ws_bytes, dsa_stream_t stream);
 
 /* ------------------------------------------------------------------ no workspace */
 

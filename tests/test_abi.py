@@ -127,3 +127,43 @@ def test_append_and_paged_argument_errors_without_a_device(dsa):
     assert L.dsa_topk(fake, ctypes.byref(ok), 16, fake, fake, 256, None) == dsa.DSA_OK
     nob = dsa._Batch(1, 0, 0, 256, fake, fake, None)
     assert L.dsa_topk(fake, ctypes.byref(nob), 16, fake, fake, 256, None) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_hot_argument_errors_without_a_device(dsa):
+    L = dsa.lib
+    fake = ctypes.c_void_p(4096)
+    b = _batch(dsa, max_len=256)
+    ws = ctypes.c_void_p(1 << 20)
+
+    def hot(slots=64, max_pos=256, arrays=True):
+        p = fake if arrays else None
+        return dsa._Hot(slots, max_pos, p, p, p, p, p, p)
+
+    ok = hot()
+    assert L.dsa_hot_plan(fake, 16, ctypes.byref(b), ctypes.byref(hot(slots=0)), 0, fake, ws, 256,
+                          None) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_hot_plan(fake, 16, ctypes.byref(b), ctypes.byref(hot(slots=dsa.HOT_MAX_SLOTS + 1)),
+                          0, fake, ws, 256, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert L.dsa_hot_plan(fake, 16, ctypes.byref(b), ctypes.byref(hot(max_pos=128)), 0, fake, ws,
+                          256, None) == dsa.DSA_ERR_INVALID_ARG
+    assert b"max_pos" in L.dsa_last_error_string()
+    assert L.dsa_hot_plan(fake, 16, ctypes.byref(b), ctypes.byref(hot(arrays=False)), 0, fake, ws,
+                          256, None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_hot_plan(fake, 16, ctypes.byref(b), ctypes.byref(ok), -1, fake, ws, 256,
+                          None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_hot_plan(fake, 16, ctypes.byref(b), None, 0, fake, ws, 256,
+                          None) == dsa.DSA_ERR_INVALID_ARG
+    # cold caches: host memory CUDA does not know (pageable) is refused
+    host = (ctypes.c_uint8 * 4096)()
+    addr = (ctypes.addressof(host) + 15) & ~15
+    cold = (ctypes.c_void_p * 1)(addr)
+    hotp = (ctypes.c_void_p * 1)(4096)
+    assert L.dsa_hot_fetch(ctypes.byref(ok), ctypes.byref(b), 1, ctypes.cast(cold, dsa._PP), 2,
+                           ctypes.cast(hotp, dsa._PP), dsa.DSA_BF16, ws, 256,
+                           None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_hot_fetch(ctypes.byref(ok), ctypes.byref(b), 1, ctypes.cast(cold, dsa._PP), 2,
+                           ctypes.cast(hotp, dsa._PP), 7, ws, 256, None) == dsa.DSA_ERR_UNSUPPORTED
+    # rows-mode attention: FP8 rows need 64 heads
+    assert L.dsa_sparse_mla_attn_rows(fake, fake, fake, 100, dsa.DSA_FP8_E4M3, fake, 64, 16, 0.0625,
+                                      ctypes.byref(b), fake, None, ws, 256,
+                                      None) == dsa.DSA_ERR_UNSUPPORTED
