@@ -52,7 +52,7 @@ DESCR = {
 NCU_TRAFFIC = {
     # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch, scaled by
     # tokens to the 8192-token launch (q/out traffic is per token; the kv cache is a few MB)
-    "sparse_mla": {"bytes": 1.0590e+09, "workload": "prefill8k", "src": "0fba8f882d686733"},
+    "sparse_mla": {"bytes": 1.0560e+09, "workload": "prefill8k", "src": "6e4acbd34e2e0697"},
 }
 
 
