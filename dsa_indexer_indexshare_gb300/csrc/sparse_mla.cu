@@ -91,6 +91,7 @@ struct MlaParams {
   const uint8_t* kv8;  // or FP8 rows [kv_rows, 656]: 512 E4M3, 4 fp32 group scales, 64 bf16
   int64_t kv_rows;
   int direct;  // index entries are absolute kv rows (no causal test), not positions
+  int l2_prefetch;  // prefetch the block after next into L2 (caches larger than L2)
   const int32_t* idx;
   int K;
   float scale_log2;
@@ -441,7 +442,34 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(B_CFULL + g))
                    : "memory");
     };
+    // ---- the rows of the block after next are prefetched into L2 (bulk, no
+    // completion) while this block runs, so that the refill gathers hit L2
+    // rather than HBM; the 8 threads of a row share it, thread kch == 0 issues
+    int psel[RPT];
+    auto fetch_pf = [&](int jj) {
+      if (kch == 0 && p.l2_prefetch)
+#pragma unroll
+        for (int c = 0; c < RPT; ++c) {
+          const int sl = jj * 128 + rb + GROW * c;
+          psel[c] = (jj < j1 && sl < nvalid) ? idx_row[sl] : -1;
+        }
+    };
+    auto prefetch_rows = [&]() {
+      if (kch == 0 && p.l2_prefetch)
+#pragma unroll
+        for (int c = 0; c < RPT; ++c) {
+          const int e = psel[c];
+          if (e < 0 || (!p.direct && e > pos)) continue;
+          const int64_t rr = row_of(e);
+          if (rr < 0 || rr >= p.kv_rows) continue;
+          if constexpr (KV8)
+            bulk_prefetch_l2(p.kv8 + rr * 656, 656);
+          else
+            bulk_prefetch_l2(p.kv + rr * 576, 1152);
+        }
+    };
     if (j0 < j1) {
+      fetch_pf(j0 + 1);
       fetch_sel(j0);
       resolve_rows();
       if constexpr (KV8) {
@@ -470,6 +498,8 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         e_next = (more && sn < nvalid) ? idx_row[sn] : -1;
       }
       if (more) fetch_sel(j + 1);  // consumed after P of this block
+      if (j == j0) prefetch_rows();  // block j0 + 1
+      if (j + 2 < j1) fetch_pf(j + 2);  // prefetched after this block's refill
       if (!mbar_wait(bar(B_S), u & 1, abort_flag, p.status, to)) break;
       tc_fence_after();
       bool valid = e >= 0 && (p.direct || e <= pos);  // the gather's test, on this thread's key
@@ -594,6 +624,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         }
         if (!alive) break;
         if constexpr (KV8) convert8(3, 0);
+        if (j + 2 < j1) prefetch_rows();
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -766,6 +797,9 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   p.kv8 = kv_fp8 ? static_cast<const uint8_t*>(kv) : nullptr;
   p.kv_rows = kv_rows;
   p.direct = direct_rows ? 1 : 0;
+  // A cache that L2 holds (short prefills) is read from L2 anyway; larger ones
+  // (decode, long prefixes) get the next rows prefetched from HBM.
+  p.l2_prefetch = kv_rows * (kv_fp8 ? 656 : 1152) > (int64_t(96) << 20) ? 1 : 0;
   p.idx = idx;
   p.K = k;
   p.scale_log2 = scale * kLog2e;
