@@ -619,9 +619,19 @@ def indexshare_group_forward_hot(group: Group, batch: Batch, hot: HotGroup, step
     span's hot buffer, swap in its missing rows for every layer of the span,
     and attend over hot rows.  Returns (outs, lses, idx_buf)."""
     dev = batch.device
+    nl = len(group.layer_types)
+    if len(hot.cold_kv) != nl:
+        raise ValueError(f"{len(hot.cold_kv)} cold caches for {nl} layers")
+    if len(hot.spans) != group.layer_types.count("F"):
+        raise ValueError("one HotState per F layer")
+    for l in range(nl):
+        hk, ck = group.layers[l]["kv"], hot.cold_kv[l]
+        if hk.dtype != ck.dtype or hk.shape[1] != ck.shape[1]:
+            raise ValueError(f"layer {l}: hot and cold rows differ in dtype or width")
     if idx_buf is None:
         idx_buf = torch.empty((batch.num_q, group.k), dtype=torch.int32, device=dev)
     _need(idx_buf, "idx_buf", torch.int32, dev, (batch.num_q, group.k))
+    _need(hot.rows, "hot.rows", torch.int32, dev, (batch.num_q, group.k))
     if ws is None:
         ws = workspace(group.workspace_size(batch), dev)
     hot._c.step = int(step)
