@@ -11,7 +11,12 @@ the oracle from host copies of the same inputs:
   output, legitimately; such rows are validated through their index set);
 * sparse MLA alone: the oracle's own index rows are fed to the GPU kernel for
   the sampled rows, and the outputs must agree within the same bound;
-* FP8 variant: the library quantiser's codes must equal the oracle's.
+* FP8 variant: the library quantiser's codes must equal the oracle's;
+* FP8 KV latent: the library's 656-byte rows must equal the oracle's
+  quantisation of the same bf16 rows, and the oracle reads their
+  dequantised values;
+* hot/cold KV (decode shape, 6144 hot slots): the hot group call equals the
+  device-resident group call bit for bit over steps that miss and hit.
 """
 import numpy as np
 import pytest
@@ -50,8 +55,14 @@ def _host_inputs(lay, layers, rows, fp8):
 
     host = []
     for L in layers:
+        if L["kv"].dtype == torch.uint8:  # FP8 KV rows: the library's codes are the oracle's
+            codes = cache(L["kv"]).cpu().numpy()
+            assert np.array_equal(codes, oracle.kv_fp8_quantize(bits(cache(L["kv_bf16"]))))
+            kv_host = oracle.kv_fp8_dequantize(codes)
+        else:
+            kv_host = bits(cache(L["kv"]))
         d = {"q_lat": bits(L["q_lat"].index_select(0, rt)),
-             "q_rope": bits(L["q_rope"].index_select(0, rt)), "kv": bits(cache(L["kv"]))}
+             "q_rope": bits(L["q_rope"].index_select(0, rt)), "kv": kv_host}
         if "q_idx" in L:
             d["w"] = L["w"].index_select(0, rt).cpu().numpy()
             if fp8:
@@ -73,7 +84,7 @@ def _host_inputs(lay, layers, rows, fp8):
     return host, pos, key0
 
 
-def _run(name, sample):
+def _run(name, sample, kv_fp8=False):
     cfg = dict(synth.WORKLOADS[name])
     lay = synth.workload_layout(name)
     types, H, K = cfg["layers"], cfg["H"], cfg["K"]
@@ -86,6 +97,10 @@ def _run(name, sample):
                 qc, qs = dsa.dsa_fp8_quantize(L["q_idx"])
                 kc, ks = dsa.dsa_fp8_quantize(L["k_idx"])
                 L.update(q_idx=qc, q_scale=qs, k_idx=kc, k_scale=ks)
+    if kv_fp8:
+        for L in layers:
+            L["kv_bf16"] = L["kv"]
+            L["kv"] = dsa.dsa_kv_fp8_quantize(L["kv"])
     batch = dsa.Batch(lay.q_start, lay.q_pos, lay.seq_row0, lay.max_len, device=DEV)
     rows = np.array(sorted(set(r for r in sample if 0 <= r < lay.num_q)), np.int64)
     host, pos, key0 = _host_inputs(lay, layers, rows, fp8)
@@ -143,3 +158,47 @@ def test_chunked_full_size():
 
 def test_decode1m_fp8_full_size():
     _run("decode1m", [2])
+
+
+def test_decode64_fp8_kv_full_size():
+    _run("decode64", [0, 33, 63], kv_fp8=True)
+
+
+def test_decode8_hot_cold_equals_resident():
+    cfg = dict(synth.WORKLOADS["decode8"])
+    lay = synth.workload_layout("decode8")
+    types, H, K = cfg["layers"], cfg["H"], cfg["K"]
+    layers = synth.device_layers(lay, types, H, device=DEV, seed=0)
+    batch = dsa.Batch(lay.q_start, lay.q_pos, lay.seq_row0, lay.max_len, device=DEV)
+    slots = 6144
+    # a second indexer query set, so that one step selects other positions
+    g2 = torch.Generator(device=DEV)
+    g2.manual_seed(77)
+    layers2 = [dict(L) for L in layers]
+    layers2[0]["q_idx"] = (torch.randn(layers[0]["q_idx"].shape, generator=g2, device=DEV)
+                           / np.sqrt(128)).to(torch.bfloat16)
+    res = [dsa.Group(types, ls, k=K, scale=SCALE) for ls in (layers, layers2)]
+    cold = []
+    for L in layers:
+        h = torch.empty(L["kv"].shape, dtype=L["kv"].dtype, pin_memory=True)
+        h.copy_(L["kv"])
+        cold.append(h)
+    hot_kv = [torch.zeros((lay.num_seqs * slots, 576), dtype=torch.bfloat16, device=DEV) for _ in layers]
+    hot = [dsa.Group(types, [dict(L, kv=hk) for L, hk in zip(ls, hot_kv)], k=K, scale=SCALE)
+           for ls in (layers, layers2)]
+    spans = [dsa.HotState(lay.num_seqs, slots, lay.max_len, DEV)]
+    hg = dsa.HotGroup(spans, cold, num_q=lay.num_q, k=K, device=DEV)
+    ws = dsa.workspace(res[0].workspace_size(batch), DEV)
+    for step, which in enumerate((0, 1, 0, 0)):
+        outs_r, _, idx_r = dsa.indexshare_group_forward(res[which], batch, ws=ws)
+        outs_r = [o.clone() for o in outs_r]
+        idx_r = idx_r.clone()
+        outs_h, _, idx_h = dsa.indexshare_group_forward_hot(hot[which], batch, hg, step, ws=ws)
+        dsa.status_fetch(ws)
+        assert torch.equal(idx_h, idx_r)
+        for a, b in zip(outs_h, outs_r):
+            assert torch.equal(a, b)
+        fetched = int(spans[0].fetch_count.sum())
+        # steps 0 and 1 select new positions; steps 2 and 3 repeat step 0's
+        # selection, still resident (2 x 2048 rows fit in 6144 slots): all hit
+        assert (fetched > 0) == (step < 2)
