@@ -287,16 +287,27 @@ __global__ void __launch_bounds__(kFetchBS) hot_fetch_kernel(const HotArgs h, co
       continue;
     }
     const int64_t dst = static_cast<int64_t>(seq) * H + s;
-    for (int l = 0; l < L.n; ++l) {
-      const uint4* from = reinterpret_cast<const uint4*>(L.cold[l] + src * ROWB);
-      uint4* to = reinterpret_cast<uint4*>(L.hot[l] + dst * ROWB);
-      uint4 v[PER];
+    // the rows of up to four layers are all in flight before any is stored
+    // (a host read is a long round trip; stores could alias the loads, so the
+    // compiler would not hoist them on its own)
+    for (int l0 = 0; l0 < L.n; l0 += 4) {
+      uint4 v[4][PER];
 #pragma unroll
-      for (int j = 0; j < PER; ++j)
-        if (lane + 32 * j < NCH) v[j] = from[lane + 32 * j];
+      for (int q = 0; q < 4; ++q) {
+        if (l0 + q >= L.n) break;
+        const uint4* from = reinterpret_cast<const uint4*>(L.cold[l0 + q] + src * ROWB);
 #pragma unroll
-      for (int j = 0; j < PER; ++j)
-        if (lane + 32 * j < NCH) to[lane + 32 * j] = v[j];
+        for (int j = 0; j < PER; ++j)
+          if (lane + 32 * j < NCH) v[q][j] = from[lane + 32 * j];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (l0 + q >= L.n) break;
+        uint4* to = reinterpret_cast<uint4*>(L.hot[l0 + q] + dst * ROWB);
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+          if (lane + 32 * j < NCH) to[lane + 32 * j] = v[q][j];
+      }
     }
   }
 }
@@ -334,9 +345,9 @@ cudaError_t launch_hot_fetch(const dsa_hot_t& h, const dsa_batch_t& b, int layer
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // about four CTAs per SM over the whole batch, at most one warp per slot
+  // about eight CTAs per SM over the whole batch, at most one warp per slot
   const int per_seq_max = (h.hot_slots + kFetchBS / 32 - 1) / (kFetchBS / 32);
-  int gx = (4 * sms + b.num_seqs - 1) / b.num_seqs;
+  int gx = (8 * sms + b.num_seqs - 1) / b.num_seqs;
   gx = gx < 1 ? 1 : (gx > per_seq_max ? per_seq_max : gx);
   for (int l0 = 0; l0 < layers; l0 += kFetchLayers) {
     FetchLayers L{};
