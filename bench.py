@@ -52,7 +52,7 @@ DESCR = {
 NCU_TRAFFIC = {
     # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch, scaled by
     # tokens to the 8192-token launch (q/out traffic is per token; the kv cache is a few MB)
-    "sparse_mla": {"bytes": 1.0560e+09, "workload": "prefill8k", "src": "6e4acbd34e2e0697"},
+    "sparse_mla": {"bytes": 1.0550e+09, "workload": "prefill8k", "src": "034d3a0a6d0faecf"},
 }
 
 
