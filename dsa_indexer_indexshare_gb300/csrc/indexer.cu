@@ -16,6 +16,8 @@
 // decode), then one TMA producer warp and one MMA issuer warp (TMEM owner).  The key tiles
 // stream through a STAGES-deep shared-memory ring; the accumulator is double
 // buffered in TMEM so the epilogue of tile i overlaps the MMAs of tile i+1.
+#include <cstdint>
+
 #include "common.cuh"
 
 namespace dsa {
@@ -237,16 +239,21 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
     const int quarter = warp & 3;
     const int n0 = (warp >> 2) * C::TOK_PER_WARP;
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    // FP8: this thread's key scale, loaded one tile ahead so that its memory
+    // latency overlaps the previous tile instead of following the MMA
+    auto load_kscale = [&](int i) -> float {
+      if (!FP8 || i >= nkb) return 1.f;
+      const int64_t kr = cache_row(p.b, seq, row0, s_begin + i * 128 + quarter * 32 + lane);
+      return (kr >= 0 && kr < p.k_rows) ? __ldg(&p.k_scale[kr]) : 0.f;
+    };
+    float kscale_next = load_kscale(0);
     for (int i = 0; i < nkb; ++i) {
       const int acc = i & 1;
       if (!mbar_wait(bar(B_ACCF + acc), (i >> 1) & 1, abort_flag, p.status, to)) break;
       tc_fence_after();
       const int s = s_begin + i * 128 + quarter * 32 + lane;
-      float kscale = 1.f;
-      if (FP8) {
-        const int64_t kr = cache_row(p.b, seq, row0, s);
-        kscale = (kr >= 0 && kr < p.k_rows) ? p.k_scale[kr] : 0.f;
-      }
+      const float kscale = kscale_next;
+      kscale_next = load_kscale(i + 1);
 #pragma unroll
       for (int nn = 0; nn < C::TOK_PER_WARP; ++nn) {
         const int n = n0 + nn;
@@ -292,12 +299,36 @@ cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, Indexer
   using C = IdxCfg<NTOK, FP8, STAGES>;
   auto* kern = indexer_kernel<NTOK, FP8, STAGES>;
   static int configured_device = -1;  // attribute is per device
+  static int slots = 0;               // resident CTAs on the whole GPU
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT, C::SMEM);
+    if (e != cudaSuccess) return e;
+    slots = sms * (per_sm > 0 ? per_sm : 1);
     configured_device = dev;
+  }
+  if (NTOK == 1) {
+    // decode: tiles per CTA chosen so that the CTAs fill whole waves of the
+    // resident slots, weighing each CTA's start (barriers, TMEM, Q, first
+    // tile) as about four tiles of streaming: min over kc of
+    // ceil(CTAs(kc) / slots) * (kc + 4)
+    const int64_t tiles = (p.b.max_len + 127) / 128;
+    int best = 32;
+    int64_t best_cost = INT64_MAX;
+    for (int kc = 16; kc <= 128; ++kc) {
+      const int64_t ctas = static_cast<int64_t>(p.b.num_seqs) * ((tiles + kc - 1) / kc);
+      const int64_t cost = ((ctas + slots - 1) / slots) * (kc + 4);
+      if (cost < best_cost || (cost == best_cost && kc == 32)) {
+        best_cost = cost;
+        best = kc;
+      }
+    }
+    p.kc_blocks = best;
   }
   p.num_qb = (p.b.max_q + NTOK - 1) / NTOK;
   p.num_kc = (p.b.max_len + p.kc_blocks * 128 - 1) / (p.kc_blocks * 128);
@@ -336,7 +367,7 @@ cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float*
   p.k_rows = k_rows;
   p.scores = scores;
   p.status = status;
-  p.kc_blocks = decode ? 32 : 64;  // 128-key tiles per CTA (one Q load per 8K keys)
+  p.kc_blocks = 64;  // 128-key tiles per CTA (one Q load per 8K keys); decode: see launch_one
   p.fill_tail = fill_tail ? 1 : 0;
   p.timeout_ns = wait_timeout_ns();
   if (decode)
