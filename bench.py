@@ -688,7 +688,7 @@ def main():
 
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
     if not args.no_cpu and rank == 0 and world == 1:
-        nrows = args.cpu_rows or {"tiny": 512, "prefill8k": 48, "decode64": 4, "chunked": 24,
+        nrows = args.cpu_rows or {"tiny": 512, "prefill8k": 480, "decode64": 4, "chunked": 24,
                                   "decode1m": 1, "prefill2k": 48, "decode8": 4,
                                   "chunked1k": 24}[args.workload]
         rows, host = oracle_sample(args.workload, lay, layers, cfg, fp8, nrows, phys=phys)
