@@ -109,6 +109,7 @@ def _load():
                               c_size_t, c_void_p]),
         "dsa_hot_fetch": (st, [POINTER(_Hot), B, c_int32, _PP, c_int64, _PP, c_int, c_void_p,
                                c_size_t, c_void_p]),
+        "dsa_hot_touch": (st, [c_int32, _PP, c_int64, c_int64, c_void_p]),
         "dsa_sparse_mla_attn_rows": (st, [c_void_p, c_void_p, c_void_p, c_int64, c_int, c_void_p,
                                           c_int32, c_int32, c_float, B, c_void_p, c_void_p,
                                           c_void_p, c_size_t, c_void_p]),
@@ -566,6 +567,22 @@ def dsa_hot_fetch(state: HotState, batch: Batch, cold_kv, hot_kv, *, ws=None, st
                              ctypes.cast(hot, _PP), DSA_FP8_E4M3 if fp8 else DSA_BF16, _ptr(ws),
                              ws.numel(), _stream(stream, dev)), "dsa_hot_fetch")
     return hot_kv
+
+
+def dsa_hot_touch(cold_kv, *, stride: int = 65536, stream=None, device="cuda"):
+    """Read every host page of the cold caches once from the device (one
+    read per `stride` bytes), so that later swap-ins find their translations."""
+    n = len(cold_kv)
+    for l, t in enumerate(cold_kv):
+        _cold(t, f"cold_kv[{l}]")
+    if n == 0:
+        return
+    nbytes = cold_kv[0].numel() * cold_kv[0].element_size()
+    if any(t.numel() * t.element_size() != nbytes for t in cold_kv):
+        raise ValueError("cold caches must have the same size")
+    cold = (c_void_p * n)(*[t.data_ptr() for t in cold_kv])
+    _check(lib.dsa_hot_touch(n, ctypes.cast(cold, _PP), nbytes, int(stride),
+                             _stream(stream, torch.device(device))), "dsa_hot_touch")
 
 
 def dsa_sparse_mla_attn_rows(q_lat, q_rope, kv, rows, batch: Batch, *, scale: float, out=None,

@@ -503,6 +503,30 @@ dsa_status_t dsa_hot_fetch(const dsa_hot_t* h, const dsa_batch_t* b, int32_t lay
                         stream);
 }
 
+}  // extern "C"
+
+namespace dsa {
+// hot.cu: one device read per `stride` bytes of each cold cache
+cudaError_t launch_hot_touch(int layers, const void* const* cold, int64_t bytes, int64_t stride,
+                             cudaStream_t stream);
+}  // namespace dsa
+
+extern "C" {
+
+dsa_status_t dsa_hot_touch(int32_t layers, const void* const* cold_kv, int64_t cold_bytes,
+                           int64_t stride, dsa_stream_t stream) {
+  if (layers < 0 || layers > 4096) return fail(DSA_ERR_INVALID_ARG, "layers=%d", layers);
+  if (layers == 0) return DSA_OK;
+  if (!cold_kv) return fail(DSA_ERR_INVALID_ARG, "cold_kv is required");
+  if (cold_bytes < 1) return fail(DSA_ERR_INVALID_ARG, "cold_bytes < 1");
+  if (stride < 16 || stride % 16 != 0) return fail(DSA_ERR_INVALID_ARG, "stride must be a multiple of 16");
+  std::vector<const void*> cold(static_cast<size_t>(layers));
+  for (int l = 0; l < layers; ++l)
+    if (dsa_status_t s = device_view(cold_kv[l], "cold_kv", l, &cold[l])) return s;
+  return launch_status(launch_hot_touch(layers, cold.data(), cold_bytes, stride, stream),
+                       "hot touch launch");
+}
+
 dsa_status_t dsa_sparse_mla_attn_rows(const void* q_lat, const void* q_rope, const void* kv,
                                       int64_t kv_rows, dsa_dtype_t kv_dtype, const int32_t* rows,
                                       int32_t k, int32_t heads, float scale, const dsa_batch_t* b,

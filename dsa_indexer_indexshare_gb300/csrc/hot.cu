@@ -312,6 +312,23 @@ __global__ void __launch_bounds__(kFetchBS) hot_fetch_kernel(const HotArgs h, co
   }
 }
 
+// One read every `stride` bytes of each cold cache, so that the device-side
+// translations of its host pages exist before the first swap-in (a first
+// access to a host page costs far more than a later one).  The loads are
+// volatile, so they are issued although nothing uses their values.
+__global__ void __launch_bounds__(256) hot_touch_kernel(const FetchLayers L, int64_t bytes,
+                                                        int64_t stride) {
+  const int64_t per = (bytes + stride - 1) / stride;
+  const int64_t total = per * L.n;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int l = static_cast<int>(i / per);
+    const int64_t off = (i % per) * stride;
+    uint32_t v;
+    asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(L.cold[l] + off) : "memory");
+  }
+}
+
 HotArgs to_hot(const dsa_hot_t& h) {
   return HotArgs{h.hot_slots, h.max_pos, h.slot_pos, h.slot_stamp, h.pos_slot,
                  h.fetch_pos, h.fetch_slot, h.fetch_count};
@@ -366,6 +383,23 @@ cudaError_t launch_hot_fetch(const dsa_hot_t& h, const dsa_batch_t& b, int layer
                                                                         cold_rows, status);
     prof_end(kLaunchFetch, stream);
     count_launch(kLaunchFetch);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_hot_touch(int layers, const void* const* cold, int64_t bytes, int64_t stride,
+                             cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  for (int l0 = 0; l0 < layers; l0 += kFetchLayers) {
+    FetchLayers L{};
+    L.n = layers - l0 < kFetchLayers ? layers - l0 : kFetchLayers;
+    for (int i = 0; i < L.n; ++i) L.cold[i] = static_cast<const uint8_t*>(cold[l0 + i]);
+    hot_touch_kernel<<<static_cast<unsigned>(8 * sms), 256, 0, stream>>>(L, bytes, stride);
+    count_launch(kLaunchOther);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -425,6 +425,17 @@ DSA_API dsa_status_t dsa_hot_fetch(const dsa_hot_t* h, const dsa_batch_t* b, int
                                    const void* const* cold_kv, int64_t cold_rows,
                                    void* const* hot_kv, dsa_dtype_t kv_dtype, void* ws,
                                    size_t ws_bytes, dsa_stream_t stream);
+/*
+ * dsa_hot_touch: one read every `stride` bytes (a multiple of 16; the host
+ * page size, e.g. 65536 on Grace) of each of `layers` cold caches of
+ * cold_bytes bytes, so that the device's translations of their host pages
+ * exist before the first swap-in: measured on GB300, a swap-in whose rows
+ * lie on host pages the GPU has never read runs 6-30x slower than one over
+ * pages it has read before.  Call once after a cold cache is allocated (or
+ * grown); it changes no memory.  cold_kv as for dsa_hot_fetch.
+ */
+DSA_API dsa_status_t dsa_hot_touch(int32_t layers, const void* const* cold_kv, int64_t cold_bytes,
+                                   int64_t stride, dsa_stream_t stream);
 DSA_API dsa_status_t dsa_sparse_mla_attn_rows(const void* q_lat, const void* q_rope,
                                               const void* kv, int64_t kv_rows,
                                               dsa_dtype_t kv_dtype, const int32_t* rows,

@@ -167,3 +167,16 @@ def test_hot_argument_errors_without_a_device(dsa):
     assert L.dsa_sparse_mla_attn_rows(fake, fake, fake, 100, dsa.DSA_FP8_E4M3, fake, 64, 16, 0.0625,
                                       ctypes.byref(b), fake, None, ws, 256,
                                       None) == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_hot_touch_argument_errors_without_a_device(dsa):
+    L = dsa.lib
+    host = (ctypes.c_uint8 * 4096)()
+    cold = (ctypes.c_void_p * 1)((ctypes.addressof(host) + 15) & ~15)
+    pp = ctypes.cast(cold, dsa._PP)
+    assert L.dsa_hot_touch(1, pp, 1024, 24, None) == dsa.DSA_ERR_INVALID_ARG  # stride % 16
+    assert L.dsa_hot_touch(1, pp, 0, 4096, None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_hot_touch(1, None, 1024, 4096, None) == dsa.DSA_ERR_INVALID_ARG
+    assert L.dsa_hot_touch(0, None, 1024, 4096, None) == dsa.DSA_OK
+    # pageable host memory is refused
+    assert L.dsa_hot_touch(1, pp, 1024, 4096, None) == dsa.DSA_ERR_INVALID_ARG

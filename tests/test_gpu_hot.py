@@ -141,6 +141,7 @@ def test_fetch_and_attention_over_hot_rows(layout, kv_fp8):
     else:
         batch = make_batch(dsa, lay, DEV)
     cold = _cold_layers(kvs, table, R, lay)
+    dsa.dsa_hot_touch(cold, stride=4096, device=DEV)  # reads only: the caches stay as they were
     row_w = dsa.KV_ROW_FP8 if kv_fp8 else dsa.KV_ROW
     dt = torch.uint8 if kv_fp8 else torch.bfloat16
     hot_kv = [torch.zeros((lay.num_seqs * hot, row_w), dtype=dt, device=DEV) for _ in kvs]
