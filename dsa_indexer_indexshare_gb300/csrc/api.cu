@@ -518,7 +518,8 @@ dsa_status_t dsa_hot_touch(int32_t layers, const void* const* cold_kv, int64_t c
   if (layers < 0 || layers > 4096) return fail(DSA_ERR_INVALID_ARG, "layers=%d", layers);
   if (layers == 0) return DSA_OK;
   if (!cold_kv) return fail(DSA_ERR_INVALID_ARG, "cold_kv is required");
-  if (cold_bytes < 1) return fail(DSA_ERR_INVALID_ARG, "cold_bytes < 1");
+  if (cold_bytes < 16 || cold_bytes % 16 != 0)
+    return fail(DSA_ERR_INVALID_ARG, "cold_bytes must be a positive multiple of 16");
   if (stride < 16 || stride % 16 != 0) return fail(DSA_ERR_INVALID_ARG, "stride must be a multiple of 16");
   std::vector<const void*> cold(static_cast<size_t>(layers));
   for (int l = 0; l < layers; ++l)

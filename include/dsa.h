@@ -428,7 +428,7 @@ DSA_API dsa_status_t dsa_hot_fetch(const dsa_hot_t* h, const dsa_batch_t* b, int
 /*
  * dsa_hot_touch: one read every `stride` bytes (a multiple of 16; the host
  * page size, e.g. 65536 on Grace) of each of `layers` cold caches of
- * cold_bytes bytes, so that the device's translations of their host pages
+ * cold_bytes bytes (a multiple of 16), so that the device's translations of their host pages
  * exist before the first swap-in: measured on GB300, a swap-in whose rows
  * lie on host pages the GPU has never read runs 6-30x slower than one over
  * pages it has read before.  Call once after a cold cache is allocated (or
