@@ -695,7 +695,8 @@ def main():
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
-        line["e2e"] = e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, world)
+        line["e2e"] = e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, world,
+                              phys=phys)
 
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
     if not args.no_cpu and rank == 0 and world == 1:
@@ -715,45 +716,66 @@ def main():
         dist.destroy_process_group()
 
 
-def e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, world):
+def e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, world, phys=None):
     """Same metric through indexshare_group_forward, with every step's inputs
     copied from pinned host memory and the outputs copied back inside the
-    timed region.  Two sets of device buffers let step i+1's uploads and step
-    i-1's read-back (on their own streams) overlap step i's group call."""
+    timed region.  A step's inputs are its per-query tensors and the cache
+    rows of its own tokens (position q_pos[t] of each query: every row for a
+    prefill, one row per sequence for a decode step); the rest of each cache
+    is state that stays on the device.  Three sets of device buffers, with
+    uploads, the group call and the read-back on three streams, let step
+    i+1's uploads and step i-1's read-back overlap step i's group call."""
     import torch
-    keys = ("q_lat", "q_rope", "kv", "q_idx", "w", "k_idx", "q_scale", "k_scale")
-    host = []  # pinned host copies of every layer input, shared by both buffer sets
-    for L in layers:
-        host.append({k_: torch.empty(L[k_].shape, dtype=L[k_].dtype, pin_memory=True).copy_(L[k_])
-                     for k_ in keys if k_ in L})
+    cache_keys = ("kv", "k_idx", "k_scale")
+    query_keys = ("q_lat", "q_rope", "q_idx", "w", "q_scale")
+    seq_of = np.repeat(np.arange(lay.num_seqs), np.diff(lay.q_start))
+    rows_new = (lay.seq_row0[seq_of].astype(np.int64) + lay.q_pos.astype(np.int64))
+    rows_dev = torch.from_numpy(rows_new).to(dev)
+    if phys is not None:  # paged caches: the physical rows of those positions
+        rows_dev = phys.index_select(0, rows_dev)
+    NSLOT = 3
     slots = []
-    for sl in range(2):
+    for sl in range(NSLOT):
         if sl == 0:
             dl, g, wsl, idx = layers, group, ws, idx_buf
         else:
-            dl = [{k_: torch.empty_like(v) if k_ in keys else v for k_, v in L.items()} for L in layers]
+            dl = [{k_: torch.empty_like(v) if k_ in query_keys else v for k_, v in L.items()}
+                  for L in layers]
             g = dsa.Group(group.layer_types, dl, k=group.k, scale=1 / 16)
             wsl = dsa.workspace(g.workspace_size(batch), dev)
             idx = torch.empty_like(idx_buf)
-        pairs = [(host[l][k_], dl[l][k_]) for l in range(len(layers)) for k_ in host[l]]
+        ups = []  # (pinned host, device destination, rows to scatter or None)
+        for L in dl:
+            for k_, v in L.items():
+                if k_ in query_keys:
+                    ups.append((torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v), v, None))
+                elif k_ in cache_keys:
+                    new_rows = v.index_select(0, rows_dev)
+                    ups.append((torch.empty(new_rows.shape, dtype=v.dtype, pin_memory=True).copy_(new_rows),
+                                v, torch.empty_like(new_rows)))
         outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in g.outs]
-        slots.append({"pairs": pairs, "g": g, "ws": wsl, "idx": idx, "outs_h": outs_h,
+        slots.append({"ups": ups, "g": g, "ws": wsl, "idx": idx, "outs_h": outs_h,
                       "up": torch.cuda.Event(), "done": torch.cuda.Event(), "down": torch.cuda.Event()})
-    h2d = sum(h.numel() * h.element_size() for h, _ in slots[0]["pairs"])
+    h2d = sum(h.numel() * h.element_size() for h, _, _ in slots[0]["ups"])
     d2h = sum(o.numel() * o.element_size() for o in slots[0]["outs_h"])
-    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_up, s_comp, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
 
     def step(i):
-        sl = slots[i % 2]
-        if i >= 2:  # the slot's previous step has been computed and read back
+        sl = slots[i % NSLOT]
+        if i >= NSLOT:  # the slot's previous step has been computed and read back
             s_up.wait_event(sl["down"])
         with torch.cuda.stream(s_up):
-            for h, d in sl["pairs"]:
-                d.copy_(h, non_blocking=True)
+            for h, d, stage in sl["ups"]:
+                if stage is None:
+                    d.copy_(h, non_blocking=True)
+                else:  # the new tokens' cache rows, then scattered to their rows
+                    stage.copy_(h, non_blocking=True)
+                    d.index_copy_(0, rows_dev, stage)
             sl["up"].record(s_up)
-        stream.wait_event(sl["up"])
-        dsa.indexshare_group_forward(sl["g"], batch, sl["idx"], ws=sl["ws"], stream=stream)
-        sl["done"].record(stream)
+        s_comp.wait_event(sl["up"])
+        dsa.indexshare_group_forward(sl["g"], batch, sl["idx"], ws=sl["ws"], stream=s_comp)
+        sl["done"].record(s_comp)
         s_down.wait_event(sl["done"])
         with torch.cuda.stream(s_down):
             for o_h, o_d in zip(sl["outs_h"], sl["g"].outs):
@@ -761,17 +783,17 @@ def e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, worl
             sl["down"].record(s_down)
 
     steps = max(4, args.steps // 2)
-    for i in range(2):
+    for i in range(NSLOT):
         step(i)
     torch.cuda.synchronize(dev)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(s_up)
-    for i in range(2, 2 + steps):
+    for i in range(NSLOT, NSLOT + steps):
         step(i)
-    for sl in slots:  # the end waits for the last read-back on every stream
-        stream.wait_event(sl["down"])
-    b.record(stream)
+    for sl in slots:  # the end waits for the last read-back of every slot
+        s_comp.wait_event(sl["down"])
+    b.record(s_comp)
     torch.cuda.synchronize(dev)
     for sl in slots:
         dsa.status_fetch(sl["ws"])
@@ -779,7 +801,8 @@ def e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, worl
     return {"value": round(replica_throughput(lay.num_q, steps, world, ms), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms / steps, 3),
-            "pipelining": "two buffer sets; uploads, group call and read-back on three streams"}
+            "inputs": "per-query tensors + the cache rows of the step's tokens",
+            "pipelining": "three buffer sets; uploads, group call and read-back on three streams"}
 
 
 def reference_arm(args):
