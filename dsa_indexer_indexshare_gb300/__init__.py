@@ -68,7 +68,7 @@ class _HotGroup(ctypes.Structure):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it first (dsa_indexer_indexshare_gb300._build.build())")
+        raise ImportError(f"{LIB_PATH} is missing: build it first (python dsa_indexer_indexshare_gb300/_build.py)")
     L = ctypes.CDLL(LIB_PATH)
     B = POINTER(_Batch)
     st = c_int
