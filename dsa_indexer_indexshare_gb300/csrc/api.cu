@@ -164,6 +164,39 @@ dsa_status_t check_group(const dsa_group_t* g, const dsa_batch_t* b, const int32
   return DSA_OK;
 }
 
+// The parts of a group workspace: status block, fp32 score matrix, top-K scratch.
+struct GroupWs {
+  int* status;
+  float* scores;
+  uint8_t* topk_scratch;
+  size_t topk_bytes;
+  uint8_t* mla_extra;  // after the status block (the MLA's own scratch)
+  size_t mla_extra_bytes;
+};
+
+GroupWs group_ws(const dsa_group_t* g, const dsa_batch_t* b, void* ws, size_t need) {
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const size_t score_bytes = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4);
+  return GroupWs{static_cast<int*>(ws), reinterpret_cast<float*>(wsb + kStatusBytes),
+                 wsb + kStatusBytes + score_bytes, round256(topk_scratch_bytes(*b, g->k)),
+                 wsb + kStatusBytes, need - kStatusBytes};
+}
+
+// F layer l of a group: candidate scoring, then top-K into the shared index buffer.
+dsa_status_t run_f_layer(const dsa_group_t* g, const dsa_batch_t* b, int l, int32_t* idx_buf,
+                         const GroupWs& w, cudaStream_t stream) {
+  const bool fp8 = g->idx_dtype == DSA_FP8_E4M3;
+  if (dsa_status_t s = launch_status(
+          launch_indexer(g->q_idx[l], fp8 ? g->q_scale[l] : nullptr, g->w[l], g->k_idx[l],
+                         fp8 ? g->k_scale[l] : nullptr, g->k_rows, fp8, *b, w.scores, false, w.status,
+                         stream),
+          "indexer launch"))
+    return s;
+  return launch_status(launch_topk(w.scores, *b, g->k, idx_buf, w.status, w.topk_scratch, w.topk_bytes,
+                                   stream),
+                       "top-K launch");
+}
+
 // A pointer the device can dereference: device, managed or page-locked host
 // memory (its device address returned); pageable host memory is refused.
 dsa_status_t device_view(const void* p, const char* what, int l, const void** dev) {
@@ -422,33 +455,16 @@ dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b
   const int nl = static_cast<int>(strlen(g->layer_types));
   const size_t need = dsa_group_workspace_size(g, b);
   if (dsa_status_t s = check_ws(ws, ws_bytes, need)) return s;
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  int* status = static_cast<int*>(ws);
-  float* scores = reinterpret_cast<float*>(wsb + kStatusBytes);
-  const size_t score_bytes = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4);
-  uint8_t* topk_scratch = wsb + kStatusBytes + score_bytes;
-  const size_t topk_bytes = round256(topk_scratch_bytes(*b, g->k));
-  const bool fp8 = g->idx_dtype == DSA_FP8_E4M3;
+  const GroupWs w = group_ws(g, b, ws, need);
   const bool kv_fp8 = g->kv_dtype == DSA_FP8_E4M3;
   for (int l = 0; l < nl; ++l) {
-    if (g->layer_types[l] == 'F') {
-      // F layer: candidate scoring, then top-K into the shared index buffer
-      if (dsa_status_t s = launch_status(
-              launch_indexer(g->q_idx[l], fp8 ? g->q_scale[l] : nullptr, g->w[l], g->k_idx[l],
-                             fp8 ? g->k_scale[l] : nullptr, g->k_rows, fp8, *b, scores, false,
-                             status, stream),
-              "indexer launch"))
-        return s;
-      if (dsa_status_t s = launch_status(launch_topk(scores, *b, g->k, idx_buf, status,
-                                                     topk_scratch, topk_bytes, stream),
-                                         "top-K launch"))
-        return s;
-    }
+    if (g->layer_types[l] == 'F')
+      if (dsa_status_t s = run_f_layer(g, b, l, idx_buf, w, stream)) return s;
     // every layer: gather from its own cache + sparse attention over idx_buf
     if (dsa_status_t s = launch_status(
             launch_sparse_mla(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, idx_buf, g->k,
                               g->heads, g->scale, *b, g->out[l], g->lse ? g->lse[l] : nullptr,
-                              wsb + kStatusBytes, need - kStatusBytes, status, stream, kv_fp8),
+                              w.mla_extra, w.mla_extra_bytes, w.status, stream, kv_fp8),
             "sparse MLA launch"))
       return s;
   }
@@ -571,46 +587,30 @@ dsa_status_t indexshare_group_forward_hot(const dsa_group_t* g, const dsa_batch_
     return fail(DSA_ERR_UNSUPPORTED, "num_q * k >= 2^31");
   const size_t need = dsa_group_workspace_size(g, b);
   if (dsa_status_t s = check_ws(ws, ws_bytes, need)) return s;
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  int* status = static_cast<int*>(ws);
-  float* scores = reinterpret_cast<float*>(wsb + kStatusBytes);
-  const size_t score_bytes = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4);
-  uint8_t* topk_scratch = wsb + kStatusBytes + score_bytes;
-  const size_t topk_bytes = round256(topk_scratch_bytes(*b, g->k));
-  const bool fp8 = g->idx_dtype == DSA_FP8_E4M3;
+  const GroupWs w = group_ws(g, b, ws, need);
   const bool kv_fp8 = g->kv_dtype == DSA_FP8_E4M3;
   int span = -1;
   for (int l = 0; l < nl; ++l) {
     if (g->layer_types[l] == 'F') {
       ++span;
-      if (dsa_status_t s = launch_status(
-              launch_indexer(g->q_idx[l], fp8 ? g->q_scale[l] : nullptr, g->w[l], g->k_idx[l],
-                             fp8 ? g->k_scale[l] : nullptr, g->k_rows, fp8, *b, scores, false,
-                             status, stream),
-              "indexer launch"))
-        return s;
-      if (dsa_status_t s = launch_status(launch_topk(scores, *b, g->k, idx_buf, status,
-                                                     topk_scratch, topk_bytes, stream),
-                                         "top-K launch"))
-        return s;
+      if (dsa_status_t s = run_f_layer(g, b, l, idx_buf, w, stream)) return s;
       // one plan for the span, then the span's missing rows for all of its layers
       const dsa_hot_t& h = hot->spans[span];
       if (dsa_status_t s = launch_status(
-              launch_hot_plan(idx_buf, g->k, *b, h, hot->step, hot->rows, status, stream),
+              launch_hot_plan(idx_buf, g->k, *b, h, hot->step, hot->rows, w.status, stream),
               "hot plan launch"))
         return s;
       int l1 = l + 1;
       while (l1 < nl && g->layer_types[l1] == 'S') ++l1;
       if (dsa_status_t s = hot_fetch_impl(&h, b, l1 - l, hot->cold_kv + l, hot->cold_rows,
-                                          const_cast<void* const*>(g->kv + l), g->kv_dtype, status,
+                                          const_cast<void* const*>(g->kv + l), g->kv_dtype, w.status,
                                           stream))
         return s;
     }
     if (dsa_status_t s = launch_status(
             launch_sparse_mla(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, hot->rows, g->k,
                               g->heads, g->scale, *b, g->out[l], g->lse ? g->lse[l] : nullptr,
-                              wsb + kStatusBytes, need - kStatusBytes, status, stream, kv_fp8,
-                              true),
+                              w.mla_extra, w.mla_extra_bytes, w.status, stream, kv_fp8, true),
             "sparse MLA launch"))
       return s;
   }

@@ -29,6 +29,27 @@ def test_header_declares_the_hot_path_calls():
         assert name in fns
 
 
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++11")])
+def test_header_is_plain_c(lang, std, tmp_path):
+    """The boundary header compiles on its own, as C99 and as C++, with no
+    CUDA or torch headers (a C caller needs nothing else), and a C program
+    can take the address of every declared entry point."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    r = subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-x", lang, HEADER], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    src = tmp_path / ("use.c" if lang == "c" else "use.cc")
+    body = "\n".join(f"  (void)&{f};" for f in declared_functions())
+    src.write_text(f'#include "{HEADER}"\nint main(void) {{\n{body}\n  return 0;\n}}\n')
+    r = subprocess.run([cc, f"-std={std}", "-Wall", "-Werror", "-fsyntax-only", str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_declared_symbol(dsa):
     lib = ctypes.CDLL(dsa.LIB_PATH)
     missing = [f for f in declared_functions() if not hasattr(lib, f)]
