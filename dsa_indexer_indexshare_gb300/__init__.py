@@ -107,8 +107,8 @@ def _load():
                                              c_void_p, c_size_t, c_void_p]),
         "dsa_hot_plan": (st, [c_void_p, c_int32, B, POINTER(_Hot), c_int32, c_void_p, c_void_p,
                               c_size_t, c_void_p]),
-        "dsa_hot_fetch": (st, [POINTER(_Hot), B, c_int32, _PP, c_int64, _PP, c_int, c_void_p,
-                               c_size_t, c_void_p]),
+        "dsa_hot_fetch": (st, [POINTER(_Hot), B, c_int32, _PP, c_int64, _PP, c_int64, c_int,
+                               c_void_p, c_size_t, c_void_p]),
         "dsa_hot_touch": (st, [c_int32, _PP, c_int64, c_int64, c_void_p]),
         "dsa_sparse_mla_attn_rows": (st, [c_void_p, c_void_p, c_void_p, c_int64, c_int, c_void_p,
                                           c_int32, c_int32, c_float, B, c_void_p, c_void_p,
@@ -564,8 +564,9 @@ def dsa_hot_fetch(state: HotState, batch: Batch, cold_kv, hot_kv, *, ws=None, st
     cold = (c_void_p * n)(*[t.data_ptr() for t in cold_kv])
     hot = (c_void_p * n)(*[t.data_ptr() for t in hot_kv])
     _check(lib.dsa_hot_fetch(state.c, batch.c, n, ctypes.cast(cold, _PP), cold_kv[0].shape[0],
-                             ctypes.cast(hot, _PP), DSA_FP8_E4M3 if fp8 else DSA_BF16, _ptr(ws),
-                             ws.numel(), _stream(stream, dev)), "dsa_hot_fetch")
+                             ctypes.cast(hot, _PP), hot_kv[0].shape[0],
+                             DSA_FP8_E4M3 if fp8 else DSA_BF16, _ptr(ws), ws.numel(),
+                             _stream(stream, dev)), "dsa_hot_fetch")
     return hot_kv
 
 

@@ -511,9 +511,13 @@ dsa_status_t hot_fetch_impl(const dsa_hot_t* h, const dsa_batch_t* b, int32_t la
 
 dsa_status_t dsa_hot_fetch(const dsa_hot_t* h, const dsa_batch_t* b, int32_t layers,
                            const void* const* cold_kv, int64_t cold_rows, void* const* hot_kv,
-                           dsa_dtype_t kv_dtype, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+                           int64_t hot_rows, dsa_dtype_t kv_dtype, void* ws, size_t ws_bytes,
+                           dsa_stream_t stream) {
   if (dsa_status_t s = check_batch(b)) return s;
   if (dsa_status_t s = check_hot(h, b)) return s;
+  if (hot_rows < static_cast<int64_t>(b->num_seqs) * h->hot_slots)
+    return fail(DSA_ERR_INVALID_ARG, "hot_rows=%lld < num_seqs * hot_slots",
+                static_cast<long long>(hot_rows));
   if (dsa_status_t s = check_ws(ws, ws_bytes, kStatusBytes)) return s;
   return hot_fetch_impl(h, b, layers, cold_kv, cold_rows, hot_kv, kv_dtype, static_cast<int*>(ws),
                         stream);

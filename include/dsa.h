@@ -405,7 +405,8 @@ typedef struct {
  * dsa_hot_fetch: the swap-in of the last plan's fetch lists for `layers`
  * layers: hot_kv[l][b * hot_slots + slot] = cold_kv[l][row of (b, position)]
  * with the batch's cache layout (seq_row0 or block table) addressing the cold
- * caches of cold_rows rows.  cold_kv[l] is host memory the device can read
+ * caches of cold_rows rows; each hot_kv[l] has hot_rows rows, at least
+ * num_seqs * hot_slots (DSA_ERR_INVALID_ARG otherwise).  cold_kv[l] is host memory the device can read
  * (page-locked: cudaHostAlloc / cudaMallocHost, or cudaHostRegister'ed;
  * device memory is accepted too); pageable memory returns
  * DSA_ERR_INVALID_ARG.  The kernel reads it directly (NVLink-C2C on Grace),
@@ -423,8 +424,8 @@ DSA_API dsa_status_t dsa_hot_plan(const int32_t* idx, int32_t k, const dsa_batch
                                   size_t ws_bytes, dsa_stream_t stream);
 DSA_API dsa_status_t dsa_hot_fetch(const dsa_hot_t* h, const dsa_batch_t* b, int32_t layers,
                                    const void* const* cold_kv, int64_t cold_rows,
-                                   void* const* hot_kv, dsa_dtype_t kv_dtype, void* ws,
-                                   size_t ws_bytes, dsa_stream_t stream);
+                                   void* const* hot_kv, int64_t hot_rows, dsa_dtype_t kv_dtype,
+                                   void* ws, size_t ws_bytes, dsa_stream_t stream);
 /*
  * dsa_hot_touch: one read every `stride` bytes (a multiple of 16; the host
  * page size, e.g. 65536 on Grace) of each of `layers` cold caches of

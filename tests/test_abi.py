@@ -180,10 +180,15 @@ def test_hot_argument_errors_without_a_device(dsa):
     cold = (ctypes.c_void_p * 1)(addr)
     hotp = (ctypes.c_void_p * 1)(4096)
     assert L.dsa_hot_fetch(ctypes.byref(ok), ctypes.byref(b), 1, ctypes.cast(cold, dsa._PP), 2,
-                           ctypes.cast(hotp, dsa._PP), dsa.DSA_BF16, ws, 256,
+                           ctypes.cast(hotp, dsa._PP), 64, dsa.DSA_BF16, ws, 256,
                            None) == dsa.DSA_ERR_INVALID_ARG
     assert L.dsa_hot_fetch(ctypes.byref(ok), ctypes.byref(b), 1, ctypes.cast(cold, dsa._PP), 2,
-                           ctypes.cast(hotp, dsa._PP), 7, ws, 256, None) == dsa.DSA_ERR_UNSUPPORTED
+                           ctypes.cast(hotp, dsa._PP), 64, 7, ws, 256, None) == dsa.DSA_ERR_UNSUPPORTED
+    # hot arrays smaller than num_seqs * hot_slots rows
+    assert L.dsa_hot_fetch(ctypes.byref(ok), ctypes.byref(b), 1, ctypes.cast(cold, dsa._PP), 2,
+                           ctypes.cast(hotp, dsa._PP), 63, dsa.DSA_BF16, ws, 256,
+                           None) == dsa.DSA_ERR_INVALID_ARG
+    assert b"hot_rows" in L.dsa_last_error_string()
     # rows-mode attention: FP8 rows need 64 heads
     assert L.dsa_sparse_mla_attn_rows(fake, fake, fake, 100, dsa.DSA_FP8_E4M3, fake, 64, 16, 0.0625,
                                       ctypes.byref(b), fake, None, ws, 256,
