@@ -1,0 +1,80 @@
+"""The benchmark's algorithmic work per launch (the roofline numerators) and
+its throughput arithmetic, checked on the CPU against counts made here by
+walking the queries and their visible positions one by one."""
+import numpy as np
+import pytest
+
+import bench
+import synth
+
+
+def _walk(lay, H, K, kv_row, fp8):
+    """Per-launch work by explicit enumeration: every (query, visible
+    position) pair scored, every selected key attended, every cache row of a
+    sequence read at most once per launch."""
+    idx_pairs = mla_keys = 0
+    rows_read = 0
+    for b in range(lay.num_seqs):
+        sel_b = 0
+        for t in range(int(lay.q_start[b]), int(lay.q_start[b + 1])):
+            vis = int(lay.q_pos[t]) + 1
+            idx_pairs += vis
+            sel = min(vis, K)
+            mla_keys += sel
+            sel_b += sel
+        rows_read += min(sel_b, int(lay.q_pos[lay.q_start[b + 1] - 1]) + 1)
+    key_bytes = 128 * (1 if fp8 else 2) + (4 if fp8 else 0)
+    seq_len = sum(int(lay.q_pos[lay.q_start[b + 1] - 1]) + 1 for b in range(lay.num_seqs))
+    return {
+        "indexer_flops": 2.0 * 32 * 128 * idx_pairs,
+        "indexer_bytes": seq_len * key_bytes + lay.num_q * 32 * (128 * (1 if fp8 else 2) + 4)
+        + idx_pairs * 4,
+        "topk_bytes": idx_pairs * 4 + lay.num_q * K * 4,
+        "mla_flops": 2.0 * H * (576 + 512) * mla_keys,
+        "mla_bytes": rows_read * kv_row + lay.num_q * H * (576 + 512) * 2,
+    }
+
+
+@pytest.mark.parametrize("case", ["prefill", "decode", "chunked"])
+@pytest.mark.parametrize("kv_row", [1152, 656])
+def test_algorithmic_work_matches_an_explicit_count(case, kv_row):
+    if case == "prefill":
+        lay, H, K = synth.make_layout([512], [512]), 16, 64
+    elif case == "decode":
+        lay, H, K = synth.make_layout([5000, 300, 2048], [1, 1, 1]), 64, 2048
+    else:
+        lay, H, K = synth.make_layout([3000, 700], [200, 50]), 64, 256
+    for fp8 in (False, True):
+        w = bench.algorithmic(lay, {"H": H, "K": K}, fp8, kv_row)
+        ref = _walk(lay, H, K, kv_row, fp8)
+        assert w["indexer"]["flops"] == ref["indexer_flops"]
+        assert w["indexer"]["bytes"] == ref["indexer_bytes"]
+        assert w["topk"]["bytes"] == ref["topk_bytes"]
+        assert w["sparse_mla"]["flops"] == ref["mla_flops"]
+        assert w["sparse_mla"]["bytes"] == ref["mla_bytes"]
+
+
+def test_decode_reads_each_selected_row_once():
+    # one query per sequence: a decode launch reads min(len, K) rows per sequence
+    lay = synth.make_layout([100000, 1000], [1, 1])
+    w = bench.algorithmic(lay, {"H": 64, "K": 2048}, False)
+    assert w["sparse_mla"]["bytes"] == (2048 + 1000) * 1152 + 2 * 64 * 1088 * 2
+
+
+def test_bounds_and_throughput():
+    peaks = {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0}
+    prefill = bench.algorithmic(synth.make_layout([8192], [8192]), {"H": 64, "K": 2048}, False)
+    decode = bench.algorithmic(synth.make_layout([131072] * 4, [1] * 4), {"H": 64, "K": 2048}, False)
+    assert bench.kernel_bound("sparse_mla", prefill["sparse_mla"], peaks, False)[0] == "tensor"
+    assert bench.kernel_bound("indexer", decode["indexer"], peaks, False)[0] == "hbm"
+    assert bench.kernel_bound("sparse_mla", decode["sparse_mla"], peaks, False)[0] == "hbm"
+    assert bench.kernel_bound("topk", prefill["topk"], peaks, False)[0] == "hbm"
+    # whole-job rate: every replica processes the workload; time = the slowest rank
+    assert bench.replica_throughput(8192, 20, 4, 250.0) == pytest.approx(4 * 8192 * 20 / 0.25)
+    assert bench.slowest_rank_ms(12.5, 1) == 12.5
+
+
+def test_every_workload_is_described():
+    assert set(bench.DESCR) == set(synth.WORKLOADS)
+    for name, text in bench.DESCR.items():
+        assert text and "KV latent" not in text  # the KV dtype is its own config key
