@@ -164,6 +164,51 @@ def host_layers(layout: Layout, layer_types: str, H: int, *, ints: bool, seed: i
     return layers
 
 
+def planted_host_layers(layout: Layout, layer_types: str, H: int, *, m: int, seed: int = 0,
+                        latent_gain: float = 4.0):
+    """Gaussian layers as host_layers, plus a planted set of m relevant
+    positions per sequence (drawn among the positions every query of the
+    sequence sees): their indexer keys lie along a direction u_b that every
+    indexer head of the sequence's queries also points along (with positive
+    head weights), and their latent rows along a direction v_b shared by the
+    queries' latent parts, scaled so that those positions lead both the
+    indexer ranking and the attention (latent_gain sets the attention's margin:
+    a planted key's score exceeds a random one's by about latent_gain^2 / 16
+    in the softmax exponent).  Returns (layers,
+    planted positions per sequence).  The premise of sparse attention made
+    explicit, for tolerance checks of quantised indexers."""
+    layers = host_layers(layout, layer_types, H, ints=False, seed=seed)
+    g = HostGen(seed + 7919)
+    planted = []
+    for b in range(layout.num_seqs):
+        qs, qe = int(layout.q_start[b]), int(layout.q_start[b + 1])
+        if qe == qs:
+            planted.append(np.zeros(0, np.int64))
+            continue
+        first = int(layout.q_pos[qs:qe].min()) + 1       # positions every query sees
+        r = g.rng(10 * b)
+        pos = np.sort(r.choice(first, size=min(m, first), replace=False)).astype(np.int64)
+        planted.append(pos)
+        rows = int(layout.seq_row0[b]) + pos
+        u = r.standard_normal(DI)
+        u /= np.linalg.norm(u)
+        v = r.standard_normal(DL)
+        v /= np.linalg.norm(v)
+        for l, t in enumerate(layer_types):
+            L = layers[l]
+            lat = bf16_bits_to_f32(L["kv"][rows, :DL])
+            L["kv"][rows, :DL] = f32_to_bf16_bits((lat + latent_gain * v).astype(np.float32))
+            ql = bf16_bits_to_f32(L["q_lat"][qs:qe])
+            L["q_lat"][qs:qe] = f32_to_bf16_bits((ql + latent_gain * v).astype(np.float32))
+            if t == "F":
+                k = bf16_bits_to_f32(L["k_idx"][rows])
+                L["k_idx"][rows] = f32_to_bf16_bits((k + u).astype(np.float32))
+                q = bf16_bits_to_f32(L["q_idx"][qs:qe])
+                L["q_idx"][qs:qe] = f32_to_bf16_bits((q + u).astype(np.float32))
+                L["w"][qs:qe] = np.abs(L["w"][qs:qe])
+    return layers, planted
+
+
 # ---------------------------------------------------------------- device (torch)
 def device_layers(layout: Layout, layer_types: str, H: int, *, device, seed: int = 0,
                   ints: bool = False):
