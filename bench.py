@@ -422,6 +422,19 @@ class HotMode:
                 "h2d_copy_gbs": self.c2c_gbs}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 # ---------------------------------------------------------------- CPU oracle
 def oracle_sample(workload, lay, layers, cfg, fp8, nrows, seed=1, phys=None):
     """Host copies of a sampled set of query rows (and the caches they read,
@@ -707,7 +720,7 @@ def main():
         import oracle
         secs = run_oracle(lay, host, rows, cfg, fp8)
         line["cpu_baseline"] = {"value": round(len(rows) / secs, 3), "unit": UNIT,
-                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "cores": oracle.num_threads(), "cpu": cpu_model(), "kind": "oracle",
                                 "sample": f"{len(rows)} query rows of the same workload (full group, "
                                           f"all layers), {secs:.1f} s"}
     if rank == 0:
@@ -830,6 +843,7 @@ def reference_arm(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": DESCR[args.workload], "layers": cfg["layers"]},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(),
+                         "cpu": cpu_model(),
                          "kind": "oracle",
                          "sample": f"{len(rows)} query rows per step of the same workload"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
