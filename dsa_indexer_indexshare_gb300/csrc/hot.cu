@@ -324,8 +324,7 @@ __global__ void __launch_bounds__(256) hot_touch_kernel(const FetchLayers L, int
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int l = static_cast<int>(i / per);
     const int64_t off = (i % per) * stride;
-    uint32_t v;
-    asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(L.cold[l] + off) : "memory");
+    asm volatile("{\n\t.reg .u32 t;\n\tld.volatile.global.u32 t, [%0];\n\t}" ::"l"(L.cold[l] + off) : "memory");
   }
 }
 

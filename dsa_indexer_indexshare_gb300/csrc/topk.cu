@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kLongBS) topk_select_kernel(const float* __res
   __shared__ uint32_t h[kHBins];
   __shared__ int warp_sums[32];
   __shared__ int s_b1, s_above;
-  const int t = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+  const int t = blockIdx.y, tid = threadIdx.x;
   const int pos = query_pos(b, t, nullptr);
   if (pos + 1 <= K) return;
   int lo, hi;
