@@ -15,17 +15,24 @@
  *  - "GLM-5 -> 5.1 -> 5.2" section 10: indexer once per layer group, shared
  *    indices written to a buffer reused within the group, each layer gathers
  *    the selected entries from its own K/V cache, then sparse attention.
+ *  - Beyond the layer group itself: paged caches (CH 4.4, PagedAttention over
+ *    the compressed MLA KV), FP8 KV latent rows (config table and glossary
+ *    "KV8 / KV FP8"), the indexer cache append with interleaved RoPE (CH 7.1)
+ *    and a hot/cold KV with a GPU hot buffer in front of a host store
+ *    (glossary "HiSparse").
  *
  * Conventions for every entry point:
  *  - Pointers named d_* and every tensor argument are DEVICE pointers owned by
  *    the caller; the library allocates and frees nothing.  Host structs
- *    (dsa_batch_t, dsa_group_t) are read during the call only.
+ *    (dsa_batch_t, dsa_group_t, dsa_hot_t, dsa_hot_group_t) are read during
+ *    the call only; a hot/cold cold store is page-locked HOST memory.
  *  - Calls are asynchronous on `stream`: they validate their host-side
  *    arguments, enqueue kernels and return.  Argument errors are reported
  *    synchronously before anything is enqueued.  Errors only a kernel can see
  *    (an index outside [-1, q_pos], inconsistent batch arrays, a bounded wait
- *    that ran out) are OR-ed into the status word at the head of the
- *    workspace; dsa_status_fetch() reads and clears it.
+ *    that ran out, a hot buffer without room for a step's misses) are OR-ed
+ *    into the status word at the head of the workspace; dsa_status_fetch()
+ *    reads and clears it.
  *  - Nothing falls back: an unsupported shape or dtype returns
  *    DSA_ERR_UNSUPPORTED.  No exception crosses the ABI.
  *  - bf16 tensors are IEEE bfloat16 bit patterns; fp8 tensors are OCP E4M3
@@ -130,8 +137,9 @@ DSA_API dsa_status_t dsa_workspace_init(void* d_ws, size_t ws_bytes, dsa_stream_
 
 /* Synchronise `stream`, return the device status accumulated in `d_ws` as a
  * dsa_status_t (DSA_OK if clean; otherwise the most severe recorded error,
- * DSA_ERR_TIMEOUT before DSA_ERR_DEVICE_INDEX) and clear it.  *raw_bits, if
- * non-null, receives the raw error bits. */
+ * DSA_ERR_TIMEOUT before DSA_ERR_DEVICE_INDEX before DSA_ERR_HOT_OVERFLOW)
+ * and clear it.  *raw_bits, if non-null, receives the raw error bits (1
+ * timeout, 2 index, 4 batch arrays, 8 hot-buffer overflow). */
 DSA_API dsa_status_t dsa_status_fetch(void* d_ws, dsa_stream_t stream, int32_t* raw_bits);
 
 /* Per-kernel launch counters kept by the host side of the library (for
