@@ -206,3 +206,52 @@ def test_hot_touch_argument_errors_without_a_device(dsa):
     assert L.dsa_hot_touch(0, None, 1024, 4096, None) == dsa.DSA_OK
     # pageable host memory is refused
     assert L.dsa_hot_touch(1, pp, 1024, 4096, None) == dsa.DSA_ERR_INVALID_ARG
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "dsa.h"
+
+int main(void) {
+  dsa_batch_t b;
+  memset(&b, 0, sizeof b);
+  b.num_seqs = 1; b.num_q = 4; b.max_q = 4; b.max_len = 200;  /* not a multiple of 128 */
+  b.q_start = (const int32_t*)256; b.q_pos = (const int32_t*)256; b.seq_row0 = (const int64_t*)256;
+  void* p = (void*)4096;
+  if (dsa_topk((const float*)p, &b, 16, (int32_t*)p, p, 256, NULL) != DSA_ERR_INVALID_ARG) return 1;
+  if (strstr(dsa_last_error_string(), "multiple of 128") == NULL) return 2;
+  b.max_len = 256;
+  if (dsa_topk((const float*)p, &b, 0, (int32_t*)p, p, 256, NULL) != DSA_ERR_UNSUPPORTED) return 3;
+  if (dsa_sparse_mla_attn(p, p, p, 100, (const int32_t*)p, 64, 32, 0.0625f, &b, p, NULL, p, 256,
+                          NULL) != DSA_ERR_UNSUPPORTED) return 4;
+  if (dsa_status_bytes() != 256) return 5;
+  dsa_hot_t h;
+  memset(&h, 0, sizeof h);
+  if (dsa_hot_plan((const int32_t*)p, 16, &b, &h, 0, (int32_t*)p, p, 256, NULL) != DSA_ERR_UNSUPPORTED)
+    return 6;
+  printf("ok\n");
+  return 0;
+}
+"""
+
+
+def test_a_c_program_links_and_gets_argument_errors(dsa, tmp_path):
+    """A C caller compiled against include/dsa.h and linked to libdsa.so
+    gets the documented status codes from host-side argument checks (no
+    kernel is launched)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(dsa.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src),
+                        "-o", str(exe), "-L", libdir, "-ldsa", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
