@@ -50,8 +50,11 @@ def _compare(st_gpu, st_ref):
         assert np.array_equal(g[key], st_ref[key]), key
 
 
-@pytest.mark.parametrize("hot_slots,K", [(400, 128), (6144, 2048)])
-def test_hot_plan_matches_oracle_over_steps(hot_slots, K):
+@pytest.mark.parametrize("hot_slots,K,step0", [(400, 128, 0), (6144, 2048, 0),
+                                               (400, 128, (1 << 24) - 3)])
+def test_hot_plan_matches_oracle_over_steps(hot_slots, K, step0):
+    """step0 > 0 starts the step numbers just below 2^24, so the stamps cross
+    a digit of the kernel's radix select over them."""
     rng = np.random.default_rng(hot_slots)
     if K == 2048:  # decode-shaped: 16 sequences of ~100K positions, one query each
         lens = rng.integers(98304, 131073, 16)
@@ -63,7 +66,8 @@ def test_hot_plan_matches_oracle_over_steps(hot_slots, K):
     ref = oracle.hot_state(lay.num_seqs, hot_slots, lay.max_len)
     pool = [np.zeros(0, np.int64) for _ in range(lay.num_seqs)]
     ws = dsa.workspace(256, DEV)
-    for step in range(4 if K == 2048 else 8):
+    for i in range(4 if K == 2048 else 8):
+        step = step0 + i
         idx = _trace_idx(rng, lay, K, pool)
         rows = dsa.dsa_hot_plan(torch.from_numpy(idx).to(DEV), batch, st, step, ws=ws)
         assert dsa.status_fetch(ws) == 0
