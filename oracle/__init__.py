@@ -55,8 +55,14 @@ def lib():
             L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
             L.oracle_e4m3_encode.restype = ctypes.c_uint8
             L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            L.oracle_e4m3_encode_f64.restype = ctypes.c_uint8
+            L.oracle_e4m3_encode_f64.argtypes = [dbl]
+            L.oracle_e4m3_encode_array.argtypes = [vp, i64, vp]
+            L.oracle_e4m3_decode_array.argtypes = [vp, i64, vp]
+            L.oracle_fp8_block_scale.restype = ctypes.c_float
+            L.oracle_fp8_block_scale.argtypes = [dbl]
             L.oracle_hadamard128_f64.argtypes = [vp, vp]
-            L.oracle_fwht128_f32.argtypes = [vp]
+            L.oracle_fp8_rotate_rows.argtypes = [vp, i64, vp]
             L.oracle_fp8_quantize_rows.argtypes = [vp, i64, vp, vp]
             L.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
             L.oracle_f64_to_bf16.restype = ctypes.c_uint16
@@ -86,15 +92,28 @@ def num_threads() -> int:
 
 # ---------------------------------------------------------------- FP8 / Hadamard
 def e4m3_decode(codes) -> np.ndarray:
-    codes = np.asarray(codes, dtype=np.uint8)
-    f = lib().oracle_e4m3_decode
-    return np.array([f(int(c)) for c in codes.ravel()], dtype=np.float64).reshape(codes.shape)
+    """E4M3 codes -> their exact values (fp64; NaN for 0x7F / 0xFF)."""
+    c, pc = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    lib().oracle_e4m3_decode_array(pc, c.size, out.ctypes.data_as(ctypes.c_void_p))
+    return out
 
 
 def e4m3_encode(x) -> np.ndarray:
-    x = np.asarray(x, dtype=np.float32)
-    f = lib().oracle_e4m3_encode
-    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint8).reshape(x.shape)
+    """Values -> the nearest E4M3 codes (ties to even, saturating at +-448).
+    fp32 inputs are taken as fp32 values; anything else as fp64 values."""
+    x = np.asarray(x)
+    if x.dtype != np.float32:
+        x = x.astype(np.float64)
+    v, pv = _c(x.astype(np.float64), np.float64)   # fp32 -> fp64 is exact
+    out = np.empty(v.shape, np.uint8)
+    lib().oracle_e4m3_encode_array(pv, v.size, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def fp8_block_scale(amax: float) -> np.float32:
+    """amax / 448 as the nearest fp32 (1 for amax == 0): a block's FP8 scale."""
+    return np.float32(lib().oracle_fp8_block_scale(float(amax)))
 
 
 def hadamard128_f64(v) -> np.ndarray:
@@ -105,15 +124,18 @@ def hadamard128_f64(v) -> np.ndarray:
     return out
 
 
-def fwht128_f32(v) -> np.ndarray:
-    v = np.array(v, dtype=np.float32, copy=True)
-    assert v.shape == (128,)
-    lib().oracle_fwht128_f32(v.ctypes.data_as(ctypes.c_void_p))
-    return v
+def fp8_rotate_rows(x_bf16_bits) -> np.ndarray:
+    """H_128 x / sqrt(128) (fp64) of rows of 128 bf16 values: [rows, 128]."""
+    x, px = _c(x_bf16_bits, np.uint16)
+    rows = x.size // 128
+    y = np.empty((rows, 128), np.float64)
+    lib().oracle_fp8_rotate_rows(px, rows, y.ctypes.data_as(ctypes.c_void_p))
+    return y
 
 
 def fp8_quantize_rows(x_bf16_bits):
-    """Hadamard-rotate and FP8-quantise rows of 128 bf16 values.
+    """Hadamard-rotate and FP8-quantise rows of 128 bf16 values, from the
+    definition (fp64 rotation, fp32 scale nearest to amax/448, nearest E4M3).
     Returns (codes uint8 [rows,128], scale float32 [rows])."""
     x, px = _c(x_bf16_bits, np.uint16)
     rows = x.size // 128

@@ -8,10 +8,14 @@
  * sources.
  *
  * Arithmetic is fp64 on the exact values of the inputs (bf16 -> double,
- * E4M3 code * fp32 scale -> double).  The one exception is the FP8 quantiser,
- * which produces the quantised inputs both sides consume and therefore takes
- * its rounding decisions in fp32, the precision of the kernel that performs
- * the same step (see oracle_fp8_quantize_rows).
+ * E4M3 code * fp32 scale -> double).  The FP8 quantisers follow their
+ * definition in fp64 as well: rotate (indexer) by the normalised Hadamard
+ * matrix, scale = the fp32 number nearest to amax / 448 (the scale is stored
+ * as fp32), code = the E4M3 value nearest to x / scale.  The one rounding
+ * this restatement adds is fp64's own (2^-53 relative), far below the fp32
+ * error of any single-precision quantiser, so GPU codes are compared with
+ * these by a rule that allows a code step only within the GPU arithmetic's
+ * error bound of an E4M3 rounding boundary.
  *
  * Sources (GLM-5.2 pages):
  *  - "GLM-5.2 / 总览", config table (@tbl-glm52-config): 64 heads, QK head dim
@@ -62,16 +66,20 @@ double oracle_e4m3_decode(uint8_t c) {
   return s ? -v : v;
 }
 
-/* Round-to-nearest-even encode with saturation to +-448 (finite inputs). */
-uint8_t oracle_e4m3_encode(float xf) {
-  double x = (double)xf;
+/* Round-to-nearest-even encode with saturation to +-448, from a double: the
+ * value is scaled by a power of two (exact) so that the E4M3 grid of its
+ * binade becomes the integers, rounded with nearbyint (default rounding
+ * mode: nearest, ties to even) and decoded back into a code.  No E4M3
+ * infinity exists, so every magnitude from 448 up (and +-inf) saturates to
+ * the largest finite code; NaN maps to 0x7F. */
+uint8_t oracle_e4m3_encode_f64(double x) {
   uint8_t sign = (signbit(x) ? 0x80 : 0x00);
   double a = fabs(x);
   if (isnan(x)) return 0x7F;
   if (a >= 448.0) return (uint8_t)(sign | 0x7E);
   if (a < ldexp(1.0, -6)) {
     /* subnormal grid: multiples of 2^-9; q == 8 is the smallest normal */
-    double q = nearbyint(a / ldexp(1.0, -9)); /* default mode: ties to even */
+    double q = nearbyint(a / ldexp(1.0, -9)); /* exact scaling; ties to even */
     return (uint8_t)(sign | (uint8_t)q);
   }
   int e;
@@ -89,6 +97,48 @@ uint8_t oracle_e4m3_encode(float xf) {
   return (uint8_t)(sign | code);
 }
 
+/* The same for an fp32 input (its value is exact in a double). */
+uint8_t oracle_e4m3_encode(float xf) { return oracle_e4m3_encode_f64((double)xf); }
+
+/* Element-wise forms for arrays (test bookkeeping). */
+void oracle_e4m3_encode_array(const double* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode_f64(x[i]);
+}
+void oracle_e4m3_decode_array(const uint8_t* c, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
+}
+
+/* The fp32 number nearest to a / 448 for a finite a >= 0 (ties to the even
+ * significand): the fp32 rounding of the fp64 quotient is a candidate, and
+ * it and its two fp32 neighbours are compared by their exact distance to
+ * a / 448, i.e. |a - 448 c| (448 c is exact in a double, and so is the
+ * difference of two doubles this close). */
+static float f32_nearest_quotient_448(double a) {
+  const float r = (float)(a / 448.0);
+  float best = r;
+  double bd = fabs(a - 448.0 * (double)r);
+  const float cand[2] = {nextafterf(r, -INFINITY), nextafterf(r, INFINITY)};
+  for (int i = 0; i < 2; ++i) {
+    const float c = cand[i];
+    if (!(c >= 0.0f) || isinf(c)) continue;
+    const double d = fabs(a - 448.0 * (double)c);
+    uint32_t ub, uc;
+    memcpy(&ub, &best, 4);
+    memcpy(&uc, &c, 4);
+    if (d < bd || (d == bd && (uc & 1u) == 0 && (ub & 1u) == 1)) {
+      best = c;
+      bd = d;
+    }
+  }
+  return best;
+}
+
+/* Per-block FP8 scale of a block whose largest magnitude is amax: amax / 448
+ * stored as fp32, 1 for an all-zero block. */
+float oracle_fp8_block_scale(double amax) {
+  return amax > 0.0 ? f32_nearest_quotient_448(amax) : 1.0f;
+}
+
 /* ------------------------------------------------------------ Hadamard */
 
 /* Exact definition, fp64: out = H_128 * in / sqrt(128) where H is built by
@@ -102,46 +152,37 @@ void oracle_hadamard128_f64(const double* in, double* out) {
   }
 }
 
-/* Fast Walsh-Hadamard transform in fp32, unnormalised, in Sylvester order:
- * stage h = 1, 2, ..., 64 replaces (v[j], v[j+h]) by (v[j]+v[j+h],
- * v[j]-v[j+h]) for every j whose bit h is clear.  Each sum and difference
- * is one IEEE single rounding. */
-void oracle_fwht128_f32(float* v) {
-  for (int h = 1; h < 128; h <<= 1)
-    for (int i = 0; i < 128; i += 2 * h)
-      for (int j = i; j < i + h; ++j) {
-        volatile float a = v[j], b = v[j + h];
-        v[j] = a + b;
-        v[j + h] = a - b;
-      }
-}
-
-/* FP8 per-block quantiser for indexer vectors (one block = one 128-vector):
- * rotate by the normalised Hadamard, take the block's largest magnitude,
- * scale = amax / 448 (1 when the block is all zero), code = E4M3(x / scale).
- * All steps in fp32 so that every code is decided in the same precision as
- * the device quantiser.  x is bf16 [rows, 128]; q is [rows, 128] codes;
- * scale is [rows]. */
-void oracle_fp8_quantize_rows(const uint16_t* x, int64_t rows, uint8_t* q, float* scale) {
-  const float inv_sqrt128 = 0.08838834764831845f; /* 1/sqrt(128) rounded to fp32 */
+/* The rotated rows H_128 x / sqrt(128) of bf16 rows x [rows, 128], in fp64
+ * (test bookkeeping: the values the quantiser below encodes). */
+void oracle_fp8_rotate_rows(const uint16_t* x, int64_t rows, double* y) {
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r) {
-    float v[128];
-    for (int j = 0; j < 128; ++j) v[j] = (float)bf16_value(x[r * 128 + j]);
-    oracle_fwht128_f32(v);
-    float amax = 0.0f;
-    for (int j = 0; j < 128; ++j) {
-      volatile float t = v[j] * inv_sqrt128;
-      v[j] = t;
-      float m = fabsf(t);
-      if (m > amax) amax = m;
-    }
-    volatile float sc = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+    double v[128];
+    for (int j = 0; j < 128; ++j) v[j] = bf16_value(x[r * 128 + j]);
+    oracle_hadamard128_f64(v, y + r * 128);
+  }
+}
+
+/* FP8 per-block quantiser for indexer vectors ("GLM-5.2 / 总览" sub-doc
+ * index row 02: "FP8 per-block + Hadamard"; one block = one 128-vector):
+ *   y     = H_128 x / sqrt(128)                       (fp64, definition above)
+ *   scale = amax / 448 as fp32, amax = max_j |y_j|    (1 for an all-zero block)
+ *   q_j   = E4M3(y_j / scale), nearest, ties to even, saturating
+ * The quotient is formed in fp64 (one rounding of 2^-53 relative) and
+ * encoded from that double.  x is bf16 [rows, 128]; q is [rows, 128] codes;
+ * scale is [rows]. */
+void oracle_fp8_quantize_rows(const uint16_t* x, int64_t rows, uint8_t* q, float* scale) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    double v[128], y[128];
+    for (int j = 0; j < 128; ++j) v[j] = bf16_value(x[r * 128 + j]);
+    oracle_hadamard128_f64(v, y);
+    double amax = 0.0;
+    for (int j = 0; j < 128; ++j)
+      if (fabs(y[j]) > amax) amax = fabs(y[j]);
+    const float sc = oracle_fp8_block_scale(amax);
     scale[r] = sc;
-    for (int j = 0; j < 128; ++j) {
-      volatile float y = v[j] / sc;
-      q[r * 128 + j] = oracle_e4m3_encode(y);
-    }
+    for (int j = 0; j < 128; ++j) q[r * 128 + j] = oracle_e4m3_encode_f64(y[j] / (double)sc);
   }
 }
 
@@ -202,36 +243,39 @@ void oracle_rope_bf16(const uint16_t* x, const int32_t* pos, int64_t n, int dim,
 /* FP8 KV cache row (656 bytes per position; "GLM-5.2 / 总览" config table:
  * per-token per-layer KV cache BF16 = 1152 B, FP8 ~656 B per-group): the
  * 512-d latent as E4M3 codes in four groups of 128 dims, each with its own
- * fp32 scale amax/448 (1 for an all-zero group), then the 64-d RoPE key kept
- * in bf16:  bytes [0, 512) codes, [512, 528) four fp32 scales,
- * [528, 656) 64 bf16.  Codes are decided in fp32 (x / scale, E4M3 round to
- * nearest even, saturating), as by the quantiser that writes the cache. */
+ * scale amax/448 stored as fp32 (1 for an all-zero group), then the 64-d
+ * RoPE key kept in bf16:  bytes [0, 512) codes, [512, 528) four fp32 scales,
+ * [528, 656) 64 bf16.  Code = the E4M3 value nearest to x / scale (ties to
+ * even, saturating).  The quotient of a bf16 value by an fp32 scale is
+ * formed in fp64; it can lie no closer than about 2^-30 relative to an
+ * E4M3 rounding boundary without being on it, far more than fp64's 2^-53,
+ * so each code is the exact quotient's. */
 void oracle_kv_fp8_quantize(const uint16_t* kv, int64_t rows, uint8_t* out) {
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r) {
     const uint16_t* x = kv + r * 576;
     uint8_t* o = out + r * 656;
     for (int g = 0; g < 4; ++g) {
-      float amax = 0.0f;
+      double amax = 0.0;
       for (int j = 0; j < 128; ++j) {
-        const float m = fabsf((float)bf16_value(x[128 * g + j]));
+        const double m = fabs(bf16_value(x[128 * g + j]));
         if (m > amax) amax = m;
       }
-      volatile float sc = (amax > 0.0f) ? amax / 448.0f : 1.0f;
-      memcpy(o + 512 + 4 * g, (const void*)&sc, 4);
-      for (int j = 0; j < 128; ++j) {
-        volatile float y = (float)bf16_value(x[128 * g + j]) / sc;
-        o[128 * g + j] = oracle_e4m3_encode(y);
-      }
+      const float sc = oracle_fp8_block_scale(amax);
+      memcpy(o + 512 + 4 * g, &sc, 4);
+      for (int j = 0; j < 128; ++j)
+        o[128 * g + j] = oracle_e4m3_encode_f64(bf16_value(x[128 * g + j]) / (double)sc);
     }
     memcpy(o + 528, x + 512, 128);
   }
 }
 
 /* The bf16 row the attention reads from an FP8 KV row: latent value =
- * code * scale formed as an fp32 product (the scale's precision; round to
- * nearest even), then rounded to the bf16 the attention multiplies; the RoPE
- * key as stored. */
+ * code * scale formed as an fp32 product (round to nearest even), then
+ * rounded to the bf16 the attention multiplies; the RoPE key as stored.  The
+ * pages fix no rounding for this step; two roundings (fp32, then bf16)
+ * rather than one of the exact product is the reading taken because it is
+ * the cheaper one to widen inside the attention kernel. */
 void oracle_kv_fp8_dequantize(const uint8_t* in, int64_t rows, uint16_t* kv) {
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r) {

@@ -109,3 +109,39 @@ def test_dequantisation_rounds_the_fp32_product():
     # a product with no rounding at either step keeps every bit
     d2 = oracle.kv_fp8_dequantize(_row([0x7E, 0x01], [2.0 ** -3, 1, 1, 1]))[0]
     assert d2[0] == 0x4260 and d2[1] == 0x3980  # 448/8 = 56, 2^-9 / 8 = 2^-12
+
+
+def test_codes_are_the_exact_quotients():
+    # bf16 elements and group maxima for which the fp32 quotient x / scale
+    # lands exactly on an E4M3 midpoint while the exact quotient lies just
+    # above it: the definition (nearest E4M3 to x / scale) rounds up, where
+    # an fp32 quotient followed by ties-to-even would round down.
+    #   amax 1.375, x 0.2578125: x / scale = 84.0000018 -> 88 (fp32: 84 -> 80)
+    #   amax 1.046875, x 0.003067: 1.31250004 -> 1.375  (fp32: 1.3125 -> 1.25)
+    #   amax 1.40625, x 0.00824: 2.62500008 -> 2.75     (fp32: 2.625 -> 2.5)
+    row = np.zeros((1, 576), np.uint16)
+    row[0, [0, 1]] = [0x3FB0, 0x3E84]
+    row[0, [128, 129]] = [0x3F86, 0x3B49]
+    row[0, [256, 257]] = [0x3FB4, 0x3C07]
+    q = oracle.kv_fp8_quantize(row)
+    assert [int(q[0, 1]), int(q[0, 129]), int(q[0, 257])] == [0x6B, 0x3B, 0x43]
+    assert oracle.e4m3_decode(q[0, [1, 129, 257]]).tolist() == [88.0, 1.375, 2.75]
+    # the scales are the fp32 quotients amax / 448 (exact amax, one rounding)
+    sc = _scales(q)[0]
+    assert sc[0] == np.float32(1.375) / np.float32(448) and sc[3] == 1.0
+
+
+def test_codes_nearest_by_brute_force():
+    from fractions import Fraction as F
+    rng = np.random.default_rng(9)
+    kv = synth.f32_to_bf16_bits(rng.standard_normal((2, 576)).astype(np.float32) * np.float32(0.05))
+    q = oracle.kv_fp8_quantize(kv)
+    sc = _scales(q)
+    x = synth.bf16_bits_to_f32(kv).astype(np.float64)
+    grid = [(c, F(float(oracle.e4m3_decode(np.array([c], np.uint8))[0])))
+            for c in range(256) if c not in (0x7F, 0xFF)]
+    for r in range(2):
+        for d in range(0, 512, 7):
+            t = F(float(x[r, d])) / F(float(sc[r, d // 128]))
+            best = min(grid, key=lambda cv: (abs(t - cv[1]), cv[0] & 1))[0]
+            assert q[r, d] == best, (r, d)
