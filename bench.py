@@ -78,6 +78,39 @@ def load_peaks():
     return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
 
 
+# a timed region shorter than this runs at the burst clock; longer ones settle
+# under the power cap, so their tensor-bound kernels are graded against the
+# sustained peak
+SUSTAINED_AFTER_S = 3.0
+
+
+def measure_fp8_peak(dev):
+    """Dense E4M3 x E4M3 -> bf16 GEMM throughput (TFLOP/s, best of 10
+    8192^3 products through cuBLASLt), the denominator of a tensor-bound FP8
+    indexer; None where the library call is unavailable."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = None
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        return round(2.0 * n ** 3 / (best / 1e3) / 1e12, 1)
+    except Exception:  # noqa: BLE001 - report the nominal ratio instead
+        return None
+
+
 # ---------------------------------------------------------------- algorithmic work
 def algorithmic(lay, cfg, fp8, kv_row_bytes=1152):
     """Per-launch algorithmic FLOPs / bytes of each kernel for this layout."""
@@ -104,14 +137,72 @@ def algorithmic(lay, cfg, fp8, kv_row_bytes=1152):
             "sparse_mla": {"flops": mla_flops, "bytes": float(mla_bytes)}}
 
 
-def kernel_bound(name, work, peaks, fp8):
-    """Roofline bound of a kernel: whichever of tensor / HBM time is larger."""
-    tc = peaks["bf16_sustained"] * (2.0 if (fp8 and name == "indexer") else 1.0)
+def tensor_peak(peaks, fp8_indexer=False, timed_s=0.0):
+    """(TFLOP/s, description) of the tensor-core peak a kernel is graded
+    against: the burst bf16 GEMM for a timed region shorter than
+    SUSTAINED_AFTER_S, the sustained one otherwise; for the FP8 indexer the
+    measured E4M3 GEMM, else the bf16 peak times the nominal 2x ratio."""
+    sustained = timed_s >= SUSTAINED_AFTER_S
+    bf16 = peaks["bf16_sustained"] if sustained else peaks["bf16"]
+    kind = "sustained" if sustained else "burst"
+    if not fp8_indexer:
+        return bf16, f"{peaks['src']} {kind} bf16 GEMM"
+    if peaks.get("fp8"):
+        f = peaks["fp8"] * (peaks["bf16_sustained"] / peaks["bf16"] if sustained else 1.0)
+        return f, f"measured E4M3 GEMM ({kind})"
+    return 2.0 * bf16, f"{peaks['src']} {kind} bf16 GEMM x 2 (nominal FP8 ratio)"
+
+
+def kernel_bound(name, work, peaks, fp8, timed_s=0.0):
+    """Roofline bound of a kernel: whichever of tensor / HBM time is larger.
+    Returns (bound, peak, unit, peak description)."""
+    tc, tc_src = tensor_peak(peaks, fp8 and name == "indexer", timed_s)
     t_tc = work["flops"] / (tc * 1e12) if work["flops"] else 0.0
     t_hbm = work["bytes"] / (peaks["hbm"] * 1e9)
     if t_tc >= t_hbm:
-        return "tensor", tc, "TFLOP/s"
-    return "hbm", peaks["hbm"], "GB/s"
+        return "tensor", tc, "TFLOP/s", tc_src
+    return "hbm", peaks["hbm"], "GB/s", f"{peaks['src']} HBM copy"
+
+
+def kernel_records(prof, work, peaks, fp8, timed_s, c2c_gbs=None):
+    """Per-kernel roofline records from the library's live CUDA-event
+    profile of the timed steps."""
+    kernels = {}
+    for name in ("indexer", "topk", "sparse_mla", "append", "hot_plan", "hot_fetch"):
+        if name not in work or name not in prof:
+            continue
+        ms, n = prof[name]
+        if n == 0:
+            continue
+        avg_s = ms / n / 1e3
+        if name == "hot_fetch":  # reads over NVLink-C2C: against the measured host->device copy
+            bound, peak, unit, src = "c2c", c2c_gbs, "GB/s", "measured host->device copy"
+        else:
+            bound, peak, unit, src = kernel_bound(name, work[name], peaks, fp8, timed_s)
+        ach = (work[name]["flops"] / avg_s / 1e12) if bound == "tensor" else (
+            work[name]["bytes"] / avg_s / 1e9)
+        kernels[name] = {"launches": n, "ms_per_launch": round(ms / n, 4), "share": None,
+                         "bound": bound, "achieved": round(ach, 2), "peak": peak, "unit": unit,
+                         "frac": round(ach / peak, 4), "peak_src": src}
+    ktot = sum(v["ms_per_launch"] * v["launches"] for v in kernels.values())
+    for v in kernels.values():
+        v["share"] = round(v["ms_per_launch"] * v["launches"] / ktot, 4) if ktot else None
+    return kernels
+
+
+def scan_gather_record(kernels, work, peaks):
+    """HBM-bound (decode) groups: the index scans and the sparse gathers of
+    the timed steps together, algorithmic bytes over their summed launch
+    times; None when either kernel is not HBM-bound."""
+    if not all(kernels.get(k, {}).get("bound") == "hbm" for k in ("indexer", "sparse_mla")):
+        return None
+    byt = sum(work[k]["bytes"] * kernels[k]["launches"] for k in ("indexer", "sparse_mla"))
+    sec = sum(kernels[k]["ms_per_launch"] * kernels[k]["launches"] / 1e3
+              for k in ("indexer", "sparse_mla"))
+    ach = byt / sec / 1e9
+    return {"achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
+            "frac": round(ach / peaks["hbm"], 4),
+            "what": "indexer scans + sparse-MLA gathers of the timed steps"}
 
 
 # ---------------------------------------------------------------- replicas
@@ -279,6 +370,84 @@ def setup(workload, dev, seed=0, paged=0, kv_fp8=False):
     else:
         batch = dsa.Batch(lay.q_start, lay.q_pos, lay.seq_row0, lay.max_len, device=dev)
     return cfg, lay, layers, batch, fp8, phys
+
+
+def ablation_layers(cfg, layers, types):
+    """The layers of a group run as `types`: the workload's own layers, or for
+    the every-layer-indexer ablation each layer with the indexer inputs of
+    the F layer that leads its group."""
+    if types == cfg["layers"]:
+        return layers
+    out = []
+    last_f = None
+    for l, c in enumerate(cfg["layers"]):
+        if c == "F":
+            last_f = layers[l]
+        d = dict(layers[l])
+        for k_ in ("q_idx", "w", "k_idx", "q_scale", "k_scale"):
+            if k_ in last_f:
+                d[k_] = last_f[k_]
+        out.append(d)
+    return out
+
+
+def make_group_for(dsa, cfg, lay, layers, batch, types, dev):
+    """(Group, workspace, index buffer) of one group configuration."""
+    import torch
+    g = dsa.Group(types, ablation_layers(cfg, layers, types), k=cfg["K"], scale=1 / 16)
+    ws = dsa.workspace(g.workspace_size(batch), dev)
+    idx = torch.empty((lay.num_q, cfg["K"]), dtype=torch.int32, device=dev)
+    return g, ws, idx
+
+
+def measure_workload(dsa, name, args, dev, peaks, stream, flush):
+    """One more workload of the configs, timed like the headline one (device-
+    resident inputs, L2 flushed between steps, CUDA events, clocks sampled
+    during the timed steps), with its per-kernel roofline records, the
+    scan + gather HBM fraction of decode groups and the every-layer-indexer
+    ablation.  Its device memory is released before returning."""
+    import torch
+    cfg, lay, layers, batch, fp8, _ = setup(name, dev)
+    steps = max(5, args.steps if cfg["kind"] == "decode" else min(args.steps, 10))
+    group, ws, idx = make_group_for(dsa, cfg, lay, layers, batch, cfg["layers"], dev)
+    run = lambda: dsa.indexshare_group_forward(group, batch, idx, ws=ws)
+    for _ in range(args.warmup):
+        run()
+        flush()
+    dsa.status_fetch(ws)
+    torch.cuda.synchronize(dev)
+    dsa.launch_counts_reset()
+    dsa.dsa_profile_enable(True)
+    clk = ClockSampler(getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None))
+    clk.start()
+    time.sleep(0.3)
+    times = time_steps(run, steps, 0, flush, stream)
+    clocks = clk.stop()
+    dsa.dsa_profile_enable(False)
+    prof = dsa.dsa_profile_collect()
+    launches = sum(dsa.launch_counts().values())
+    dsa.status_fetch(ws)
+    total_ms = sum(times)
+    work = algorithmic(lay, cfg, fp8)
+    kernels = kernel_records(prof, work, peaks, fp8, total_ms / 1e3)
+    rec = {"workload": DESCR[name], "value": round(lay.num_q * steps / (total_ms / 1e3), 1),
+           "unit": UNIT, "steps": steps, "warmup": args.warmup,
+           "ms_per_step": round(total_ms / steps, 4), "layers": cfg["layers"],
+           "dtype": "bf16" + ("+fp8-indexer" if fp8 else ""), "kernels": kernels,
+           "scan_gather_hbm": scan_gather_record(kernels, work, peaks), "gpu_launches": launches,
+           "clocks": clocks}
+    types_all = "F" * len(cfg["layers"])
+    g2, ws2, idx2 = make_group_for(dsa, cfg, lay, layers, batch, types_all, dev)
+    t2 = time_steps(lambda: dsa.indexshare_group_forward(g2, batch, idx2, ws=ws2), steps,
+                    args.warmup, flush, stream)
+    dsa.status_fetch(ws2)
+    rec["ablation"] = {"layers": types_all, "value": round(lay.num_q * steps / (sum(t2) / 1e3), 1),
+                       "ms_per_step": round(sum(t2) / steps, 4),
+                       "indexshare_speedup": round(sum(t2) / total_ms, 3)}
+    del group, ws, idx, g2, ws2, idx2, layers, batch
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return rec
 
 
 def time_steps(run, steps, warmup, flush, stream, after=None):
@@ -511,6 +680,10 @@ def main():
     ap.add_argument("--hot-no-touch", action="store_true",
                     help="with --hot: skip the one-time device read of every host page of the "
                          "cold store (first swap-ins then pay for first page accesses)")
+    ap.add_argument("--extra-workloads", default=None, metavar="NAMES",
+                    help="comma-separated workloads timed after the main one, each recorded "
+                         "under 'workloads' (default with the prefill8k workload: "
+                         "decode64,chunked,decode1m; '' for none; N = 1 only)")
     ap.add_argument("--paged", type=int, default=0, metavar="ROWS",
                     help="paged caches: blocks of ROWS positions (a multiple of 128) in a "
                          "permuted pool, addressed through a block table")
@@ -534,6 +707,11 @@ def main():
 
     import dsa_indexer_indexshare_gb300 as dsa
     peaks = load_peaks()
+    peaks["fp8"] = measure_fp8_peak(dev)
+    if args.extra_workloads is None:
+        plain = not (args.hot or args.paged or args.kv_fp8 or args.with_append)
+        args.extra_workloads = ("decode64,chunked,decode1m"
+                                if args.workload == "prefill8k" and plain else "")
     cfg, lay, layers, batch, fp8, phys = setup(args.workload, dev, paged=args.paged,
                                                kv_fp8=args.kv_fp8)
     stream = torch.cuda.current_stream(dev)
@@ -541,27 +719,7 @@ def main():
     flush = lambda: flush_buf.fill_(1)
 
     def make_group(types):
-        g = dsa.Group(types, layers_for(types), k=cfg["K"], scale=1 / 16)
-        ws = dsa.workspace(g.workspace_size(batch), dev)
-        idx = torch.empty((lay.num_q, cfg["K"]), dtype=torch.int32, device=dev)
-        return g, ws, idx
-
-    def layers_for(types):
-        if types == cfg["layers"]:
-            return layers
-        # every-layer-indexer ablation: each layer runs its own indexer over
-        # the F layer's indexer inputs of its group
-        out = []
-        last_f = None
-        for l, c in enumerate(cfg["layers"]):
-            if c == "F":
-                last_f = layers[l]
-            d = dict(layers[l])
-            for k_ in ("q_idx", "w", "k_idx", "q_scale", "k_scale"):
-                if k_ in last_f:
-                    d[k_] = last_f[k_]
-            out.append(d)
-        return out
+        return make_group_for(dsa, cfg, lay, layers, batch, types, dev)
 
     hot = None
     if args.hot:
@@ -627,37 +785,9 @@ def main():
         dsa.status_fetch(append_ws)
     if hot is not None:
         work.update(hot.work(args.steps, prof))
-    kernels = {}
-    for name in ("indexer", "topk", "sparse_mla", "append", "hot_plan", "hot_fetch"):
-        if name not in work or name not in prof:
-            continue
-        ms, n = prof[name]
-        if n == 0:
-            continue
-        avg_s = ms / n / 1e3
-        if name == "hot_fetch":  # reads over NVLink-C2C: against the measured host->device copy
-            bound, peak, unit = "c2c", hot.c2c_gbs, "GB/s"
-        else:
-            bound, peak, unit = kernel_bound(name, work[name], peaks, fp8)
-        ach = (work[name]["flops"] / avg_s / 1e12) if bound == "tensor" else (
-            work[name]["bytes"] / avg_s / 1e9)
-        kernels[name] = {"launches": n, "ms_per_launch": round(ms / n, 4), "share": None,
-                         "bound": bound, "achieved": round(ach, 2), "peak": peak, "unit": unit,
-                         "frac": round(ach / peak, 4)}
-    ktot = sum(v["ms_per_launch"] * v["launches"] for v in kernels.values())
-    for v in kernels.values():
-        v["share"] = round(v["ms_per_launch"] * v["launches"] / ktot, 4) if ktot else None
-    # HBM-bound (decode) groups: the index scan and the sparse gathers of the
-    # step together, algorithmic bytes over their summed launch times
-    scan_gather = None
-    if all(kernels.get(k, {}).get("bound") == "hbm" for k in ("indexer", "sparse_mla")):
-        byt = sum(work[k]["bytes"] * kernels[k]["launches"] for k in ("indexer", "sparse_mla"))
-        sec = sum(kernels[k]["ms_per_launch"] * kernels[k]["launches"] / 1e3
-                  for k in ("indexer", "sparse_mla"))
-        ach = byt / sec / 1e9
-        scan_gather = {"achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
-                       "frac": round(ach / peaks["hbm"], 4),
-                       "what": "indexer scans + sparse-MLA gathers of the timed steps"}
+    kernels = kernel_records(prof, work, peaks, fp8, total_ms / 1e3,
+                             hot.c2c_gbs if hot is not None else None)
+    scan_gather = scan_gather_record(kernels, work, peaks)
     # the dominant on-GPU kernel (the hot swap-in is bound by the host link and
     # reported in "hot")
     top = max((k for k in kernels if not k.startswith("hot_")),
@@ -669,7 +799,7 @@ def main():
         traffic = NCU_TRAFFIC[top]["bytes"]
     roofline = {"kernel": top, "bound": tk["bound"], "achieved": tk["achieved"], "peak": tk["peak"],
                 "unit": tk["unit"], "frac": tk["frac"], "traffic": traffic,
-                "peak_src": f"{peaks['src']} ({'sustained bf16' if tk['bound'] == 'tensor' else 'HBM copy'})",
+                "peak_src": tk["peak_src"],
                 "units_per_launch": (work[top]["flops"] if tk["bound"] == "tensor" else work[top]["bytes"])}
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -689,7 +819,7 @@ def main():
                                 "group" if args.with_append else "the group forward"),
                        "l2": "flushed between steps (256 MiB write, outside the timed events)"},
             "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
-            "scan_gather_hbm": scan_gather,
+            "scan_gather_hbm": scan_gather, "fp8_peak_tflops": peaks.get("fp8"),
             "hot": hot.summary(args.steps, kernels) if hot is not None else None,
             "clocks": clocks, "wall_s_timed": round(wall, 3)}
 
@@ -711,13 +841,22 @@ def main():
         line["e2e"] = e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, world,
                               phys=phys)
 
+    # ---- the other workloads of the configs, each timed the same way (N = 1)
+    extras = [w for w in (args.extra_workloads.split(",") if args.extra_workloads else []) if w]
+    if extras and world == 1:
+        del group, ws, idx_buf
+        line["workloads"] = {}
+        for name in extras:
+            line["workloads"][name] = measure_workload(dsa, name, args, dev, peaks, stream, flush)
+
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
     if not args.no_cpu and rank == 0 and world == 1:
-        nrows = args.cpu_rows or {"tiny": 512, "prefill8k": 480, "decode64": 4, "chunked": 24,
-                                  "decode1m": 1, "prefill2k": 48, "decode8": 4,
-                                  "chunked1k": 24}[args.workload]
-        rows, host = oracle_sample(args.workload, lay, layers, cfg, fp8, nrows, phys=phys)
         import oracle
+        # at least one query row per host core (the oracle spreads rows over cores)
+        nrows = args.cpu_rows or max(oracle.num_threads(), {
+            "tiny": 512, "prefill8k": 480, "decode64": 4, "chunked": 24, "decode1m": 1,
+            "prefill2k": 48, "decode8": 4, "chunked1k": 24}[args.workload])
+        rows, host = oracle_sample(args.workload, lay, layers, cfg, fp8, nrows, phys=phys)
         secs = run_oracle(lay, host, rows, cfg, fp8)
         line["cpu_baseline"] = {"value": round(len(rows) / secs, 3), "unit": UNIT,
                                 "cores": oracle.num_threads(), "cpu": cpu_model(), "kind": "oracle",
@@ -826,9 +965,10 @@ def reference_arm(args):
     cfg = dict(synth.WORKLOADS[args.workload])
     lay = synth.workload_layout(args.workload)
     fp8 = bool(cfg.get("fp8"))
-    nrows = args.cpu_rows or {"tiny": 64, "prefill8k": 8, "decode64": 1, "chunked": 4,
-                              "decode1m": 1, "prefill2k": 8, "decode8": 1,
-                              "chunked1k": 4}[args.workload]
+    # at least one query row per host core (the oracle spreads rows over cores)
+    nrows = args.cpu_rows or max(oracle.num_threads(), {
+        "tiny": 64, "prefill8k": 8, "decode64": 1, "chunked": 4, "decode1m": 1, "prefill2k": 8,
+        "decode8": 1, "chunked1k": 4}[args.workload])
     sub, rows, host = reference_inputs(lay, cfg, fp8, nrows)
     for _ in range(args.warmup):
         run_oracle(sub, host, rows, cfg, fp8)

@@ -16,16 +16,8 @@ namespace dsa {
 
 namespace {
 thread_local std::string g_last_error;
-std::atomic<uint64_t> g_launches[kNumLaunchKinds];
-std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+}  // namespace
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn g_encode = nullptr;
-
-dsa_status_t fail(dsa_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 dsa_status_t fail(dsa_status_t s, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -41,7 +33,9 @@ dsa_status_t cuda_status(cudaError_t e, const char* where) {
   return fail(DSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
+namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
 
 dsa_status_t check_batch(const dsa_batch_t* b) {
   if (!b) return fail(DSA_ERR_INVALID_ARG, "batch is NULL");
@@ -70,17 +64,6 @@ dsa_status_t check_batch(const dsa_batch_t* b) {
   return DSA_OK;
 }
 
-dsa_status_t check_ws(void* ws, size_t have, size_t need) {
-  if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
-  if (reinterpret_cast<uintptr_t>(ws) & 255u)
-    return fail(DSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  if (have < need)
-    return fail(DSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", have, need);
-  return DSA_OK;
-}
-
-size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 dsa_status_t check_indexer_args(const void* q_idx, const float* q_scale, const float* w,
                                 const void* k_idx, const float* k_scale, int64_t k_rows,
                                 dsa_dtype_t dt) {
@@ -94,6 +77,32 @@ dsa_status_t check_indexer_args(const void* q_idx, const float* q_scale, const f
   if (k_rows > (int64_t(1) << 31) - 1) return fail(DSA_ERR_UNSUPPORTED, "k_rows >= 2^31");
   return DSA_OK;
 }
+
+dsa_status_t check_topk_k(int32_t k) {
+  if (k < 1 || k > 4096) return fail(DSA_ERR_UNSUPPORTED, "k=%d (supported: 1..4096)", k);
+  return DSA_OK;
+}
+
+namespace {
+std::atomic<uint64_t> g_launches[kNumLaunchKinds];
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+dsa_status_t check_ws(void* ws, size_t have, size_t need) {
+  if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return fail(DSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (have < need)
+    return fail(DSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", have, need);
+  return DSA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 dsa_status_t check_mla_args(const void* q_lat, const void* q_rope, const void* kv, int64_t kv_rows,
                             const int32_t* idx, int32_t k, int32_t heads, float scale,
@@ -390,7 +399,7 @@ size_t dsa_topk_workspace_size(const dsa_batch_t* b, int32_t k) {
 dsa_status_t dsa_topk(const float* scores, const dsa_batch_t* b, int32_t k, int32_t* idx, void* ws,
                       size_t ws_bytes, dsa_stream_t stream) {
   if (dsa_status_t s = check_batch(b)) return s;
-  if (k < 1 || k > 4096) return fail(DSA_ERR_UNSUPPORTED, "k=%d (supported: 1..4096)", k);
+  if (dsa_status_t s = check_topk_k(k)) return s;
   if (!scores || !idx) return fail(DSA_ERR_INVALID_ARG, "scores and idx are required");
   if (!aligned16(scores)) return fail(DSA_ERR_INVALID_ARG, "scores must be 16-byte aligned");
   const size_t need = dsa_topk_workspace_size(b, k);

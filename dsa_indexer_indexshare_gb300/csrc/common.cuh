@@ -66,6 +66,16 @@ __device__ __forceinline__ int query_pos(const BatchArgs& b, int t, int* status)
 
 // ------------------------------------------------------------- host helpers
 // Implemented in api.cu.
+// Record a message for dsa_last_error_string and return s.
+dsa_status_t fail(dsa_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+// DSA_OK for cudaSuccess, else DSA_ERR_CUDA with the error's name and `where`.
+dsa_status_t cuda_status(cudaError_t e, const char* where);
+// Argument checks shared by the entry points (each records its message).
+dsa_status_t check_batch(const dsa_batch_t* b);
+dsa_status_t check_indexer_args(const void* q_idx, const float* q_scale, const float* w,
+                                const void* k_idx, const float* k_scale, int64_t k_rows,
+                                dsa_dtype_t dt);
+dsa_status_t check_topk_k(int32_t k);
 bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
                   uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows);
 void count_launch(int which);

@@ -1,5 +1,5 @@
 // Inline-PTX building blocks for the sm_103a kernels of this library:
-// mbarriers with bounded waits, TMA tile / gather4 loads, tcgen05 (TMEM
+// mbarriers with bounded waits, TMA tile loads, tcgen05 (TMEM
 // allocation, MMA issue, commit, TMEM loads and stores), cluster / DSMEM
 // helpers, and the shared-memory and instruction descriptors that tcgen05.mma
 // consumes.  Every wait on an mbarrier is bounded by a wall-clock limit: when
@@ -104,18 +104,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int32
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// Gather of four rows (y0..y3) of a 2-D tensor, columns [x, x + box width),
-// into four consecutive box rows of shared memory.  The tensor map's box is
-// one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
       : "memory");
 }
 

@@ -27,8 +27,13 @@ namespace {
 constexpr int kStageMax = 18432;                 // positions staged per CTA
 constexpr int kStageBytesMax = kStageMax * 4;    // 72 KB of shared memory
 
+// Order-preserving image of an fp32 score: a > b as floats iff key(a) >
+// key(b) as unsigned integers.  -0.0 is first replaced by +0.0 so that the
+// two zeros are one value (equal scores, ties to the lower position); a NaN
+// with the sign bit clear ranks above +inf, one with it set below -inf.
 __device__ __forceinline__ uint32_t order_key(float x) {
-  const uint32_t u = __float_as_uint(x);
+  uint32_t u = __float_as_uint(x);
+  u = (u == 0x80000000u) ? 0u : u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

@@ -201,8 +201,10 @@ DSA_API dsa_status_t dsa_indexer_scores(const void* q_idx, const float* q_scale,
  * position.  idx[t, :] receives them in ascending position order; if
  * q_pos[t] + 1 < k every visible position is taken and the remaining slots
  * are -1.  scores is fp32 [num_q, max_len] (only s <= q_pos[t] is read), idx
- * int32 [num_q, k].  1 <= k <= 4096.  The comparison uses the fp32 bit
- * order (NaN ranks above +inf).  ws: dsa_topk_workspace_size (the status
+ * int32 [num_q, k].  1 <= k <= 4096.  Scores compare as fp32 values:
+ * -0.0 equals +0.0 (a tie, so the lower position wins); a NaN whose sign bit
+ * is clear ranks above +inf and one whose sign bit is set below -inf.
+ * ws: dsa_topk_workspace_size (the status
  * block, plus 48 KB of scratch per row for batches of fewer than 32 rows
  * longer than 16K positions).
  */
@@ -494,13 +496,17 @@ DSA_API dsa_status_t indexshare_group_forward_hot(const dsa_group_t* g, const ds
  * dsa_indexer_scores and dsa_topk; idx is int32 [num_q, k].
  *
  * The first call on a device looks up the array's device address with that
- * device current; make that first call before any stream capture.  Every
- * call clears the status word, then enqueues both kernels on `stream`; if
- * d_status_out (a device int32) is non-NULL the call's device status bits are
- * copied there at the end (0 = clean).  All calls share the array and it
- * keeps the last call's contents, so calls whose kernels overlap on the GPU
- * (other streams, other host threads on the same device) race on it.  Nothing
- * is allocated or freed by this call.
+ * device current (and again after the device's context has changed, e.g.
+ * after cudaDeviceReset); make that first call before any stream capture.
+ * Every call clears the status word, then enqueues both kernels on `stream`;
+ * if d_status_out (a device int32) is non-NULL the call's device status bits
+ * are copied there at the end (0 = clean).  d_status_out is written only
+ * when the call returns DSA_OK; on an error return the steps before the
+ * failing one may already be enqueued, and dsa_last_error_string names the
+ * step that failed.  All calls share the array and it keeps the last call's
+ * contents, so calls whose kernels overlap on the GPU (other streams, other
+ * host threads on the same device) race on it.  Nothing is allocated or
+ * freed by this call.
  */
 DSA_API dsa_status_t dsa_indexer_topk_noalloc(const void* q_idx, const float* q_scale,
                                               const float* w, const void* k_idx,

@@ -178,22 +178,12 @@ def planted_host_layers(layout: Layout, layer_types: str, H: int, *, m: int, see
     planted positions per sequence).  The premise of sparse attention made
     explicit, for tolerance checks of quantised indexers."""
     layers = host_layers(layout, layer_types, H, ints=False, seed=seed)
-    g = HostGen(seed + 7919)
     planted = []
-    for b in range(layout.num_seqs):
-        qs, qe = int(layout.q_start[b]), int(layout.q_start[b + 1])
-        if qe == qs:
-            planted.append(np.zeros(0, np.int64))
-            continue
-        first = int(layout.q_pos[qs:qe].min()) + 1       # positions every query sees
-        r = g.rng(10 * b)
-        pos = np.sort(r.choice(first, size=min(m, first), replace=False)).astype(np.int64)
+    for b, (qs, qe, pos, u, v) in enumerate(_planted_draws(layout, m, seed)):
         planted.append(pos)
+        if qe == qs:
+            continue
         rows = int(layout.seq_row0[b]) + pos
-        u = r.standard_normal(DI)
-        u /= np.linalg.norm(u)
-        v = r.standard_normal(DL)
-        v /= np.linalg.norm(v)
         for l, t in enumerate(layer_types):
             L = layers[l]
             lat = bf16_bits_to_f32(L["kv"][rows, :DL])
@@ -207,6 +197,57 @@ def planted_host_layers(layout: Layout, layer_types: str, H: int, *, m: int, see
                 L["q_idx"][qs:qe] = f32_to_bf16_bits((q + u).astype(np.float32))
                 L["w"][qs:qe] = np.abs(L["w"][qs:qe])
     return layers, planted
+
+
+def _planted_draws(layout: Layout, m: int, seed: int):
+    """Per sequence: (query rows [qs, qe), planted positions, u [128], v [512])
+    drawn from the seeded host stream shared by both planting functions."""
+    g = HostGen(seed + 7919)
+    out = []
+    for b in range(layout.num_seqs):
+        qs, qe = int(layout.q_start[b]), int(layout.q_start[b + 1])
+        if qe == qs:
+            out.append((qs, qe, np.zeros(0, np.int64), None, None))
+            continue
+        first = int(layout.q_pos[qs:qe].min()) + 1       # positions every query sees
+        r = g.rng(10 * b)
+        pos = np.sort(r.choice(first, size=min(m, first), replace=False)).astype(np.int64)
+        u = r.standard_normal(DI)
+        u /= np.linalg.norm(u)
+        v = r.standard_normal(DL)
+        v /= np.linalg.norm(v)
+        out.append((qs, qe, pos, u, v))
+    return out
+
+
+def plant_device(layers, layout: Layout, layer_types: str, *, m: int, seed: int = 0,
+                 latent_gain: float = 4.0):
+    """The planted relevant set of planted_host_layers, applied in place to
+    device layers (torch tensors from device_layers), for workloads too large
+    to draw on the host: the same positions and directions for the same
+    layout, m and seed, and the same arithmetic (fp64 sum, rounded to fp32,
+    then to bf16).  Returns the planted positions per sequence."""
+    import torch
+
+    planted = []
+    for b, (qs, qe, pos, u, v) in enumerate(_planted_draws(layout, m, seed)):
+        planted.append(pos)
+        if qe == qs:
+            continue
+        dev = layers[0]["kv"].device
+        rows = torch.as_tensor(int(layout.seq_row0[b]) + pos, device=dev)
+        uu = torch.as_tensor(u, dtype=torch.float64, device=dev)
+        vv = torch.as_tensor(latent_gain * v, dtype=torch.float64, device=dev)
+        add = lambda t, d: (t.double() + d).float().to(torch.bfloat16)
+        for l, t in enumerate(layer_types):
+            L = layers[l]
+            L["kv"][rows, :DL] = add(L["kv"][rows, :DL], vv)
+            L["q_lat"][qs:qe] = add(L["q_lat"][qs:qe], vv)
+            if t == "F":
+                L["k_idx"][rows] = add(L["k_idx"][rows], uu)
+                L["q_idx"][qs:qe] = add(L["q_idx"][qs:qe], uu)
+                L["w"][qs:qe] = L["w"][qs:qe].abs()
+    return planted
 
 
 # ---------------------------------------------------------------- device (torch)

@@ -71,3 +71,29 @@ def assert_topk_within_band(got_idx, scores, lens, K, rel=1e-3, what=""):
         bad = diff[np.abs(row[diff] - kth) > band]
         assert bad.size == 0, (f"{what} row {i}: {bad.size} positions differ outside the band "
                                f"(e.g. s={bad[:5]}, scores {row[bad[:5]]}, kth {kth})")
+
+
+def oracle_attention_gathered(q_lat, q_rope, kv, rows, base_rows, idx, scale, kv_bf16=None):
+    """Oracle sparse MLA for query rows `rows` of device tensors q_lat, q_rope
+    over their index rows idx [n, K] (positions, -1 padded), reading only the
+    cache rows they select: base_rows[i] + idx[i, j] of the device cache kv,
+    gathered on the device into a compact host copy [n * K, 576].  FP8 KV
+    rows (uint8 [rows, 656]) are checked against the oracle's quantisation of
+    the same rows of kv_bf16 and read through the oracle's dequantisation.
+    Returns (out [n, H, 512], lse [n, H]) in fp64."""
+    idx = np.asarray(idx)
+    n, K = idx.shape
+    dev = kv.device
+    rt = torch.as_tensor(np.asarray(rows, np.int64), device=dev)
+    cache_rows = np.asarray(base_rows, np.int64)[:, None] + np.maximum(idx, 0)
+    cr = torch.as_tensor(cache_rows.reshape(-1), device=dev)
+    if kv.dtype == torch.uint8:
+        codes = kv.index_select(0, cr).cpu().numpy()
+        assert np.array_equal(codes, oracle.kv_fp8_quantize(bits(kv_bf16.index_select(0, cr))))
+        kvh = oracle.kv_fp8_dequantize(codes)
+    else:
+        kvh = bits(kv.index_select(0, cr))
+    local = np.where(idx >= 0, np.arange(K)[None, :], -1).astype(np.int32)
+    return oracle.sparse_mla(bits(q_lat.index_select(0, rt)), bits(q_rope.index_select(0, rt)), kvh,
+                             np.arange(n, dtype=np.int32), np.arange(n, dtype=np.int64) * K, local,
+                             scale)

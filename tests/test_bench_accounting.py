@@ -62,7 +62,7 @@ def test_decode_reads_each_selected_row_once():
 
 
 def test_bounds_and_throughput():
-    peaks = {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0}
+    peaks = {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "measured"}
     prefill = bench.algorithmic(synth.make_layout([8192], [8192]), {"H": 64, "K": 2048}, False)
     decode = bench.algorithmic(synth.make_layout([131072] * 4, [1] * 4), {"H": 64, "K": 2048}, False)
     assert bench.kernel_bound("sparse_mla", prefill["sparse_mla"], peaks, False)[0] == "tensor"
@@ -78,3 +78,17 @@ def test_every_workload_is_described():
     assert set(bench.DESCR) == set(synth.WORKLOADS)
     for name, text in bench.DESCR.items():
         assert text and "KV latent" not in text  # the KV dtype is its own config key
+
+
+def test_tensor_peak_follows_the_timed_region():
+    peaks = {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "measured"}
+    # a short timed region runs at the burst clock, a long one under the power cap
+    assert bench.tensor_peak(peaks, False, 0.25)[0] == 1900.0
+    assert bench.tensor_peak(peaks, False, 10.0)[0] == 1700.0
+    # FP8 indexer: the nominal 2x ratio without a measured FP8 GEMM, else the measurement
+    assert bench.tensor_peak(peaks, True, 0.25)[0] == 3800.0
+    peaks["fp8"] = 3500.0
+    assert bench.tensor_peak(peaks, True, 0.25)[0] == 3500.0
+    assert bench.tensor_peak(peaks, True, 10.0)[0] == pytest.approx(3500.0 * 1700 / 1900)
+    work = {"flops": 1e12, "bytes": 1e6}
+    assert bench.kernel_bound("sparse_mla", work, peaks, False, 0.25)[:2] == ("tensor", 1900.0)
