@@ -101,6 +101,101 @@ struct RopeFreq {
   double f[32];  // theta^(-2i/64), the rotary frequencies of the first 64 dims
 };
 
+// sin and cos of an fp64 angle a (|a| < 2^30) in fp64, without a library
+// call: a is reduced to r = a - k pi/2, |r| <= pi/4 (a little more when
+// a * 2/pi rounds off), quadrant k mod 4, with pi/2 split as P1 + P2, P1
+// truncated to 22 significant bits so that k * P1 is exact for |k| < 2^31
+// and a - k * P1 is exact (error of r below |k| * 1.1e-23 + 2^-53: at most
+// 2^-44 at the largest angles allowed); then the Taylor series of sin to
+// r^13 and of cos to r^14 (truncation errors r^15/15! < 2^-45 and
+// r^16/16! < 2^-49 on |r| <= 0.8).
+constexpr double kTwoOverPi = 0.6366197723675814;
+constexpr double kHalfPiHi = 1.570796012878418;      // 22 significant bits of pi/2
+constexpr double kHalfPiLo = 3.139164786504813e-07;  // pi/2 - kHalfPiHi, rounded
+constexpr double kMaxReducedAngle = 1073741824.0;    // 2^30
+
+__device__ __forceinline__ void taylor_sincos(double a, double& s, double& c) {
+  const double k = rint(a * kTwoOverPi);
+  const double r = fma(-k, kHalfPiLo, fma(-k, kHalfPiHi, a));
+  const double r2 = r * r;
+  // +-1/n!
+  double ps = 1.6059043836821613e-10;                 // 1/13!
+  ps = fma(ps, r2, -2.505210838544172e-08);           // -1/11!
+  ps = fma(ps, r2, 2.7557319223985893e-06);           // 1/9!
+  ps = fma(ps, r2, -0.0001984126984126984);           // -1/7!
+  ps = fma(ps, r2, 0.008333333333333333);             // 1/5!
+  ps = fma(ps, r2, -0.16666666666666666);             // -1/3!
+  const double sr = fma(ps * r2, r, r);
+  double pc = -1.1470745597729725e-11;                // -1/14!
+  pc = fma(pc, r2, 2.08767569878681e-09);             // 1/12!
+  pc = fma(pc, r2, -2.755731922398589e-07);           // -1/10!
+  pc = fma(pc, r2, 2.48015873015873e-05);             // 1/8!
+  pc = fma(pc, r2, -0.001388888888888889);            // -1/6!
+  pc = fma(pc, r2, 0.041666666666666664);             // 1/4!
+  pc = fma(pc, r2, -0.5);                             // -1/2!
+  const double cr = fma(pc, r2, 1.0);
+  switch (static_cast<int>(static_cast<long long>(k) & 3)) {
+    case 0: s = sr; c = cr; break;
+    case 1: s = cr; c = -sr; break;
+    case 2: s = -sr; c = -cr; break;
+    default: s = -cr; c = sr; break;
+  }
+}
+
+// x0 * ch + x0 * cl - (x1 * sh + x1 * sl) as an unevaluated fp32 pair
+// (hi, lo), |lo| <= ulp(hi) / 2, for fp32 x0, x1 and double-float (ch, cl),
+// (sh, sl): the products with the high parts are split exactly by fma, the
+// difference of their high parts by TwoSum, and the remaining small terms
+// are added in fp32 (error below 2^-45 (|x0| + |x1|) besides the error of
+// the double-float cos / sin themselves).
+__device__ __forceinline__ void df_dot2(float x0, float ch, float cl, float x1, float sh, float sl,
+                                        float& hi, float& lo) {
+  const float p = __fmul_rn(x0, ch), pe = __fmaf_rn(x0, ch, -p);
+  const float q = __fmul_rn(x1, sh), qe = __fmaf_rn(x1, sh, -q);
+  const float t = __fsub_rn(p, q);
+  const float z = __fsub_rn(t, p);
+  const float te = __fadd_rn(__fsub_rn(p, __fsub_rn(t, z)), __fsub_rn(-q, z));
+  const float small = __fadd_rn(__fadd_rn(te, __fsub_rn(pe, qe)),
+                                __fsub_rn(__fmul_rn(x0, cl), __fmul_rn(x1, sl)));
+  hi = __fadd_rn(t, small);
+  const float z2 = __fsub_rn(hi, t);
+  lo = __fadd_rn(__fsub_rn(t, __fsub_rn(hi, z2)), __fsub_rn(small, z2));
+}
+
+// bf16 bits of hi + lo (|lo| <= ulp(hi) / 2, hi finite and nonzero when lo
+// is nonzero), round to nearest even: hi is narrowed toward zero by the
+// sign of lo and marked inexact (round to odd), then rounded to bf16; fp32
+// keeps 16 more bits than bf16, so this equals one rounding of hi + lo.
+__device__ __forceinline__ uint16_t df_to_bf16_bits(float hi, float lo) {
+  uint32_t u = __float_as_uint(hi);
+  if (lo != 0.f) {
+    if ((lo < 0.f) != (hi < 0.f)) u -= 1u;  // |hi + lo| < |hi|: one unit toward zero
+    u |= 1u;
+  }
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// Distance of hi + lo from the midpoint between the two bf16 values around
+// hi exceeds e (so that any value within e of hi + lo rounds to the same
+// bf16).  hi - m is exact (m lies in hi's binade, within a factor of two).
+__device__ __forceinline__ bool df_clear_of_bf16_midpoint(float hi, float lo, float e) {
+  const float m = __uint_as_float((__float_as_uint(hi) & 0xFFFF0000u) | 0x8000u);
+  return fabsf(__fadd_rn(__fsub_rn(hi, m), lo)) > e;
+}
+
+// The exact path of one pair: fp64 rotation by the library's fp64 sin / cos
+// of the fp64 angle a, each result rounded once to bf16 (kept out of line:
+// it runs for about one pair in 10^9).
+__device__ __noinline__ uint32_t rotate_pair_f64(double a, float x0, float x1) {
+  double sd, cd;
+  sincos(a, &sd, &cd);
+  const double d0 = x0, d1 = x1;
+  const uint32_t lo = f64_to_bf16_bits(__dsub_rn(__dmul_rn(d0, cd), __dmul_rn(d1, sd)));
+  const uint32_t hi = f64_to_bf16_bits(__dadd_rn(__dmul_rn(d0, sd), __dmul_rn(d1, cd)));
+  return lo | (hi << 16);
+}
+
 // Indexer cache append / query preparation ("GLM-5.2 架构深度拆解" CH 7.1:
 // interleaved RoPE of the indexer vectors; then the FP8 per-block quantiser
 // above).  Warp w takes the `group` vectors w*group .. w*group+group-1 (of
@@ -132,43 +227,116 @@ __global__ void __launch_bounds__(256) rope_append_kernel(
     if (lane == 0) atomicOr(status, DSA_DEVERR_INDEX);
     return;
   }
-  double sn[2] = {0.0, 0.0}, cs[2] = {1.0, 1.0};
-  if (lane < 16) {
-#pragma unroll
-    for (int q = 0; q < 2; ++q) sincos(static_cast<double>(pos) * rf.f[2 * lane + q], &sn[q], &cs[q]);
+  // cos / sin of the 32 angles pos * f[i], one per lane, in fp64 (Taylor
+  // series after an fp64 reduction), as double-float fp32 pairs; lanes 0..15
+  // (which hold the 64 rotated entries) then fetch those of their two pairs
+  float ch, cl, sh, sl;
+  bool fast;
+  {
+    const double a = static_cast<double>(pos) * rf.f[lane];
+    fast = fabs(a) < kMaxReducedAngle;
+    double sd = 0.0, cd = 1.0;
+    if (fast) taylor_sincos(a, sd, cd);
+    ch = static_cast<float>(cd);
+    cl = static_cast<float>(cd - static_cast<double>(ch));
+    sh = static_cast<float>(sd);
+    sl = static_cast<float>(sd - static_cast<double>(sh));
   }
-#pragma unroll 1
-  for (int k = 0; k < group; ++k) {
-    const int64_t v = w * group + k, row = row0 + k;
-    const uint2 raw = *reinterpret_cast<const uint2*>(x + v * 128 + lane * 4);
-    uint16_t h[4] = {static_cast<uint16_t>(raw.x & 0xFFFF), static_cast<uint16_t>(raw.x >> 16),
-                     static_cast<uint16_t>(raw.y & 0xFFFF), static_cast<uint16_t>(raw.y >> 16)};
-    if (lane < 16) {
+  float CH[2], CL[2], SH[2], SL[2];
+  bool FAST[2];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const double x0 = bf16_bits_to_float(h[2 * q]), x1 = bf16_bits_to_float(h[2 * q + 1]);
-        h[2 * q] = f64_to_bf16_bits(__dsub_rn(__dmul_rn(x0, cs[q]), __dmul_rn(x1, sn[q])));
-        h[2 * q + 1] = f64_to_bf16_bits(__dadd_rn(__dmul_rn(x0, sn[q]), __dmul_rn(x1, cs[q])));
+  for (int q = 0; q < 2; ++q) {
+    const int src = (2 * lane + q) & 31;
+    CH[q] = __shfl_sync(0xffffffffu, ch, src);
+    CL[q] = __shfl_sync(0xffffffffu, cl, src);
+    SH[q] = __shfl_sync(0xffffffffu, sh, src);
+    SL[q] = __shfl_sync(0xffffffffu, sl, src);
+    FAST[q] = __shfl_sync(0xffffffffu, fast ? 1 : 0, src) != 0;
+  }
+  // four vectors' loads in flight before any is used
+#pragma unroll 1
+  for (int k0 = 0; k0 < group; k0 += 4) {
+    uint2 raw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      raw[u] = k0 + u < group
+                   ? *reinterpret_cast<const uint2*>(x + (w * group + k0 + u) * 128 + lane * 4)
+                   : make_uint2(0u, 0u);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (k0 + u >= group) break;
+      const int64_t row = row0 + k0 + u;
+      uint16_t h[4] = {static_cast<uint16_t>(raw[u].x & 0xFFFF), static_cast<uint16_t>(raw[u].x >> 16),
+                       static_cast<uint16_t>(raw[u].y & 0xFFFF), static_cast<uint16_t>(raw[u].y >> 16)};
+      if (lane < 16) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float x0 = bf16_bits_to_float(h[2 * q]), x1 = bf16_bits_to_float(h[2 * q + 1]);
+          // y0 = x0 cos - x1 sin, y1 = x0 sin + x1 cos in double-float: error
+          // below 2^-43 (|x0| + |x1|) in all (reduction, series, the fp32
+          // splits and sums); their bf16 rounding is the exact one unless a
+          // value lies within that of a bf16 midpoint
+          float y0h, y0l, y1h, y1l;
+          df_dot2(x0, CH[q], CL[q], x1, SH[q], SL[q], y0h, y0l);
+          df_dot2(x0, SH[q], SL[q], -x1, CH[q], CL[q], y1h, y1l);
+          const float mag = fabsf(x0) + fabsf(x1);
+          const float e = mag * 9.094947017729282e-13f;  // 2^-40: a margin of 8x
+          const bool ok = FAST[q] && mag >= 7.888609052210118e-31f  // 2^-100: no subnormal steps
+                          && fabsf(y0h) < 3.0e38f && fabsf(y1h) < 3.0e38f &&
+                          df_clear_of_bf16_midpoint(y0h, y0l, e) &&
+                          df_clear_of_bf16_midpoint(y1h, y1l, e);
+          if (ok) {
+            h[2 * q] = df_to_bf16_bits(y0h, y0l);
+            h[2 * q + 1] = df_to_bf16_bits(y1h, y1l);
+          } else {
+            // within 2^-40 of a bf16 midpoint or outside the fast path
+            const uint32_t r =
+                rotate_pair_f64(static_cast<double>(pos) * rf.f[2 * lane + q], x0, x1);
+            h[2 * q] = static_cast<uint16_t>(r & 0xFFFF);
+            h[2 * q + 1] = static_cast<uint16_t>(r >> 16);
+          }
+        }
+      }
+      if constexpr (!FP8) {
+        uint2 o;
+        o.x = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
+        o.y = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16);
+        *reinterpret_cast<uint2*>(out_bf16 + row * 128 + lane * 4) = o;
+      } else {
+        float vv[4] = {bf16_bits_to_float(h[0]), bf16_bits_to_float(h[1]),
+                       bf16_bits_to_float(h[2]), bf16_bits_to_float(h[3])};
+        hadamard_quant_store(vv, lane, out_codes + row * 128, out_scale + row);
       }
     }
-    if constexpr (!FP8) {
-      uint2 o;
-      o.x = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
-      o.y = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[3]) << 16);
-      *reinterpret_cast<uint2*>(out_bf16 + row * 128 + lane * 4) = o;
-    } else {
-      float vv[4] = {bf16_bits_to_float(h[0]), bf16_bits_to_float(h[1]),
-                     bf16_bits_to_float(h[2]), bf16_bits_to_float(h[3])};
-      hadamard_quant_store(vv, lane, out_codes + row * 128, out_scale + row);
-    }
   }
+}
+
+// E4M3 code of the exact quotient x / sc (nearest, ties to even,
+// saturating) for an fp32 x and a positive fp32 scale.  Both are first
+// scaled by the same power of two so that sc lies in [1, 2) (exact; an x
+// that underflows there has a quotient far below the smallest E4M3
+// subnormal).  The quotient is rounded toward zero to fp32 and its lowest
+// bit set when the division was inexact (the fma gives the exact remainder's
+// sign, and with sc in [1, 2) a nonzero remainder cannot underflow): fp32
+// keeps 20 more bits than E4M3, so rounding this round-to-odd value to
+// nearest equals one rounding of the exact quotient.
+__device__ __forceinline__ __nv_fp8_storage_t e4m3_of_quotient(float x, float sc) {
+  int e;
+  frexpf(sc, &e);
+  const float s1 = ldexpf(sc, 1 - e), x1 = ldexpf(x, 1 - e);
+  const float qz = __fdiv_rz(x1, s1);
+  uint32_t u = __float_as_uint(qz);
+  if (fmaf(-qz, s1, x1) != 0.f) u |= 1u;
+  return __nv_cvt_float_to_fp8(__uint_as_float(u), __NV_SATFINITE, __NV_E4M3);
 }
 
 // FP8 KV latent rows ("GLM-5.2 / 总览" config table: FP8 KV ~656 B per token
 // and layer, per-group): warp r quantises bf16 row r [576] into 656 bytes,
 // the 512 latent dims as E4M3 codes in four groups of 128 (lane l: dims
-// 16l .. 16l+15, group l / 8), each group scaled by amax/448 (fp32; 1 for
-// an all-zero group), then the four fp32 scales, then the 64 bf16 RoPE dims.
+// 16l .. 16l+15, group l / 8), each group scaled by amax/448 (the fp32
+// division of the exact amax, i.e. its nearest fp32; 1 for an all-zero
+// group) and every code the nearest E4M3 to the exact quotient x / scale,
+// then the four fp32 scales, then the 64 bf16 RoPE dims.
 __global__ void __launch_bounds__(256) kv_fp8_quant_kernel(const uint16_t* __restrict__ kv,
                                                            int64_t rows,
                                                            uint8_t* __restrict__ out) {
@@ -197,9 +365,7 @@ __global__ void __launch_bounds__(256) kv_fp8_quant_kernel(const uint16_t* __res
     uint32_t pk = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const __nv_fp8_storage_t c =
-          __nv_cvt_float_to_fp8(__fdiv_rn(v[4 * k + j], sc), __NV_SATFINITE, __NV_E4M3);
-      pk |= static_cast<uint32_t>(c) << (8 * j);
+      pk |= static_cast<uint32_t>(e4m3_of_quotient(v[4 * k + j], sc)) << (8 * j);
     }
     packed[k] = pk;
   }
