@@ -50,11 +50,11 @@ DESCR = {
 # ncu DRAM traffic of the dominant kernel (bytes per launch), with the hash of
 # the kernel sources it was measured on; ignored once the sources change.
 NCU_TRAFFIC = {
-    # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch, scaled by
-    # tokens to the 8192-token launch (q/out traffic is per token; the kv cache is a few MB)
-    "sparse_mla": {"bytes": 1.0550e+09, "workload": "prefill8k", "src": "034d3a0a6d0faecf"},
+    # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch (204.5 MB
+    # read + 125.0 MB written), scaled by tokens to the 8192-token launch (q/out traffic is per
+    # token; the kv cache is a few MB)
+    "sparse_mla": {"bytes": 1.0545e+09, "workload": "prefill8k", "src": "c41ef80cd549b518"},
 }
-
 
 def kernel_src_hash(files):
     h = hashlib.sha256()

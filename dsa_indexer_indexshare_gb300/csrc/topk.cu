@@ -236,30 +236,41 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
 
 
 // ------------------------------------------------------------------ long rows
-// Few long rows (decode): three launches, no inter-CTA waits.
-//  1. hist:   each CTA adds a 12-bit histogram of its slice of a row into the
-//             row's global histogram.
-//  2. select: every CTA of the row finds the threshold bin b1 (the bin that
-//             holds the k-th largest key) from that histogram, writes every
-//             position of a higher bin straight to the output row and
-//             appends the positions of bin b1 (the candidates) to a per-row
-//             list of up to kCandCap entries.
-//  3. finish: one CTA per row selects the remaining `need` positions among
-//             the candidates (radix on the low 20 key bits, ties to the lower
-//             position), then sorts the row's k positions ascending.  A row
-//             whose candidate list overflowed rescans its scores instead.
+// Few long rows (decode of a few sequences): a row is cut into `split` slices of
+// consecutive positions; four launches without inter-CTA waits, and a
+// fallback launch for rows whose sample misled:
+//  0. cutoff:  one CTA per row histograms a sample of the row (kPrefix
+//              positions in 16 runs spread over it) and picks a cutoff bin
+//              that leaves about 1.5 times the sample's share of K above it.
+//  1. capture: every CTA of a row appends every key of its slice at or
+//              above the cutoff (float compare, warp ballots, no atomics per
+//              position) with its position to the row's capture list.
+//  2. resolve: one CTA per row.  With at least K keys captured (and none
+//              dropped) the k-th largest key is at or above the cutoff, so
+//              every key the selection takes is in the list: the threshold
+//              key T and the cut position pstar among keys equal to T follow
+//              from radix passes over the list, and the taken positions of
+//              each slice give every slice its first output slot.  A row
+//              without that guarantee is marked for the fallback.
+//  3. write:   every CTA writes its slice's positions with key > T, or key
+//              == T at a position up to pstar, in ascending order from its
+//              slot (block prefix scans): the row comes out sorted.
+//  4. fallback: the many-rows kernel below, on the marked rows only (each
+//              read in full, histogrammed, resolved exactly).
 constexpr int kHBits = 12;
 constexpr int kHBins = 1 << kHBits;   // 4096 bins over key bits [31:20]
-constexpr int kCandCap = 8192;        // candidates kept per row
+constexpr int kCandCap = 16384;       // captured keys kept per row
+constexpr int kLongSlack = 16;        // sampled keys added to the cutoff's 1.5x share of K
 constexpr int kLongBS = 512;
 constexpr int kFinBS = 512;
-constexpr int kFinDynBytes = 2 * kCandCap * 4;  // candidate keys + positions (64 KB)
-constexpr int kLocalCand = 2048;                 // candidates buffered per select CTA
+constexpr int kCapSeg = 192;          // captured keys buffered per warp of a capture CTA
+constexpr int kCnt = 8;  // per-row words: 1 captured, 2 dropped, 3 cutoff, 4 T, 5 pstar, 6 fallback
 
 struct LongScratch {
-  uint32_t* hist;  // [num_q][kHBins]
-  int* cnt;        // [num_q][4]: written-above, candidates, b1, above-count
-  int32_t* cand;   // [num_q][kCandCap]
+  int* cnt;          // [num_q][kCnt]
+  uint32_t* ckey;    // [num_q][kCandCap] captured keys
+  int32_t* cpos;     // [num_q][kCandCap] their positions
+  int* slice_off;    // [num_q][split]: first output slot of each slice
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -273,34 +284,6 @@ __device__ __forceinline__ void slice_of(int len, int split, int c, int& lo, int
   const int chunk = (((len + split - 1) / split) + 3) & ~3;
   lo = min(c * chunk, len);
   hi = min(lo + chunk, len);
-}
-
-__global__ void __launch_bounds__(kLongBS) topk_hist_kernel(const float* __restrict__ scores,
-                                                            BatchArgs b, int K, int split,
-                                                            LongScratch ws) {
-  __shared__ uint32_t h[kHBins];
-  const int t = blockIdx.y, tid = threadIdx.x;
-  const int pos = query_pos(b, t, nullptr);
-  if (pos + 1 <= K) return;
-  int lo, hi;
-  slice_of(pos + 1, split, blockIdx.x, lo, hi);
-  if (lo >= hi) return;
-  for (int i = tid; i < kHBins; i += kLongBS) h[i] = 0;
-  __syncthreads();
-  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
-  const int hi4 = lo + ((hi - lo) & ~3);
-  for (int s = lo + tid * 4; s < hi4; s += kLongBS * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(row + s);
-    atomicAdd(&h[order_key(v.x) >> 20], 1u);
-    atomicAdd(&h[order_key(v.y) >> 20], 1u);
-    atomicAdd(&h[order_key(v.z) >> 20], 1u);
-    atomicAdd(&h[order_key(v.w) >> 20], 1u);
-  }
-  for (int s = hi4 + tid; s < hi; s += kLongBS) atomicAdd(&h[order_key(row[s]) >> 20], 1u);
-  __syncthreads();
-  uint32_t* g = ws.hist + static_cast<int64_t>(t) * kHBins;
-  for (int i = tid; i < kHBins; i += kLongBS)
-    if (h[i]) atomicAdd(&g[i], h[i]);
 }
 
 // Threshold bin of a row from its histogram: the bin d with
@@ -327,76 +310,7 @@ __device__ void threshold_bin(const uint32_t* hist, int K, int* warp_sums, int* 
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kLongBS) topk_select_kernel(const float* __restrict__ scores,
-                                                              BatchArgs b, int K, int split,
-                                                              LongScratch ws, int32_t* idx) {
-  __shared__ uint32_t h[kHBins];
-  __shared__ int warp_sums[32];
-  __shared__ int s_b1, s_above;
-  const int t = blockIdx.y, tid = threadIdx.x;
-  const int pos = query_pos(b, t, nullptr);
-  if (pos + 1 <= K) return;
-  int lo, hi;
-  slice_of(pos + 1, split, blockIdx.x, lo, hi);
-  if (lo >= hi) return;
-  const uint32_t* g = ws.hist + static_cast<int64_t>(t) * kHBins;
-  for (int i = tid; i < kHBins; i += kLongBS) h[i] = g[i];
-  __syncthreads();
-  threshold_bin<kLongBS>(h, K, warp_sums, &s_b1, &s_above);
-  const uint32_t b1 = static_cast<uint32_t>(s_b1);
-  int* cnt = ws.cnt + static_cast<int64_t>(t) * 4;
-  if (tid == 0 && blockIdx.x == 0) {
-    cnt[2] = s_b1;
-    cnt[3] = s_above;
-  }
-  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
-  // positions of this slice above the threshold bin (fewer than K in all) and
-  // in it (the candidates) are buffered in shared memory, then appended to
-  // the row's lists with one global atomic each
-  __shared__ int32_t sgt[4096];
-  __shared__ int32_t scand[kLocalCand];
-  __shared__ int s_ng, s_nc, s_bg, s_bc;
-  if (tid == 0) {
-    s_ng = 0;
-    s_nc = 0;
-  }
-  __syncthreads();
-  const int hi4 = lo + ((hi - lo) & ~3);
-  auto visit = [&](int s, uint32_t key) {
-    const uint32_t bin = key >> 20;
-    if (bin > b1) {
-      const int i = atomicAdd(&s_ng, 1);
-      if (i < 4096) sgt[i] = s;
-    } else if (bin == b1) {
-      const int i = atomicAdd(&s_nc, 1);
-      if (i < kLocalCand) scand[i] = s;
-    }
-  };
-  for (int s = lo + tid * 4; s < hi4; s += kLongBS * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(row + s);
-    visit(s, order_key(v.x));
-    visit(s + 1, order_key(v.y));
-    visit(s + 2, order_key(v.z));
-    visit(s + 3, order_key(v.w));
-  }
-  for (int s = hi4 + tid; s < hi; s += kLongBS) visit(s, order_key(row[s]));
-  __syncthreads();
-  if (tid == 0) {
-    s_bg = atomicAdd(&cnt[0], s_ng);
-    // a slice with more candidates than its buffer marks the row as overflowed
-    s_bc = atomicAdd(&cnt[1], s_nc <= kLocalCand ? s_nc : kCandCap + 1);
-  }
-  __syncthreads();
-  int32_t* out = idx + static_cast<int64_t>(t) * K;
-  int32_t* cand = ws.cand + static_cast<int64_t>(t) * kCandCap;
-  const int ng = min(s_ng, 4096), nc = s_nc <= kLocalCand ? s_nc : 0;
-  for (int i = tid; i < ng; i += kLongBS)
-    if (s_bg + i < K) out[s_bg + i] = sgt[i];
-  for (int i = tid; i < nc; i += kLongBS)
-    if (s_bc + i < kCandCap) cand[s_bc + i] = scand[i];
-}
-
-// Radix select inside the finish kernel: among n items (key, position),
+// Radix select of a row's threshold-bin members: among n items (key, position),
 // all with key >> 20 == b1, find the key T of the need-th largest and how
 // many items equal to T are taken (ties to the lower position are resolved
 // afterwards).  get(i) returns the key of item i (or ~0u for a non-member).
@@ -578,86 +492,6 @@ __device__ void bitmap_compact(const uint32_t* bits, int nwords, int K, int32_t*
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kFinBS, 1) topk_finish_kernel(const float* __restrict__ scores,
-                                                             BatchArgs b, int K, LongScratch ws,
-                                                             int32_t* idx, int* status,
-                                                             int dyn_words) {
-  __shared__ int hist2[2048];
-  __shared__ int warp_sums[32];
-  __shared__ int s_d, s_above, s_n;
-  extern __shared__ uint32_t fin_dyn[];  // kFinDynBytes
-  uint32_t* ckey = fin_dyn;                                        // [kCandCap]
-  int32_t* cpos = reinterpret_cast<int32_t*>(fin_dyn + kCandCap);  // [kCandCap]
-  int32_t* sorted = reinterpret_cast<int32_t*>(fin_dyn);           // [4096], after ckey is done
-  const int t = blockIdx.x, tid = threadIdx.x;
-  const int pos = query_pos(b, t, tid == 0 ? status : nullptr);
-  const int len = pos + 1;
-  int32_t* out = idx + static_cast<int64_t>(t) * K;
-  if (len <= K) {
-    for (int j = tid; j < K; j += kFinBS) out[j] = j < len ? j : -1;
-    return;
-  }
-  const int* cnt = ws.cnt + static_cast<int64_t>(t) * 4;
-  const int nabove = cnt[3];            // positions in bins above b1 (already written)
-  const uint32_t b1 = static_cast<uint32_t>(cnt[2]);
-  const int nc = cnt[1];
-  const int need1 = K - nabove;
-  if (tid == 0 && cnt[0] != nabove) atomicOr(status, DSA_DEVERR_BATCH);
-  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
-  const bool fits = nc <= kCandCap;
-  const int n = fits ? nc : len;  // overflow: scan the whole row, members are bin b1
-  if (fits) {
-    const int32_t* cand = ws.cand + static_cast<int64_t>(t) * kCandCap;
-    for (int i = tid; i < nc; i += kFinBS) {
-      const int32_t p = cand[i];
-      cpos[i] = p;
-      ckey[i] = order_key(row[p]);
-    }
-  }
-  __syncthreads();
-  auto get_key = [&](int i) -> uint32_t {
-    if (fits) return ckey[i];
-    const uint32_t k = order_key(row[i]);
-    return (k >> 20) == b1 ? k : ~0u;
-  };
-  auto get_pos = [&](int i) -> int { return fits ? cpos[i] : i; };
-  uint32_t T;
-  int need;
-  select_low_bits<kFinBS>(n, need1, get_key, b1, hist2, warp_sums, &s_d, &s_above, &T, &need);
-  const int pstar = tied_position_cut<kFinBS>(n, need, T, get_key, get_pos, hist2, warp_sums, &s_d,
-                                              &s_above, &s_n);
-  if (tid == 0) s_n = nabove;
-  __syncthreads();
-  for (int i = tid; i < n; i += kFinBS) {
-    const uint32_t k = get_key(i);
-    if (k == ~0u) continue;
-    if (k > T || (k == T && get_pos(i) <= pstar)) {
-      const int slot = atomicAdd(&s_n, 1);
-      if (slot < K) out[slot] = get_pos(i);
-    }
-  }
-  __syncthreads();
-  // ascending order: the K positions marked in a bitmap over the row (in the
-  // candidate arrays' space, no longer needed) and compacted in order by one
-  // prefix scan; rows beyond the bitmap's reach are sorted instead
-  const int nwords = (len + 31) >> 5;
-  if (nwords <= dyn_words) {
-    uint32_t* bits = fin_dyn;
-    for (int i = tid; i < nwords; i += kFinBS) bits[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < K; i += kFinBS) {
-      const int p = out[i];
-      if (p >= 0 && p < len) atomicOr(&bits[p >> 5], 1u << (p & 31));
-    }
-    __syncthreads();
-    bitmap_compact<kFinBS>(bits, nwords, K, out, warp_sums, status);
-  } else {
-    for (int i = tid; i < K; i += kFinBS) sorted[i] = out[i];
-    sort_positions<kFinBS>(sorted, K);
-    for (int i = tid; i < K; i += kFinBS) out[i] = sorted[i];
-  }
-}
-
 // ------------------------------------------------------------------ many long rows
 // Many long rows (chunked prefill: thousands of rows of 128K+ positions).
 // One CTA per SM loops over rows and normally reads each row from HBM once:
@@ -723,7 +557,7 @@ __device__ __forceinline__ void scan_row(const float* __restrict__ row, int hi, 
 
 __global__ void __launch_bounds__(kRowBS, 1) topk_rows_kernel(const float* __restrict__ scores,
                                                              BatchArgs b, int K, int32_t* idx,
-                                                             int* status) {
+                                                             int* status, const int* only) {
   extern __shared__ uint32_t row_dyn[];
   uint32_t* hcopies = row_dyn;                                  // [kHCopies][kHStride], pass 1
   uint32_t* hist = row_dyn;                                     // [kHBins], summed copies
@@ -755,6 +589,8 @@ __global__ void __launch_bounds__(kRowBS, 1) topk_rows_kernel(const float* __res
   };
 #pragma unroll 1
   for (int t = blockIdx.x; t < b.num_q; t += gridDim.x) {
+    // `only` (the long path's per-row words): rows it marks for the fallback
+    if (only && only[static_cast<int64_t>(t) * kCnt + 6] == 0) continue;
     const int pos = query_pos(b, t, tid == 0 ? status : nullptr);
     const int len = pos + 1;
     int32_t* out = idx + static_cast<int64_t>(t) * K;
@@ -939,15 +775,287 @@ __global__ void __launch_bounds__(kRowBS, 1) topk_rows_kernel(const float* __res
   }
 }
 
-// Rows beyond 16K positions: fewer than kRowsMin of them are spread over
-// several CTAs each (the three launches above); more get a CTA each.
-constexpr int kRowsMin = 32;
+// Long path, launch 0: the row's cutoff from the same sample as the
+// many-rows kernel (the bin leaving about 1.5 times the sample's share of K
+// above it, plus kLongSlack), stored as the smallest fp32 value of that bin
+// (-inf for bin 0).  The sample is histogrammed in 4 copies (lane & 3) to
+// spread the shared atomics on the few bins the scores fall into.
+constexpr int kCutCopies = 4;
+constexpr int kCutDynBytes = kCutCopies * kHBins * 4;
+__global__ void __launch_bounds__(kLongBS) topk_cutoff_kernel(const float* __restrict__ scores,
+                                                              BatchArgs b, int K, LongScratch ws) {
+  extern __shared__ uint32_t cut_dyn[];  // [kCutCopies][kHBins]
+  __shared__ int warp_sums[32];
+  __shared__ int s_cut, s_tmp;
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int pos = query_pos(b, t, nullptr);
+  const int len = pos + 1;
+  if (len <= K) return;
+  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
+  for (int i = tid; i < kCutCopies * kHBins; i += kLongBS) cut_dyn[i] = 0;
+  if (tid == 0) s_cut = 0;
+  __syncthreads();
+  uint32_t* h = cut_dyn + (tid & (kCutCopies - 1)) * kHBins;
+  const int P0 = min(len, kPrefix);
+  constexpr int kRun = kPrefix / 16;
+  const bool whole = len <= kPrefix;
+  const int stride = (len / 16) & ~3;  // run starts stay float4-aligned
+  for (int v = tid * 4; v < P0; v += kLongBS * 4) {
+    const int s = whole ? v : (v / kRun) * stride + (v % kRun);
+    const float4 x = *reinterpret_cast<const float4*>(row + s);
+    atomicAdd(&h[order_key(x.x) >> 20], 1u);
+    if (s + 1 < len) atomicAdd(&h[order_key(x.y) >> 20], 1u);
+    if (s + 2 < len) atomicAdd(&h[order_key(x.z) >> 20], 1u);
+    if (s + 3 < len) atomicAdd(&h[order_key(x.w) >> 20], 1u);
+  }
+  __syncthreads();
+  for (int i = tid; i < kHBins; i += kLongBS) {
+    uint32_t sum = 0;
+#pragma unroll
+    for (int c = 0; c < kCutCopies; ++c) sum += cut_dyn[c * kHBins + i];
+    cut_dyn[i] = sum;
+  }
+  __syncthreads();
+  const int need_p =
+      static_cast<int>(3 * static_cast<int64_t>(K) * P0 / (2 * static_cast<int64_t>(len))) +
+      kLongSlack;
+  threshold_bin<kLongBS>(cut_dyn, need_p, warp_sums, &s_cut, &s_tmp);
+  if (tid == 0) {
+    const uint32_t k0 = static_cast<uint32_t>(s_cut) << 20;
+    const float cf = s_cut == 0 ? -INFINITY
+                                : __uint_as_float((k0 & 0x80000000u) ? (k0 & 0x7fffffffu) : ~k0);
+    ws.cnt[static_cast<int64_t>(t) * kCnt + 3] = __float_as_int(cf);
+  }
+}
+
+// Long path, launch 1: the slice's keys at or above the row's cutoff.
+__global__ void __launch_bounds__(kLongBS) topk_capture_kernel(const float* __restrict__ scores,
+                                                               BatchArgs b, int K, int split,
+                                                               LongScratch ws) {
+  __shared__ uint32_t skey[(kLongBS / 32) * kCapSeg];
+  __shared__ int32_t spos[(kLongBS / 32) * kCapSeg];
+  __shared__ int s_wcnt[kLongBS / 32];
+  __shared__ int s_base;
+  const int t = blockIdx.y, c = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int pos = query_pos(b, t, nullptr);
+  const int len = pos + 1;
+  if (len <= K) return;
+  int lo, hi;
+  slice_of(len, split, c, lo, hi);
+  if (lo >= hi) return;
+  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
+  const float cf = __int_as_float(ws.cnt[static_cast<int64_t>(t) * kCnt + 3]);
+  // keys >= cf (float compare: NaN kept too, a superset is harmless), per
+  // warp in its own segment of the shared buffer, in warp-uniform tiles
+  const uint32_t lt = lanemask_lt();
+  int wcount = 0;  // warp-uniform
+  for (int base = lo + warp * 128; base < hi; base += kLongBS * 4) {
+    const int s = base + lane * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (s < hi) v = *reinterpret_cast<const float4*>(row + s);
+    const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const bool p = s + q < hi && !(x[q] < cf);
+      const uint32_t m = __ballot_sync(0xffffffffu, p);
+      if (m) {
+        if (p) {
+          const int i = wcount + __popc(m & lt);
+          if (i < kCapSeg) {
+            skey[warp * kCapSeg + i] = order_key(x[q]);
+            spos[warp * kCapSeg + i] = s + q;
+          }
+        }
+        wcount += __popc(m);
+      }
+    }
+  }
+  if (lane == 0) s_wcnt[warp] = wcount;
+  __syncthreads();
+  int* cnt = ws.cnt + static_cast<int64_t>(t) * kCnt;
+  if (tid == 0) {
+    int total = 0, dropped = 0;
+    for (int w = 0; w < kLongBS / 32; ++w) {
+      total += min(s_wcnt[w], kCapSeg);
+      dropped += s_wcnt[w] > kCapSeg;
+    }
+    s_base = atomicAdd(&cnt[1], total);
+    if (dropped || s_base + total > kCandCap) atomicOr(&cnt[2], 1);
+  }
+  __syncthreads();
+  // copy this CTA's entries to the row's list (warp w's segment after the
+  // segments of warps < w)
+  int off = s_base;
+  for (int w = 0; w < warp; ++w) off += min(s_wcnt[w], kCapSeg);
+  const int n = min(s_wcnt[warp], kCapSeg);
+  for (int i = lane; i < n; i += 32)
+    if (off + i < kCandCap) {
+      ws.ckey[static_cast<int64_t>(t) * kCandCap + off + i] = skey[warp * kCapSeg + i];
+      ws.cpos[static_cast<int64_t>(t) * kCandCap + off + i] = spos[warp * kCapSeg + i];
+    }
+}
+
+// Long path, launch 2: the threshold key and tie cut of a row from its
+// capture list, and each slice's first output slot (or the row marked for
+// the fallback).
+__global__ void __launch_bounds__(kFinBS, 1) topk_resolve_kernel(BatchArgs b, int K, int split,
+                                                                 LongScratch ws, int* status) {
+  __shared__ int hist2[2048];
+  __shared__ uint32_t h[kHBins];
+  __shared__ int warp_sums[32];
+  __shared__ int s_d, s_above, s_n, s_b1, s_nabove;
+  extern __shared__ uint32_t res_dyn[];  // captured keys and positions, then taken per slice
+  uint32_t* ckey = res_dyn;
+  int32_t* cpos = reinterpret_cast<int32_t*>(res_dyn + kCandCap);
+  int* taken = reinterpret_cast<int*>(res_dyn + 2 * kCandCap);
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int pos = query_pos(b, t, tid == 0 ? status : nullptr);
+  const int len = pos + 1;
+  if (len <= K) return;
+  int* cnt = ws.cnt + static_cast<int64_t>(t) * kCnt;
+  const int n = cnt[1];
+  if (cnt[2] != 0 || n < K || n > kCandCap) {  // no guarantee: the fallback takes the row
+    if (tid == 0) cnt[6] = 1;
+    return;
+  }
+  for (int i = tid; i < n; i += kFinBS) {
+    ckey[i] = ws.ckey[static_cast<int64_t>(t) * kCandCap + i];
+    cpos[i] = ws.cpos[static_cast<int64_t>(t) * kCandCap + i];
+  }
+  for (int i = tid; i < kHBins; i += kFinBS) h[i] = 0;
+  for (int i = tid; i < split; i += kFinBS) taken[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kFinBS) atomicAdd(&h[ckey[i] >> 20], 1u);
+  __syncthreads();
+  threshold_bin<kFinBS>(h, K, warp_sums, &s_b1, &s_nabove);
+  const uint32_t b1 = static_cast<uint32_t>(s_b1);
+  auto get_key = [&](int i) -> uint32_t { return (ckey[i] >> 20) == b1 ? ckey[i] : ~0u; };
+  auto get_pos = [&](int i) -> int { return cpos[i]; };
+  uint32_t T;
+  int need;
+  select_low_bits<kFinBS>(n, K - s_nabove, get_key, b1, hist2, warp_sums, &s_d, &s_above, &T,
+                          &need);
+  const int pstar = tied_position_cut<kFinBS>(n, need, T, get_key, get_pos, hist2, warp_sums, &s_d,
+                                              &s_above, &s_n);
+  // taken positions per slice (slice_of's cut: slices of `chunk` positions)
+  const int chunk = (((len + split - 1) / split) + 3) & ~3;
+  for (int i = tid; i < n; i += kFinBS) {
+    const uint32_t k = ckey[i];
+    if (k > T || (k == T && cpos[i] <= pstar)) atomicAdd(&taken[cpos[i] / chunk], 1);
+  }
+  __syncthreads();
+  const int per = (split + kFinBS - 1) / kFinBS;
+  int local = 0;
+  for (int k = 0; k < per; ++k) {
+    const int c = tid * per + k;
+    if (c < split) local += taken[c];
+  }
+  int total;
+  int run = block_excl_scan<kFinBS>(local, warp_sums, &total);
+  for (int k = 0; k < per; ++k) {
+    const int c = tid * per + k;
+    if (c >= split) break;
+    ws.slice_off[static_cast<int64_t>(t) * split + c] = run;
+    run += taken[c];
+  }
+  if (tid == 0) {
+    cnt[4] = static_cast<int>(T);
+    cnt[5] = pstar;
+    if (total != K) atomicOr(status, DSA_DEVERR_BATCH);
+  }
+}
+
+// Long path, launch 3: the slice's taken positions in ascending order.
+__global__ void __launch_bounds__(kLongBS) topk_write_kernel(const float* __restrict__ scores,
+                                                             BatchArgs b, int K, int split,
+                                                             LongScratch ws, int32_t* idx) {
+  __shared__ int warp_sums[32];
+  const int t = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  const int pos = query_pos(b, t, nullptr);
+  const int len = pos + 1;
+  int32_t* out = idx + static_cast<int64_t>(t) * K;
+  if (len <= K) {  // every visible position, then -1 padding
+    if (c == 0)
+      for (int j = tid; j < K; j += kLongBS) out[j] = j < len ? j : -1;
+    return;
+  }
+  const int* cnt = ws.cnt + static_cast<int64_t>(t) * kCnt;
+  if (cnt[6] != 0) return;  // the fallback writes this row
+  int lo, hi;
+  slice_of(len, split, c, lo, hi);
+  if (lo >= hi) return;
+  const uint32_t T = static_cast<uint32_t>(cnt[4]);
+  const int pstar = cnt[5];
+  int base = ws.slice_off[static_cast<int64_t>(t) * split + c];
+  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
+  // in tiles of 4 * BS positions (lo is a multiple of 4, the row's capacity
+  // a multiple of 128, so a float4 read stays inside the row)
+#pragma unroll 1
+  for (int tile = lo; tile < hi; tile += 4 * kLongBS) {
+    const int s0 = tile + tid * 4;
+    bool take[4] = {false, false, false, false};
+    int n = 0;
+    if (s0 < hi) {
+      const float4 v = *reinterpret_cast<const float4*>(row + s0);
+      const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t k = order_key(x[q]);
+        take[q] = s0 + q < hi && (k > T || (k == T && s0 + q <= pstar));
+        n += take[q];
+      }
+    }
+    int tot;
+    int slot = base + block_excl_scan<kLongBS>(n, warp_sums, &tot);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (take[q]) {
+        if (slot < K) out[slot] = s0 + q;
+        ++slot;
+      }
+    base += tot;
+  }
+}
+
+// Rows beyond 16K positions: fewer than kRowsFew of them are spread over
+// several CTAs each (the launches above); more get a persistent CTA per SM,
+// a row at a time (measured on GB300: 64 decode rows of ~115K positions take
+// 47 us there against 64 us on the sliced path, whose five launches and
+// per-row resolve cost more than the idle SMs save; 4 rows of 1M take 50 us
+// sliced).
+constexpr int kRowsFew = 32;
 
 bool use_long_path(const dsa_batch_t& b) {
-  return b.num_q < kRowsMin && b.max_len > 16384;
+  return b.num_q < kRowsFew && b.max_len > 16384;
+}
+
+// Slices (CTAs) per row of the long path: about 4 waves of 152 SMs in all,
+// at least 8K positions each.
+int long_split(const dsa_batch_t& b) {
+  int split = static_cast<int>((4 * 152 + b.num_q - 1) / b.num_q);
+  return std::max(1, std::min(split, (b.max_len + 8191) / 8192));
 }
 
 size_t round256z(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Layout of the long path's scratch; *zeroed = bytes at its head to clear.
+LongScratch long_scratch(const dsa_batch_t& b, void* base_v, size_t* total, size_t* zeroed) {
+  const size_t q = static_cast<size_t>(b.num_q), sp = static_cast<size_t>(long_split(b));
+  uint8_t* base = static_cast<uint8_t*>(base_v);
+  LongScratch ws;
+  size_t off = 0;
+  ws.cnt = reinterpret_cast<int*>(base + off);
+  off += round256z(q * kCnt * 4);
+  if (zeroed) *zeroed = off;
+  ws.ckey = reinterpret_cast<uint32_t*>(base + off);
+  off += round256z(q * kCandCap * 4);
+  ws.cpos = reinterpret_cast<int32_t*>(base + off);
+  off += round256z(q * kCandCap * 4);
+  ws.slice_off = reinterpret_cast<int*>(base + off);
+  off += round256z(q * sp * 4);
+  if (total) *total = off;
+  return ws;
+}
 
 template <int CL, int BS, bool STAGE>
 cudaError_t launch_cl(const float* scores, const dsa_batch_t& b, int k, int32_t* idx, int* status,
@@ -984,7 +1092,7 @@ cudaError_t launch_cl(const float* scores, const dsa_batch_t& b, int k, int32_t*
 }
 
 cudaError_t launch_rows(const float* scores, const dsa_batch_t& b, int k, int32_t* idx, int* status,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const int* only = nullptr) {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -997,9 +1105,9 @@ cudaError_t launch_rows(const float* scores, const dsa_batch_t& b, int k, int32_
   int sms = 152;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = static_cast<int>(std::min<int64_t>(b.num_q, sms));
-  prof_begin(stream);
-  topk_rows_kernel<<<grid, kRowBS, kRowDynBytes, stream>>>(scores, to_args(b), k, idx, status);
-  prof_end(kLaunchTopk, stream);
+  if (!only) prof_begin(stream);
+  topk_rows_kernel<<<grid, kRowBS, kRowDynBytes, stream>>>(scores, to_args(b), k, idx, status, only);
+  if (!only) prof_end(kLaunchTopk, stream);
   count_launch(kLaunchTopk);
   return cudaGetLastError();
 }
@@ -1008,8 +1116,9 @@ cudaError_t launch_rows(const float* scores, const dsa_batch_t& b, int k, int32_
 
 size_t topk_scratch_bytes(const dsa_batch_t& b, int) {
   if (b.num_q == 0 || !use_long_path(b)) return 0;
-  const size_t q = static_cast<size_t>(b.num_q);
-  return round256z(q * kHBins * 4) + round256z(q * 16) + round256z(q * kCandCap * 4);
+  size_t total = 0;
+  long_scratch(b, nullptr, &total, nullptr);
+  return total;
 }
 
 cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_t* idx,
@@ -1017,46 +1126,50 @@ cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_
   if (b.num_q == 0) return cudaSuccess;
   if (use_long_path(b)) {
     if (!scratch || scratch_bytes < topk_scratch_bytes(b, k)) return cudaErrorInvalidValue;
-    const size_t q = static_cast<size_t>(b.num_q);
-    uint8_t* base = static_cast<uint8_t*>(scratch);
-    LongScratch ws;
-    ws.hist = reinterpret_cast<uint32_t*>(base);
-    ws.cnt = reinterpret_cast<int*>(base + round256z(q * kHBins * 4));
-    ws.cand = reinterpret_cast<int32_t*>(base + round256z(q * kHBins * 4) + round256z(q * 16));
-    cudaError_t e = cudaMemsetAsync(base, 0, round256z(q * kHBins * 4) + round256z(q * 16), stream);
+    size_t zeroed = 0;
+    const LongScratch ws = long_scratch(b, scratch, nullptr, &zeroed);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, zeroed, stream);
     if (e != cudaSuccess) return e;
-    // CTAs per row: about 4 waves of 152 SMs in all, at least 8K positions each
-    int split = static_cast<int>((4 * 152 + b.num_q - 1) / b.num_q);
-    split = max(1, min(split, (b.max_len + 8191) / 8192));
+    const int split = long_split(b);
+    if (split > 4096) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(split), static_cast<unsigned>(b.num_q));
     const BatchArgs a = to_args(b);
-    prof_begin(stream);
-    topk_hist_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws);
-    topk_select_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws, idx);
-    // dynamic shared memory: the candidate arrays, or the row's position
-    // bitmap when larger (up to 200 KB: with the static 8 KB, inside 227 KB)
-    const size_t bitmap_bytes = ((static_cast<size_t>(b.max_len) + 31) / 32) * 4;
-    const size_t fin_bytes = std::max<size_t>(kFinDynBytes, std::min<size_t>(bitmap_bytes, 200 << 10));
+    // resolve: the captured keys and positions, then one count per slice
+    const size_t res_bytes = (2 * static_cast<size_t>(kCandCap) + split) * 4;
     {
       static int configured_device = -1;
       int dev = 0;
       cudaGetDevice(&dev);
       if (configured_device != dev) {
-        e = cudaFuncSetAttribute(topk_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 200 << 10);
+        e = cudaFuncSetAttribute(topk_resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (2 * kCandCap + 4096) * 4);
         if (e != cudaSuccess) return e;
         configured_device = dev;
       }
     }
-    topk_finish_kernel<<<b.num_q, kFinBS, fin_bytes, stream>>>(scores, a, k, ws, idx, status,
-                                                                static_cast<int>(fin_bytes / 4));
+    {
+      static int configured_device = -1;
+      int dev = 0;
+      cudaGetDevice(&dev);
+      if (configured_device != dev) {
+        e = cudaFuncSetAttribute(topk_cutoff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kCutDynBytes);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+      }
+    }
+    prof_begin(stream);
+    topk_cutoff_kernel<<<b.num_q, kLongBS, kCutDynBytes, stream>>>(scores, a, k, ws);
+    topk_capture_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws);
+    topk_resolve_kernel<<<b.num_q, kFinBS, res_bytes, stream>>>(a, k, split, ws, status);
+    topk_write_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws, idx);
+    e = launch_rows(scores, b, k, idx, status, stream, ws.cnt);  // marked rows only
     prof_end(kLaunchTopk, stream);
-    count_launch(kLaunchTopk);
-    count_launch(kLaunchTopk);
-    count_launch(kLaunchTopk);
+    for (int i = 0; i < 4; ++i) count_launch(kLaunchTopk);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  // Rows beyond 16K positions (kRowsMin or more of them): one persistent CTA
+  // Rows beyond 16K positions (kRowsFew or more of them): one persistent CTA
   // per SM, a row at a time.  Many short rows (prefill): one CTA of 256
   // threads per row, its row re-read from L2 per pass.  Few short rows: a
   // cluster of 8 CTAs per row, each staging its slice in shared memory once.

@@ -205,8 +205,8 @@ DSA_API dsa_status_t dsa_indexer_scores(const void* q_idx, const float* q_scale,
  * -0.0 equals +0.0 (a tie, so the lower position wins); a NaN whose sign bit
  * is clear ranks above +inf and one whose sign bit is set below -inf.
  * ws: dsa_topk_workspace_size (the status
- * block, plus 48 KB of scratch per row for batches of fewer than 32 rows
- * longer than 16K positions).
+ * block, plus about 128 KB of scratch per row for batches of fewer than 32
+ * rows longer than 16K positions).
  */
 DSA_API size_t dsa_topk_workspace_size(const dsa_batch_t* b, int32_t k);
 DSA_API dsa_status_t dsa_topk(const float* scores, const dsa_batch_t* b, int32_t k, int32_t* idx,

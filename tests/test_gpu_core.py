@@ -92,10 +92,14 @@ def test_topk_bit_exact_short_rows(values):
 
 @pytest.mark.parametrize("values", ["ties", "gauss", "const", "signed_zeros"])
 def test_topk_bit_exact_long_rows(values):
-    # few rows beyond 16K positions: histogram / select / finish launches
-    # (constant and 7-valued rows overflow the candidate list and rescan)
+    # fewer than 32 rows beyond 16K positions: cutoff / capture / resolve /
+    # write launches (constant and 7-valued rows overflow the capture list
+    # and go to the fallback)
     _topk_case([40000, 70001, 131072], [1, 1, 1], 2048, values, 3)
     _topk_case([1 << 20, 300000], [1, 1], 2048, values, 4)
+    # 31 rows: the same path; 103 rows: one persistent CTA per SM
+    _topk_case([20000, 17000, 131072], [20, 8, 3], 2048, values, 7)
+    _topk_case([20000, 17000, 131072], [60, 40, 3], 2048, values, 8)
 
 
 @pytest.mark.parametrize("values", ["ties", "gauss", "const", "signed_zeros"])
