@@ -164,41 +164,54 @@ def kernel_bound(name, work, peaks, fp8, timed_s=0.0):
     return "hbm", peaks["hbm"], "GB/s", f"{peaks['src']} HBM copy"
 
 
-def kernel_records(prof, work, peaks, fp8, timed_s, c2c_gbs=None):
+def step_units(types, steps):
+    """Work units in the timed steps: an F layer for the indexer and the
+    top-K (whatever number of launches it takes: the select-only F layer of
+    long prefill rows is a sample, a capture and a resolve launch), a layer
+    for the sparse MLA."""
+    nf = types.count("F")
+    return {"indexer": nf * steps, "topk": nf * steps, "sparse_mla": len(types) * steps}
+
+
+def kernel_records(prof, work, peaks, fp8, timed_s, c2c_gbs=None, units=None):
     """Per-kernel roofline records from the library's live CUDA-event
-    profile of the timed steps."""
+    profile of the timed steps.  work[name] is the algorithmic work of one
+    unit: of one F layer / layer (units[name] of them were timed) where
+    units is given, else of one launch."""
     kernels = {}
+    units = units or {}
     for name in ("indexer", "topk", "sparse_mla", "append", "hot_plan", "hot_fetch"):
         if name not in work or name not in prof:
             continue
         ms, n = prof[name]
         if n == 0:
             continue
-        avg_s = ms / n / 1e3
+        u = units.get(name) or n
+        avg_s = ms / u / 1e3
         if name == "hot_fetch":  # reads over NVLink-C2C: against the measured host->device copy
             bound, peak, unit, src = "c2c", c2c_gbs, "GB/s", "measured host->device copy"
         else:
             bound, peak, unit, src = kernel_bound(name, work[name], peaks, fp8, timed_s)
         ach = (work[name]["flops"] / avg_s / 1e12) if bound == "tensor" else (
             work[name]["bytes"] / avg_s / 1e9)
-        kernels[name] = {"launches": n, "ms_per_launch": round(ms / n, 4), "share": None,
+        kernels[name] = {"launches": n, "ms_per_launch": round(ms / n, 4), "units": u,
+                         "ms_per_unit": round(ms / u, 4), "ms_total": round(ms, 4), "share": None,
                          "bound": bound, "achieved": round(ach, 2), "peak": peak, "unit": unit,
                          "frac": round(ach / peak, 4), "peak_src": src}
-    ktot = sum(v["ms_per_launch"] * v["launches"] for v in kernels.values())
+    ktot = sum(v["ms_total"] for v in kernels.values())
     for v in kernels.values():
-        v["share"] = round(v["ms_per_launch"] * v["launches"] / ktot, 4) if ktot else None
+        v["share"] = round(v["ms_total"] / ktot, 4) if ktot else None
     return kernels
 
 
 def scan_gather_record(kernels, work, peaks):
     """HBM-bound (decode) groups: the index scans and the sparse gathers of
-    the timed steps together, algorithmic bytes over their summed launch
-    times; None when either kernel is not HBM-bound."""
+    the timed steps together, algorithmic bytes over their summed times;
+    None when either kernel is not HBM-bound."""
     if not all(kernels.get(k, {}).get("bound") == "hbm" for k in ("indexer", "sparse_mla")):
         return None
-    byt = sum(work[k]["bytes"] * kernels[k]["launches"] for k in ("indexer", "sparse_mla"))
-    sec = sum(kernels[k]["ms_per_launch"] * kernels[k]["launches"] / 1e3
-              for k in ("indexer", "sparse_mla"))
+    byt = sum(work[k]["bytes"] * kernels[k]["units"] for k in ("indexer", "sparse_mla"))
+    sec = sum(kernels[k]["ms_total"] / 1e3 for k in ("indexer", "sparse_mla"))
     ach = byt / sec / 1e9
     return {"achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
             "frac": round(ach / peaks["hbm"], 4),
@@ -429,7 +442,8 @@ def measure_workload(dsa, name, args, dev, peaks, stream, flush):
     dsa.status_fetch(ws)
     total_ms = sum(times)
     work = algorithmic(lay, cfg, fp8)
-    kernels = kernel_records(prof, work, peaks, fp8, total_ms / 1e3)
+    kernels = kernel_records(prof, work, peaks, fp8, total_ms / 1e3,
+                             units=step_units(cfg["layers"], steps))
     rec = {"workload": DESCR[name], "value": round(lay.num_q * steps / (total_ms / 1e3), 1),
            "unit": UNIT, "steps": steps, "warmup": args.warmup,
            "ms_per_step": round(total_ms / steps, 4), "layers": cfg["layers"],
@@ -786,12 +800,13 @@ def main():
     if hot is not None:
         work.update(hot.work(args.steps, prof))
     kernels = kernel_records(prof, work, peaks, fp8, total_ms / 1e3,
-                             hot.c2c_gbs if hot is not None else None)
+                             hot.c2c_gbs if hot is not None else None,
+                             units=step_units(cfg["layers"], args.steps))
     scan_gather = scan_gather_record(kernels, work, peaks)
     # the dominant on-GPU kernel (the hot swap-in is bound by the host link and
     # reported in "hot")
     top = max((k for k in kernels if not k.startswith("hot_")),
-              key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"])
+              key=lambda k: kernels[k]["ms_total"])
     tk = kernels[top]
     traffic = None
     if top in NCU_TRAFFIC and NCU_TRAFFIC[top].get("src") == kernel_src_hash(KSRC[top]) and \

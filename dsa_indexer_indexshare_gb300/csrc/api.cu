@@ -183,11 +183,17 @@ struct GroupWs {
   size_t mla_extra_bytes;
 };
 
+// Top-K scratch of a group's F layers: the capture lists and samples of the
+// select-only path (rows beyond 16K positions), else the top-K's own.
+size_t group_topk_bytes(const dsa_group_t* g, const dsa_batch_t* b) {
+  return round256(use_select_only(*b, g->k) ? select_only_bytes(*b) : topk_scratch_bytes(*b, g->k));
+}
+
 GroupWs group_ws(const dsa_group_t* g, const dsa_batch_t* b, void* ws, size_t need) {
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   const size_t score_bytes = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4);
   return GroupWs{static_cast<int*>(ws), reinterpret_cast<float*>(wsb + kStatusBytes),
-                 wsb + kStatusBytes + score_bytes, round256(topk_scratch_bytes(*b, g->k)),
+                 wsb + kStatusBytes + score_bytes, group_topk_bytes(g, b),
                  wsb + kStatusBytes, need - kStatusBytes};
 }
 
@@ -195,6 +201,14 @@ GroupWs group_ws(const dsa_group_t* g, const dsa_batch_t* b, void* ws, size_t ne
 dsa_status_t run_f_layer(const dsa_group_t* g, const dsa_batch_t* b, int l, int32_t* idx_buf,
                          const GroupWs& w, cudaStream_t stream) {
   const bool fp8 = g->idx_dtype == DSA_FP8_E4M3;
+  // rows beyond 16K positions: select-only (no score matrix unless a row's
+  // sample misleads), else scores then top-K
+  if (use_select_only(*b, g->k))
+    return launch_status(
+        launch_indexer_topk_select(g->q_idx[l], fp8 ? g->q_scale[l] : nullptr, g->w[l], g->k_idx[l],
+                                   fp8 ? g->k_scale[l] : nullptr, g->k_rows, fp8, *b, g->k, idx_buf,
+                                   w.scores, w.topk_scratch, w.status, stream),
+        "select-only indexer / top-K launch");
   if (dsa_status_t s = launch_status(
           launch_indexer(g->q_idx[l], fp8 ? g->q_scale[l] : nullptr, g->w[l], g->k_idx[l],
                          fp8 ? g->k_scale[l] : nullptr, g->k_rows, fp8, *b, w.scores, false, w.status,
@@ -451,7 +465,7 @@ dsa_status_t dsa_sparse_mla_attn_fp8kv(const void* q_lat, const void* q_rope, co
 size_t dsa_group_workspace_size(const dsa_group_t* g, const dsa_batch_t* b) {
   if (!g || !b) return kStatusBytes;
   const size_t scores = round256(static_cast<size_t>(b->num_q) * static_cast<size_t>(b->max_len) * 4) +
-                        round256(topk_scratch_bytes(*b, g->k));
+                        group_topk_bytes(g, b);
   const size_t mla = round256(mla_workspace_bytes(*b, g->heads, g->k));
   return kStatusBytes + (scores > mla ? scores : mla);
 }

@@ -64,6 +64,16 @@ __device__ __forceinline__ int query_pos(const BatchArgs& b, int t, int* status)
   return p;
 }
 
+// Order-preserving image of an fp32 score: a > b as floats iff key(a) >
+// key(b) as unsigned integers.  -0.0 is first replaced by +0.0 so that the
+// two zeros are one value (equal scores, ties to the lower position); a NaN
+// with the sign bit clear ranks above +inf, one with it set below -inf.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  u = (u == 0x80000000u) ? 0u : u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // ------------------------------------------------------------- host helpers
 // Implemented in api.cu.
 // Record a message for dsa_last_error_string and return s.
@@ -92,6 +102,45 @@ cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float*
                            const void* k_idx, const float* k_scale, int64_t k_rows, bool fp8,
                            const dsa_batch_t& b, float* scores, bool fill_tail, int* status,
                            cudaStream_t stream);
+// Select-only F layer for rows longer than 16K positions: the indexer's
+// epilogue keeps, per query row, only the (key, position) pairs at or above
+// a cutoff taken from a sample of the row's scores, and the top-K is resolved
+// from those lists, so that no score matrix is written (rows whose sample
+// misled fall back to the score matrix and the exact top-K).
+constexpr int kTopkCnt = 8;          // per-row words: 0 key chunks of the capture, 1 captured,
+                                     // 2 dropped, 3 cutoff (fp32 bits), 4 T, 5 pstar, 6 fallback,
+                                     // 7 sampled positions
+constexpr int kTopkCandCap = 16384;  // captured keys kept per row
+constexpr int kSampleTilesMax = 64;  // 128-key tiles sampled per row at most
+constexpr int kSegMax = 256;         // key chunks of a row at most (its list is split evenly,
+                                     // each chunk's segment again in 4 quarters)
+constexpr int kSampleChunk = 8;      // sampled tiles per CTA of the sample pass
+struct TopkLists {
+  int* cnt;        // [num_q][kTopkCnt]
+  uint32_t* ckey;  // [num_q][kTopkCandCap] captured order keys: quarter q of segment c of a
+                   // row (the keys of key chunk c in TMEM lane quarter q) at
+                   // (4c + q) * (kTopkCandCap / (4 chunks))
+  int32_t* cpos;   // [num_q][kTopkCandCap] their positions
+  int* segcnt;     // [num_q][kSegMax][4] keys each quarter found at or above the cutoff
+  float* sample;   // [num_q][kSampleTilesMax * 128] sampled scores
+};
+enum IndexerMode { kIdxScores = 0, kIdxSample = 1, kIdxCapture = 2 };
+bool use_select_only(const dsa_batch_t& b, int k);
+size_t select_only_bytes(const dsa_batch_t& b);
+TopkLists select_only_lists(const dsa_batch_t& b, void* base);
+// mode kIdxScores: scores (rows of blocks holding a row flagged in `only`
+// when only != nullptr); kIdxSample / kIdxCapture: the lists' sample / capture
+cudaError_t launch_indexer_mode(const void* q_idx, const float* q_scale, const float* w,
+                                const void* k_idx, const float* k_scale, int64_t k_rows, bool fp8,
+                                const dsa_batch_t& b, int mode, float* scores, const int* only,
+                                const TopkLists& lists, int* status, cudaStream_t stream);
+// the whole select-only F layer: sample, cutoff, capture, resolve and write,
+// then the fallback rows through the score matrix (scores: [num_q][max_len])
+cudaError_t launch_indexer_topk_select(const void* q_idx, const float* q_scale, const float* w,
+                                       const void* k_idx, const float* k_scale, int64_t k_rows,
+                                       bool fp8, const dsa_batch_t& b, int k, int32_t* idx,
+                                       float* scores, void* lists_base, int* status,
+                                       cudaStream_t stream);
 size_t topk_scratch_bytes(const dsa_batch_t& b, int k);
 cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_t* idx,
                         int* status, void* scratch, size_t scratch_bytes, cudaStream_t stream);

@@ -16,6 +16,7 @@
 // decode), then one TMA producer warp and one MMA issuer warp (TMEM owner).  The key tiles
 // stream through a STAGES-deep shared-memory ring; the accumulator is double
 // buffered in TMEM so the epilogue of tile i overlaps the MMAs of tile i+1.
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
@@ -23,7 +24,7 @@
 namespace dsa {
 namespace {
 
-template <int NTOK, bool FP8, int STAGES>
+template <int NTOK, bool FP8, int STAGES, int MODE>
 struct IdxCfg {
   static constexpr int N = NTOK * 32;                // MMA N: (token, head) pairs
   // epilogue warps: two per TMEM lane quarter (each takes half of the tokens)
@@ -62,6 +63,9 @@ struct IndexerParams {
   int num_qb;      // query blocks per sequence
   int fill_tail;   // write -inf beyond the computed blocks
   uint64_t timeout_ns;
+  const int* only;  // scores mode: only blocks holding a row flagged here (word 6 of kTopkCnt)
+  int whole_rows;   // one CTA per query block over all its keys
+  TopkLists lists;  // sample / capture modes
 };
 
 // Wait until the tcgen05.ld results in v are valid; the asm takes v as
@@ -78,11 +82,11 @@ __device__ __forceinline__ void tmem_wait_ld_dep(float (&v)[32]) {
                : "memory");
 }
 
-template <int NTOK, bool FP8, int STAGES>
-__global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
+template <int NTOK, bool FP8, int STAGES, int MODE>
+__global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES, MODE>::NT, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap, const IndexerParams p) {
-  using C = IdxCfg<NTOK, FP8, STAGES>;
+  using C = IdxCfg<NTOK, FP8, STAGES, MODE>;
   constexpr int W_PROD = C::NEPI, W_MMA = C::NEPI + 1, NEPT = C::NEPI * 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -105,11 +109,40 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
     pos[n] = n < nq ? query_pos(p.b, q0 + n, tid == 0 ? p.status : nullptr) : -1;
     pmax = max(pmax, pos[n]);
   }
-  const int s_begin = kc * p.kc_blocks * 128;
+  if constexpr (MODE == kIdxScores) {
+    if (p.only) {  // the fallback rows of a select-only F layer
+      bool any = false;
+      for (int n = 0; n < nq; ++n) any |= p.only[static_cast<int64_t>(q0 + n) * kTopkCnt + 6] != 0;
+      if (!any) return;
+    }
+  }
+  // key tiles: the chunk's consecutive tiles, or (sample mode) ns tiles
+  // spread evenly over the T tiles that cover [0, pmax], all of them when
+  // T <= ns
+  // (sample mode: CTA kc takes sampled tiles kc * kSampleChunk ..)
+  const int s_begin = MODE == kIdxSample ? 0 : kc * p.kc_blocks * 128;
   if (s_begin >= p.b.max_len) return;
   const int s_stop = min(s_begin + p.kc_blocks * 128, p.b.max_len);
-  const int nkb = pmax < s_begin ? 0 : min(p.kc_blocks, (pmax - s_begin) / 128 + 1);
-  if (p.fill_tail) {
+  const int T = pmax < 0 ? 0 : pmax / 128 + 1;
+  const int ns = min(max(32, T / 64), kSampleTilesMax);
+  const int i0 = MODE == kIdxSample ? kc * kSampleChunk : 0;  // first sampled tile of this CTA
+  int nkb;
+  if constexpr (MODE == kIdxSample) {
+    const int total = min(T, ns);
+    if (kc == 0 && tid < nq) p.lists.cnt[static_cast<int64_t>(q0 + tid) * kTopkCnt + 7] = total * 128;
+    nkb = max(0, min(kSampleChunk, total - i0));
+  } else {
+    nkb = pmax < s_begin ? 0 : min(p.kc_blocks, (pmax - s_begin) / 128 + 1);
+  }
+  auto tile_start = [&](int i) -> int {
+    if constexpr (MODE == kIdxSample) {
+      const int g = i0 + i;
+      return (T <= ns ? g : static_cast<int>(static_cast<int64_t>(g) * T / ns)) * 128;
+    } else {
+      return s_begin + i * 128;
+    }
+  };
+  if (MODE == kIdxScores && p.fill_tail) {
     const int f0 = s_begin + nkb * 128;
     const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     for (int n = 0; n < nq; ++n) {
@@ -188,7 +221,7 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
         mbar_arrive_expect_tx(bar(B_KFULL + st), C::K_BYTES);
         // first cache row of the tile (a tile never straddles a cache block);
         // an unmapped block loads as zeros (tile fully outside the map)
-        const int64_t ty = cache_row(p.b, seq, row0, s_begin + i * 128);
+        const int64_t ty = cache_row(p.b, seq, row0, tile_start(i));
         if (ty < 0) atomicOr(p.status, DSA_DEVERR_INDEX);
         const int y = ty < 0 ? -128 : static_cast<int>(ty);
 #pragma unroll
@@ -243,15 +276,35 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
     // latency overlaps the previous tile instead of following the MMA
     auto load_kscale = [&](int i) -> float {
       if (!FP8 || i >= nkb) return 1.f;
-      const int64_t kr = cache_row(p.b, seq, row0, s_begin + i * 128 + quarter * 32 + lane);
+      const int64_t kr = cache_row(p.b, seq, row0, tile_start(i) + quarter * 32 + lane);
       return (kr >= 0 && kr < p.k_rows) ? __ldg(&p.k_scale[kr]) : 0.f;
     };
+    // capture mode: the rows' cutoffs; this CTA (key chunk kc) owns segment
+    // kc of each row's list, and this warp (TMEM lane quarter q) quarter q
+    // of it, placing its keys with a warp-uniform count (no atomics)
+    const int segq = kTopkCandCap / (4 * p.num_kc);
+    float cf[C::TOK_PER_WARP];
+    int wc[C::TOK_PER_WARP];
+    uint32_t* ck[C::TOK_PER_WARP];  // this warp's quarter segment of each token's list
+    int32_t* cp[C::TOK_PER_WARP];
+#pragma unroll
+    for (int nn = 0; nn < C::TOK_PER_WARP; ++nn) {
+      const int n = n0 + nn;
+      cf[nn] = (MODE == kIdxCapture && n < nq)
+                   ? __int_as_float(p.lists.cnt[static_cast<int64_t>(q0 + n) * kTopkCnt + 3])
+                   : INFINITY;
+      wc[nn] = 0;
+      const int64_t base = static_cast<int64_t>(q0 + n) * kTopkCandCap + (4 * kc + quarter) * segq;
+      ck[nn] = p.lists.ckey + base;
+      cp[nn] = p.lists.cpos + base;
+    }
+    const uint32_t lt = (1u << lane) - 1u;
     float kscale_next = load_kscale(0);
     for (int i = 0; i < nkb; ++i) {
       const int acc = i & 1;
       if (!mbar_wait(bar(B_ACCF + acc), (i >> 1) & 1, abort_flag, p.status, to)) break;
       tc_fence_after();
-      const int s = s_begin + i * 128 + quarter * 32 + lane;
+      const int s = tile_start(i) + quarter * 32 + lane;
       const float kscale = kscale_next;
       kscale_next = load_kscale(i + 1);
 #pragma unroll
@@ -277,12 +330,42 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
           }
           float sc = (a0 + a1) + (a2 + a3);
           if (FP8) sc *= kscale;
-          if (s > pn) sc = -INFINITY;
-          p.scores[static_cast<int64_t>(q0 + n) * p.b.max_len + s] = sc;
+          if constexpr (MODE == kIdxScores) {
+            if (s > pn) sc = -INFINITY;
+            p.scores[static_cast<int64_t>(q0 + n) * p.b.max_len + s] = sc;
+          } else if constexpr (MODE == kIdxSample) {
+            if (s > pn) sc = -INFINITY;
+            p.lists.sample[static_cast<int64_t>(q0 + n) * (kSampleTilesMax * 128) + (i0 + i) * 128 +
+                           quarter * 32 + lane] = sc;
+          } else {
+            // keys at or above the row's cutoff (a float compare: NaN kept
+            // too; a superset is harmless)
+            const bool take = s <= pn && !(sc < cf[nn]);
+            const uint32_t m = __ballot_sync(0xffffffffu, take);
+            const int j = wc[nn] + __popc(m & lt);
+            if (take && j < segq) {
+              ck[nn][j] = order_key(sc);
+              cp[nn][j] = s;
+            }
+            wc[nn] += __popc(m);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(bar(B_ACCE + acc));
+    }
+    if constexpr (MODE == kIdxCapture) {
+      // this quarter's counts (a count above the quarter segment sends the
+      // row to the fallback)
+#pragma unroll
+      for (int nn = 0; nn < C::TOK_PER_WARP; ++nn) {
+        const int n = n0 + nn;
+        if (lane == 0 && n < nq) {
+          const int64_t r = q0 + n;
+          p.lists.segcnt[(r * kSegMax + kc) * 4 + quarter] = wc[nn];
+          if (kc == 0 && quarter == 0) p.lists.cnt[r * kTopkCnt + 0] = p.num_kc;
+        }
+      }
     }
   }
   tc_fence_before();
@@ -293,11 +376,11 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES>::NT, 1)
   }
 }
 
-template <int NTOK, bool FP8, int STAGES>
+template <int NTOK, bool FP8, int STAGES, int MODE>
 cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, IndexerParams p,
                        cudaStream_t stream) {
-  using C = IdxCfg<NTOK, FP8, STAGES>;
-  auto* kern = indexer_kernel<NTOK, FP8, STAGES>;
+  using C = IdxCfg<NTOK, FP8, STAGES, MODE>;
+  auto* kern = indexer_kernel<NTOK, FP8, STAGES, MODE>;
   static int configured_device = -1;  // attribute is per device
   static int slots = 0;               // resident CTAs on the whole GPU
   int dev = 0;
@@ -312,7 +395,9 @@ cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, Indexer
     slots = sms * (per_sm > 0 ? per_sm : 1);
     configured_device = dev;
   }
-  if (NTOK == 1) {
+  if (p.whole_rows) {
+    p.kc_blocks = (p.b.max_len + 127) / 128;
+  } else if (NTOK == 1) {
     // decode: tiles per CTA chosen so that the CTAs fill whole waves of the
     // resident slots, weighing each CTA's start (barriers, TMEM, Q, first
     // tile) as about four tiles of streaming: min over kc of
@@ -320,7 +405,8 @@ cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, Indexer
     const int64_t tiles = (p.b.max_len + 127) / 128;
     int best = 32;
     int64_t best_cost = INT64_MAX;
-    for (int kc = 16; kc <= 128; ++kc) {
+    // (at most kSegMax chunks per row: the capture splits a row's list by chunk)
+    for (int kc = std::max<int64_t>(16, (tiles + kSegMax - 1) / kSegMax); kc <= 128; ++kc) {
       const int64_t ctas = static_cast<int64_t>(p.b.num_seqs) * ((tiles + kc - 1) / kc);
       const int64_t cost = ((ctas + slots - 1) / slots) * (kc + 4);
       if (cost < best_cost || (cost == best_cost && kc == 32)) {
@@ -331,7 +417,14 @@ cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, Indexer
     p.kc_blocks = best;
   }
   p.num_qb = (p.b.max_q + NTOK - 1) / NTOK;
-  p.num_kc = (p.b.max_len + p.kc_blocks * 128 - 1) / (p.kc_blocks * 128);
+  if (MODE == kIdxSample) {
+    // sampled tiles of the longest row (the same rule as in the kernel)
+    const int tiles = (p.b.max_len + 127) / 128;
+    const int ns = std::min(std::max(32, tiles / 64), kSampleTilesMax);
+    p.num_kc = (std::min(tiles, ns) + kSampleChunk - 1) / kSampleChunk;
+  } else {
+    p.num_kc = (p.b.max_len + p.kc_blocks * 128 - 1) / (p.kc_blocks * 128);
+  }
   dim3 grid(static_cast<unsigned>(p.num_qb) * static_cast<unsigned>(p.num_kc),
             static_cast<unsigned>(p.b.num_seqs));
   prof_begin(stream);
@@ -341,7 +434,52 @@ cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, Indexer
   return cudaGetLastError();
 }
 
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& qmap, const CUtensorMap& kmap, const IndexerParams& p,
+                        bool decode, bool fp8, cudaStream_t stream) {
+  if (decode)
+    return fp8 ? launch_one<1, true, 6, MODE>(qmap, kmap, p, stream)
+               : launch_one<1, false, 3, MODE>(qmap, kmap, p, stream);
+  return fp8 ? launch_one<8, true, 6, MODE>(qmap, kmap, p, stream)
+             : launch_one<8, false, 4, MODE>(qmap, kmap, p, stream);
+}
+
 }  // namespace
+
+cudaError_t launch_indexer_mode(const void* q_idx, const float* q_scale, const float* w,
+                                const void* k_idx, const float* k_scale, int64_t k_rows, bool fp8,
+                                const dsa_batch_t& b, int mode, float* scores, const int* only,
+                                const TopkLists& lists, int* status, cudaStream_t stream) {
+  if (b.num_q == 0) return cudaSuccess;
+  const bool decode = b.max_q <= 1;
+  const int ntok = decode ? 1 : 8;
+  const auto dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int es = fp8 ? 1 : 2;
+  const uint32_t box_inner = fp8 ? 128 : 64;
+  CUtensorMap qmap, kmap;
+  if (!make_tmap_2d(&qmap, q_idx, dt, es, 128, static_cast<uint64_t>(b.num_q) * 32, box_inner,
+                    ntok * 32))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&kmap, k_idx, dt, es, 128, static_cast<uint64_t>(k_rows), box_inner, 128))
+    return cudaErrorInvalidValue;
+  IndexerParams p{};
+  p.b = to_args(b);
+  p.w = w;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.k_rows = k_rows;
+  p.scores = scores;
+  p.status = status;
+  p.kc_blocks = 64;  // 128-key tiles per CTA (one Q load per 8K keys); decode: see launch_one
+  p.fill_tail = 0;
+  p.timeout_ns = wait_timeout_ns();
+  p.only = only;
+  p.whole_rows = only ? 1 : 0;  // the fallback: few rows, normally none
+  p.lists = lists;
+  if (mode == kIdxSample) return launch_mode<kIdxSample>(qmap, kmap, p, decode, fp8, stream);
+  if (mode == kIdxCapture) return launch_mode<kIdxCapture>(qmap, kmap, p, decode, fp8, stream);
+  return launch_mode<kIdxScores>(qmap, kmap, p, decode, fp8, stream);
+}
 
 cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float* w,
                            const void* k_idx, const float* k_scale, int64_t k_rows, bool fp8,
@@ -370,11 +508,7 @@ cudaError_t launch_indexer(const void* q_idx, const float* q_scale, const float*
   p.kc_blocks = 64;  // 128-key tiles per CTA (one Q load per 8K keys); decode: see launch_one
   p.fill_tail = fill_tail ? 1 : 0;
   p.timeout_ns = wait_timeout_ns();
-  if (decode)
-    return fp8 ? launch_one<1, true, 6>(qmap, kmap, p, stream)
-               : launch_one<1, false, 3>(qmap, kmap, p, stream);
-  return fp8 ? launch_one<8, true, 6>(qmap, kmap, p, stream)
-             : launch_one<8, false, 4>(qmap, kmap, p, stream);
+  return launch_mode<kIdxScores>(qmap, kmap, p, decode, fp8, stream);
 }
 
 }  // namespace dsa

@@ -27,16 +27,6 @@ namespace {
 constexpr int kStageMax = 18432;                 // positions staged per CTA
 constexpr int kStageBytesMax = kStageMax * 4;    // 72 KB of shared memory
 
-// Order-preserving image of an fp32 score: a > b as floats iff key(a) >
-// key(b) as unsigned integers.  -0.0 is first replaced by +0.0 so that the
-// two zeros are one value (equal scores, ties to the lower position); a NaN
-// with the sign bit clear ranks above +inf, one with it set below -inf.
-__device__ __forceinline__ uint32_t order_key(float x) {
-  uint32_t u = __float_as_uint(x);
-  u = (u == 0x80000000u) ? 0u : u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 // Exclusive prefix sum over the CTA in thread order; *total gets the sum.
 template <int BS>
 __device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int* total) {
@@ -259,12 +249,12 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
 //              read in full, histogrammed, resolved exactly).
 constexpr int kHBits = 12;
 constexpr int kHBins = 1 << kHBits;   // 4096 bins over key bits [31:20]
-constexpr int kCandCap = 16384;       // captured keys kept per row
+constexpr int kCandCap = kTopkCandCap;  // captured keys kept per row
 constexpr int kLongSlack = 16;        // sampled keys added to the cutoff's 1.5x share of K
 constexpr int kLongBS = 512;
 constexpr int kFinBS = 512;
 constexpr int kCapSeg = 192;          // captured keys buffered per warp of a capture CTA
-constexpr int kCnt = 8;  // per-row words: 1 captured, 2 dropped, 3 cutoff, 4 T, 5 pstar, 6 fallback
+constexpr int kCnt = kTopkCnt;  // per-row words: 1 captured, 2 dropped, 3 cutoff, 4 T, 5 pstar, 6 fallback
 
 struct LongScratch {
   int* cnt;          // [num_q][kCnt]
@@ -1112,7 +1102,278 @@ cudaError_t launch_rows(const float* scores, const dsa_batch_t& b, int k, int32_
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ select-only F layer
+// The indexer's sample mode leaves, per row, the scores of up to
+// kSampleTilesMax 128-key tiles spread over the row (-inf at positions
+// beyond the row) and their count in word 7.  The cutoff is the exact value
+// of the need-th largest sample, need about 1.5 times the sample's share of
+// K (plus kLongSlack): a 12-bit histogram gives its bin, two 10-bit passes
+// over that bin's members the rest of its key (a bin edge would keep up to
+// a bin's width more keys).  +inf for rows that keep every position, -inf
+// when the sample holds fewer than need values.
+__global__ void __launch_bounds__(kLongBS) topk_sample_cutoff_kernel(BatchArgs b, int K,
+                                                                     TopkLists ls) {
+  extern __shared__ uint32_t cut_dyn[];  // [kCutCopies][kHBins]
+  __shared__ int hist2[1024];
+  __shared__ int warp_sums[32];
+  __shared__ int s_cut, s_tmp, s_valid, s_d, s_above;
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int pos = query_pos(b, t, nullptr);
+  const int len = pos + 1;
+  int* cnt = ls.cnt + static_cast<int64_t>(t) * kTopkCnt;
+  if (len <= K) {
+    if (tid == 0) cnt[3] = __float_as_int(INFINITY);
+    return;
+  }
+  for (int i = tid; i < kCutCopies * kHBins; i += kLongBS) cut_dyn[i] = 0;
+  if (tid == 0) {
+    s_cut = 0;
+    s_valid = 0;
+  }
+  __syncthreads();
+  uint32_t* h = cut_dyn + (tid & (kCutCopies - 1)) * kHBins;
+  const float* row = ls.sample + static_cast<int64_t>(t) * (kSampleTilesMax * 128);
+  const int ns = min(cnt[7], kSampleTilesMax * 128);
+  // order key of sample i, ~0 for a sampled position beyond the row (-inf)
+  auto get = [&](int i) -> uint32_t {
+    const float x = row[i];
+    return x == -INFINITY ? ~0u : order_key(x);
+  };
+  int mine = 0;
+  for (int v = tid; v < ns; v += kLongBS) {
+    const uint32_t k = get(v);
+    if (k != ~0u) {
+      atomicAdd(&h[k >> 20], 1u);
+      ++mine;
+    }
+  }
+  atomicAdd(&s_valid, mine);
+  __syncthreads();
+  for (int i = tid; i < kHBins; i += kLongBS) {
+    uint32_t sum = 0;
+#pragma unroll
+    for (int c = 0; c < kCutCopies; ++c) sum += cut_dyn[c * kHBins + i];
+    cut_dyn[i] = sum;
+  }
+  __syncthreads();
+  const int need_p =
+      static_cast<int>(3 * static_cast<int64_t>(K) * s_valid / (2 * static_cast<int64_t>(len))) +
+      kLongSlack;
+  if (need_p > s_valid) {  // too few samples: keep everything (the fallback resolves the row)
+    if (tid == 0) cnt[3] = __float_as_int(-INFINITY);
+    return;
+  }
+  threshold_bin<kLongBS>(cut_dyn, need_p, warp_sums, &s_cut, &s_tmp);
+  uint32_t T;
+  int rest;
+  select_low_bits<kLongBS>(ns, need_p - s_tmp, get, static_cast<uint32_t>(s_cut), hist2, warp_sums,
+                           &s_d, &s_above, &T, &rest);
+  if (tid == 0) {
+    // the float of key T (the inverse of order_key)
+    const float cf = __uint_as_float((T & 0x80000000u) ? (T & 0x7fffffffu) : ~T);
+    cnt[3] = __float_as_int(cf);
+  }
+}
+
+// One CTA per row: the row's capture list gathered from its key chunks'
+// segments, the threshold key T and tie cut pstar from it (as the long
+// path's resolve), then the taken positions (key > T, or key == T at a
+// position up to pstar: exactly K of them) sorted ascending into the output.
+// A row without the guarantee (too few keys captured, or a chunk with more
+// keys than its segment or the list more than kResCap) is marked for the
+// fallback (word 6).
+constexpr int kResCap = 8192;
+__global__ void __launch_bounds__(kFinBS) topk_list_resolve_write_kernel(BatchArgs b, int K,
+                                                                         TopkLists ls,
+                                                                         int32_t* idx,
+                                                                         int* status) {
+  __shared__ int hist2[2048];
+  __shared__ uint32_t h[kHBins];
+  __shared__ int warp_sums[32];
+  __shared__ int s_d, s_above, s_n, s_b1, s_nabove, s_taken, s_over;
+  __shared__ int s_segoff[4 * kSegMax];
+  extern __shared__ uint32_t res_dyn[];  // gathered keys and positions, then the taken positions
+  uint32_t* ckey = res_dyn;
+  int32_t* cpos = reinterpret_cast<int32_t*>(res_dyn + kResCap);
+  int32_t* taken = reinterpret_cast<int32_t*>(res_dyn + 2 * kResCap);
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int pos = query_pos(b, t, tid == 0 ? status : nullptr);
+  const int len = pos + 1;
+  int32_t* out = idx + static_cast<int64_t>(t) * K;
+  if (len <= K) {  // every visible position, then -1 padding
+    for (int j = tid; j < K; j += kFinBS) out[j] = j < len ? j : -1;
+    return;
+  }
+  int* cnt = ls.cnt + static_cast<int64_t>(t) * kTopkCnt;
+  const int nkc = cnt[0];
+  const int ncell = 4 * nkc;  // (key chunk, TMEM lane quarter) cells of the list
+  const int segq = nkc > 0 ? kTopkCandCap / ncell : 0;
+  const int* segcnt = ls.segcnt + static_cast<int64_t>(t) * kSegMax * 4;
+  // cell offsets in the gathered list (thread tid owns cells tid*per ..)
+  if (tid == 0) s_over = (nkc <= 0 || nkc > kSegMax) ? 1 : 0;
+  __syncthreads();
+  constexpr int per = 4 * kSegMax / kFinBS;
+  int c_[per];
+  int local = 0;
+#pragma unroll
+  for (int k2 = 0; k2 < per; ++k2) {
+    const int c = tid * per + k2;
+    const int v = c < ncell ? segcnt[c] : 0;
+    if (v > segq) s_over = 1;
+    c_[k2] = min(v, segq);
+    local += c_[k2];
+  }
+  int n;
+  int run = block_excl_scan<kFinBS>(local, warp_sums, &n);
+#pragma unroll
+  for (int k2 = 0; k2 < per; ++k2) {
+    s_segoff[tid * per + k2] = run;
+    run += c_[k2];
+  }
+  __syncthreads();
+  if (s_over || n < K || n > kResCap) {  // no guarantee: the fallback takes the row
+    if (tid == 0) cnt[6] = 1;
+    return;
+  }
+  // gather: warp w copies cells w, w + warps, ... (each cell's entries are contiguous)
+  {
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int c = warp; c < ncell; c += kFinBS / 32) {
+      const int m = min(segcnt[c], segq), o = s_segoff[c];
+      const int64_t src = static_cast<int64_t>(t) * kTopkCandCap + static_cast<int64_t>(c) * segq;
+      for (int j = lane; j < m; j += 32) {
+        ckey[o + j] = ls.ckey[src + j];
+        cpos[o + j] = ls.cpos[src + j];
+      }
+    }
+  }
+  for (int i = tid; i < kHBins; i += kFinBS) h[i] = 0;
+  if (tid == 0) s_taken = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kFinBS) atomicAdd(&h[ckey[i] >> 20], 1u);
+  __syncthreads();
+  threshold_bin<kFinBS>(h, K, warp_sums, &s_b1, &s_nabove);
+  const uint32_t b1 = static_cast<uint32_t>(s_b1);
+  auto get_key = [&](int i) -> uint32_t { return (ckey[i] >> 20) == b1 ? ckey[i] : ~0u; };
+  auto get_pos = [&](int i) -> int { return cpos[i]; };
+  uint32_t T;
+  int need;
+  select_low_bits<kFinBS>(n, K - s_nabove, get_key, b1, hist2, warp_sums, &s_d, &s_above, &T,
+                          &need);
+  const int pstar = tied_position_cut<kFinBS>(n, need, T, get_key, get_pos, hist2, warp_sums, &s_d,
+                                              &s_above, &s_n);
+  for (int i = tid; i < n; i += kFinBS) {
+    const uint32_t k = ckey[i];
+    if (k > T || (k == T && cpos[i] <= pstar)) {
+      const int j = atomicAdd(&s_taken, 1);
+      if (j < K) taken[j] = cpos[i];
+    }
+  }
+  __syncthreads();
+  if (len <= kResCap * 32) {
+    // ascending order through a bitmap over the row (in the key area, free now)
+    uint32_t* bits = ckey;
+    const int nwords = (len + 31) >> 5;
+    for (int i = tid; i < nwords; i += kFinBS) bits[i] = 0;
+    __syncthreads();
+    for (int j = tid; j < min(s_taken, K); j += kFinBS)
+      atomicOr(&bits[taken[j] >> 5], 1u << (taken[j] & 31));
+    __syncthreads();
+    bitmap_compact<kFinBS>(bits, nwords, K, out, warp_sums, status);
+  } else {
+    if (tid == 0 && s_taken != K) atomicOr(status, DSA_DEVERR_BATCH);
+    sort_positions<kFinBS>(taken, K);
+    for (int j = tid; j < K; j += kFinBS) out[j] = taken[j];
+  }
+}
+
 }  // namespace
+
+// Rows beyond 16K positions (and at most 2M, so that a row has at most
+// kSegMax key chunks of the capture), prefill and chunked prefill only: for
+// a decode batch (one query per sequence) the sample, cutoff and resolve
+// launches cost more than the top-K over the score matrix they replace.
+bool use_select_only(const dsa_batch_t& b, int) {
+  return b.num_q > 0 && b.max_q > 1 && b.max_len > 16384 && b.max_len <= kSegMax * 64 * 128;
+}
+static_assert(kSegMax * 64 * 128 <= (1 << 21), "rows of the select-only path: at most 2M positions");
+
+size_t select_only_bytes(const dsa_batch_t& b) {
+  const size_t q = static_cast<size_t>(b.num_q);
+  return round256z(q * kTopkCnt * 4) + 2 * round256z(q * kTopkCandCap * 4) +
+         round256z(q * kSegMax * 4 * 4) + round256z(q * kSampleTilesMax * 128 * 4);
+}
+
+TopkLists select_only_lists(const dsa_batch_t& b, void* base_v) {
+  const size_t q = static_cast<size_t>(b.num_q);
+  uint8_t* base = static_cast<uint8_t*>(base_v);
+  TopkLists ls;
+  size_t off = 0;
+  ls.cnt = reinterpret_cast<int*>(base + off);
+  off += round256z(q * kTopkCnt * 4);
+  ls.ckey = reinterpret_cast<uint32_t*>(base + off);
+  off += round256z(q * kTopkCandCap * 4);
+  ls.cpos = reinterpret_cast<int32_t*>(base + off);
+  off += round256z(q * kTopkCandCap * 4);
+  ls.segcnt = reinterpret_cast<int*>(base + off);
+  off += round256z(q * kSegMax * 4 * 4);
+  ls.sample = reinterpret_cast<float*>(base + off);
+  return ls;
+}
+
+cudaError_t launch_indexer_topk_select(const void* q_idx, const float* q_scale, const float* w,
+                                       const void* k_idx, const float* k_scale, int64_t k_rows,
+                                       bool fp8, const dsa_batch_t& b, int k, int32_t* idx,
+                                       float* scores, void* lists_base, int* status,
+                                       cudaStream_t stream) {
+  if (b.num_q == 0) return cudaSuccess;
+  const TopkLists ls = select_only_lists(b, lists_base);
+  cudaError_t e = cudaMemsetAsync(ls.cnt, 0, static_cast<size_t>(b.num_q) * kTopkCnt * 4, stream);
+  if (e != cudaSuccess) return e;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(topk_sample_cutoff_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCutDynBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(topk_list_resolve_write_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (2 * kResCap + 4096) * 4);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const BatchArgs a = to_args(b);
+  // 1. sampled scores, 2. the rows' cutoffs, 3. the capture lists
+  e = launch_indexer_mode(q_idx, q_scale, w, k_idx, k_scale, k_rows, fp8, b, kIdxSample, nullptr,
+                          nullptr, ls, status, stream);
+  if (e != cudaSuccess) return e;
+  prof_begin(stream);
+  topk_sample_cutoff_kernel<<<b.num_q, kLongBS, kCutDynBytes, stream>>>(a, k, ls);
+  prof_end(kLaunchTopk, stream);
+  count_launch(kLaunchTopk);
+  e = cudaMemsetAsync(ls.segcnt, 0, static_cast<size_t>(b.num_q) * kSegMax * 4 * 4, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_indexer_mode(q_idx, q_scale, w, k_idx, k_scale, k_rows, fp8, b, kIdxCapture, nullptr,
+                          nullptr, ls, status, stream);
+  if (e != cudaSuccess) return e;
+  // 4. exact selection from the lists, written in ascending order
+  int pw = 1;
+  while (pw < k) pw <<= 1;
+  prof_begin(stream);
+  topk_list_resolve_write_kernel<<<b.num_q, kFinBS, (2 * static_cast<size_t>(kResCap) + pw) * 4,
+                                   stream>>>(a, k, ls, idx, status);
+  prof_end(kLaunchTopk, stream);
+  count_launch(kLaunchTopk);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // 5. rows marked for the fallback (normally none): their scores, then the
+  // exact many-long-rows top-K on those rows only
+  e = launch_indexer_mode(q_idx, q_scale, w, k_idx, k_scale, k_rows, fp8, b, kIdxScores, scores,
+                          ls.cnt, ls, status, stream);
+  if (e != cudaSuccess) return e;
+  return launch_rows(scores, b, k, idx, status, stream, ls.cnt);
+}
 
 size_t topk_scratch_bytes(const dsa_batch_t& b, int) {
   if (b.num_q == 0 || !use_long_path(b)) return 0;

@@ -254,6 +254,14 @@ DSA_API dsa_status_t dsa_sparse_mla_attn(const void* q_lat, const void* q_rope, 
  * idx_buf: int32 [num_q, k], caller-owned; after the call it holds the
  * indices of the last F layer.  The workspace holds the status block and the
  * fp32 score matrix; size from dsa_group_workspace_size.
+ * For a prefill (some sequence with more than one query) whose rows exceed
+ * 16K positions (up to 2M), an F layer selects without writing the score
+ * matrix ("GLM-5.2 架构深度拆解" CH 2.2, the top-2048, and CH 4.4; "GLM-5 ->
+ * 5.1 -> 5.2" section 10, the fused operator steps): the indexer keeps only the keys at or
+ * above a cutoff taken from a sample of each row, and the top-K is resolved
+ * from those; a row for which that cannot be shown exact is scored into the
+ * workspace's matrix and selected there.  The indices are the same as
+ * dsa_indexer_scores + dsa_topk would give (ties to the lower position).
  */
 typedef struct {
   const char* layer_types;

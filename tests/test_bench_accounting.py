@@ -92,3 +92,31 @@ def test_tensor_peak_follows_the_timed_region():
     assert bench.tensor_peak(peaks, True, 10.0)[0] == pytest.approx(3500.0 * 1700 / 1900)
     work = {"flops": 1e12, "bytes": 1e6}
     assert bench.kernel_bound("sparse_mla", work, peaks, False, 0.25)[:2] == ("tensor", 1900.0)
+
+
+def test_kernel_records_count_work_per_unit_not_per_launch():
+    """An F layer whose indexer takes three launches (the select-only path)
+    is one unit of indexer work: the achieved rate divides one unit's work by
+    the summed time of its launches, and the scan + gather figure adds the
+    units' bytes over the summed times."""
+    peaks = {"hbm": 1000.0, "bf16": 100.0, "bf16_src": "x", "hbm_src": "y", "fp8": 200.0,
+             "fp8_src": "z", "bf16_sustained": 90.0}
+    work = {"indexer": {"flops": 0.0, "bytes": 2.0e9}, "sparse_mla": {"flops": 0.0, "bytes": 1.0e9}}
+    units = bench.step_units("FSSS", 10)
+    assert units == {"indexer": 10, "topk": 10, "sparse_mla": 40}
+    prof = {"indexer": (30.0, 30), "sparse_mla": (40.0, 40)}  # ms, launches
+    orig = bench.kernel_bound
+    bench.kernel_bound = lambda name, w, p, fp8, t: ("hbm", p["hbm"], "GB/s", "test")
+    try:
+        k = bench.kernel_records(prof, work, peaks, False, 1.0, units=units)
+        per_launch = bench.kernel_records(prof, work, peaks, False, 1.0)
+    finally:
+        bench.kernel_bound = orig
+    # 3 ms per F layer for 2 GB: 666.67 GB/s; per launch it would read 2000 GB/s
+    assert k["indexer"]["ms_per_unit"] == 3.0 and k["indexer"]["ms_per_launch"] == 1.0
+    assert k["indexer"]["achieved"] == pytest.approx(666.67, abs=0.01)
+    assert per_launch["indexer"]["achieved"] == pytest.approx(2000.0)
+    assert k["sparse_mla"]["achieved"] == pytest.approx(1000.0)
+    assert k["indexer"]["share"] == pytest.approx(30.0 / 70.0, abs=1e-4)
+    sg = bench.scan_gather_record(k, work, peaks)
+    assert sg["achieved"] == pytest.approx((10 * 2.0e9 + 40 * 1.0e9) / 0.070 / 1e9, abs=0.05)
