@@ -50,10 +50,10 @@ DESCR = {
 # ncu DRAM traffic of the dominant kernel (bytes per launch), with the hash of
 # the kernel sources it was measured on; ignored once the sources change.
 NCU_TRAFFIC = {
-    # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch (204.5 MB
-    # read + 125.0 MB written), scaled by tokens to the 8192-token launch (q/out traffic is per
+    # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch (204.7 MB
+    # read + 124.8 MB written), scaled by tokens to the 8192-token launch (q/out traffic is per
     # token; the kv cache is a few MB)
-    "sparse_mla": {"bytes": 1.0545e+09, "workload": "prefill8k", "src": "c41ef80cd549b518"},
+    "sparse_mla": {"bytes": 1.0543e+09, "workload": "prefill8k", "src": "2547eeaef5193321"},
 }
 
 def kernel_src_hash(files):
@@ -124,9 +124,20 @@ def algorithmic(lay, cfg, fp8, kv_row_bytes=1152):
     kbytes_per_pos = 128 * (1 if fp8 else 2) + (4 if fp8 else 0)
     seq_len = np.array([lay.q_pos[lay.q_start[b + 1] - 1] + 1 if lay.q_start[b + 1] > lay.q_start[b]
                         else 0 for b in range(lay.num_seqs)], np.int64)
+    # prefill rows beyond 16K positions take the select-only F layer (the
+    # library's rule): no score matrix; the top-K reads each row's sampled
+    # scores and its candidate list (at least K keys and positions: counted as
+    # 2K) and writes K indices
+    max_q = int(np.diff(lay.q_start).max()) if lay.num_seqs else 0
+    select_only = max_q > 1 and 16384 < lay.max_len <= 2 * 1024 * 1024
     idx_bytes = (seq_len.sum() * kbytes_per_pos + lay.num_q * 32 * (128 * (1 if fp8 else 2) + 4)
-                 + vis.sum() * 4)
-    topk_bytes = vis.sum() * 4 + lay.num_q * K * 4
+                 + (0 if select_only else vis.sum() * 4))
+    if select_only:
+        tiles = (vis - 1) // 128 + 1
+        sampled = np.minimum(tiles, np.clip(tiles // 64, 32, 64)) * 128
+        topk_bytes = (sampled * 4).sum() + lay.num_q * (2 * K * 8 + K * 4)
+    else:
+        topk_bytes = vis.sum() * 4 + lay.num_q * K * 4
     mla_flops = 2.0 * H * (576 + 512) * nvalid.sum()
     # distinct cache rows a launch must read: per sequence, at most its length
     rows_read = sum(min(int(nvalid[lay.q_start[b]:lay.q_start[b + 1]].sum()), int(seq_len[b]))

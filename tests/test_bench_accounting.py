@@ -25,25 +25,36 @@ def _walk(lay, H, K, kv_row, fp8):
         rows_read += min(sel_b, int(lay.q_pos[lay.q_start[b + 1] - 1]) + 1)
     key_bytes = 128 * (1 if fp8 else 2) + (4 if fp8 else 0)
     seq_len = sum(int(lay.q_pos[lay.q_start[b + 1] - 1]) + 1 for b in range(lay.num_seqs))
+    # prefill rows beyond 16K positions: the select-only F layer (no score
+    # matrix; sampled scores, a 2K-entry candidate list and K indices per row)
+    select_only = max(int(lay.q_start[b + 1] - lay.q_start[b]) for b in range(lay.num_seqs)) > 1 \
+        and lay.max_len > 16384
+    sampled = 0
+    for t in range(lay.num_q):
+        tiles = int(lay.q_pos[t]) // 128 + 1
+        sampled += min(tiles, min(max(tiles // 64, 32), 64)) * 128
     return {
         "indexer_flops": 2.0 * 32 * 128 * idx_pairs,
         "indexer_bytes": seq_len * key_bytes + lay.num_q * 32 * (128 * (1 if fp8 else 2) + 4)
-        + idx_pairs * 4,
-        "topk_bytes": idx_pairs * 4 + lay.num_q * K * 4,
+        + (0 if select_only else idx_pairs * 4),
+        "topk_bytes": (sampled * 4 + lay.num_q * (2 * K * 8 + K * 4)) if select_only
+        else idx_pairs * 4 + lay.num_q * K * 4,
         "mla_flops": 2.0 * H * (576 + 512) * mla_keys,
         "mla_bytes": rows_read * kv_row + lay.num_q * H * (576 + 512) * 2,
     }
 
 
-@pytest.mark.parametrize("case", ["prefill", "decode", "chunked"])
+@pytest.mark.parametrize("case", ["prefill", "decode", "chunked", "long_prefill"])
 @pytest.mark.parametrize("kv_row", [1152, 656])
 def test_algorithmic_work_matches_an_explicit_count(case, kv_row):
     if case == "prefill":
         lay, H, K = synth.make_layout([512], [512]), 16, 64
     elif case == "decode":
         lay, H, K = synth.make_layout([5000, 300, 2048], [1, 1, 1]), 64, 2048
-    else:
+    elif case == "chunked":
         lay, H, K = synth.make_layout([3000, 700], [200, 50]), 64, 256
+    else:  # rows beyond 16K positions: the select-only F layer
+        lay, H, K = synth.make_layout([20000, 17000], [24, 8]), 64, 2048
     for fp8 in (False, True):
         w = bench.algorithmic(lay, {"H": H, "K": K}, fp8, kv_row)
         ref = _walk(lay, H, K, kv_row, fp8)
