@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
 
 // ------------------------------------------------------------------ long rows
 // Few long rows (decode of a few sequences): a row is cut into `split` slices of
-// consecutive positions; four launches without inter-CTA waits, and a
+// consecutive positions; three launches without inter-CTA waits, and a
 // fallback launch for rows whose sample misled:
 //  0. cutoff:  one CTA per row histograms a sample of the row (kPrefix
 //              positions in 16 runs spread over it) and picks a cutoff bin
@@ -235,17 +235,15 @@ __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scor
 //  1. capture: every CTA of a row appends every key of its slice at or
 //              above the cutoff (float compare, warp ballots, no atomics per
 //              position) with its position to the row's capture list.
-//  2. resolve: one CTA per row.  With at least K keys captured (and none
-//              dropped) the k-th largest key is at or above the cutoff, so
-//              every key the selection takes is in the list: the threshold
-//              key T and the cut position pstar among keys equal to T follow
-//              from radix passes over the list, and the taken positions of
-//              each slice give every slice its first output slot.  A row
+//  2. resolve and write: one CTA per row.  With at least K keys captured
+//              (and none dropped) the k-th largest key is at or above the
+//              cutoff, so every key the selection takes is in the list: the
+//              threshold key T and the cut position pstar among keys equal
+//              to T follow from radix passes over the list, and the taken
+//              positions (key > T, or key == T at a position up to pstar)
+//              are written in ascending order from the list alone.  A row
 //              without that guarantee is marked for the fallback.
-//  3. write:   every CTA writes its slice's positions with key > T, or key
-//              == T at a position up to pstar, in ascending order from its
-//              slot (block prefix scans): the row comes out sorted.
-//  4. fallback: the many-rows kernel below, on the marked rows only (each
+//  3. fallback: the many-rows kernel below, on the marked rows only (each
 //              read in full, histogrammed, resolved exactly).
 constexpr int kHBits = 12;
 constexpr int kHBins = 1 << kHBits;   // 4096 bins over key bits [31:20]
@@ -260,7 +258,6 @@ struct LongScratch {
   int* cnt;          // [num_q][kCnt]
   uint32_t* ckey;    // [num_q][kCandCap] captured keys
   int32_t* cpos;     // [num_q][kCandCap] their positions
-  int* slice_off;    // [num_q][split]: first output slot of each slice
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -406,31 +403,94 @@ __device__ int tied_position_cut(int n, int need, uint32_t T, GetK get_key, GetP
   return static_cast<int>(pprefix);
 }
 
-// Ascending bitonic sort of buf[0, K) in shared memory (buf holds P >= K
-// entries, P the next power of two).  Ends with a CTA barrier.
-template <int BS>
-__device__ void sort_positions(int32_t* buf, int K) {
-  const int tid = threadIdx.x;
-  int P = 1;
-  while (P < K) P <<= 1;
-  for (int i = K + tid; i < P; i += BS) buf[i] = 0x7fffffff;
-  __syncthreads();
+// Ascending bitonic sort of the positions buf[0, K), written to out[0, K).
+// Thread t holds the E consecutive entries t*E .. t*E+E-1 in registers
+// (P = BS*E >= K entries, the tail padded with INT_MAX): the compare-exchange
+// steps of stride < E stay inside a thread, those of stride < 32*E go
+// between the lanes of a warp by shuffles, and only the larger strides pass
+// through shared memory (buf must hold P entries).  Ends with a CTA barrier.
+template <int BS, int E>
+__device__ void sort_positions_e(int32_t* buf, int K, int32_t* out) {
+  constexpr int P = BS * E;
+  const int tid = threadIdx.x, lane = tid & 31;
+  int v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = tid * E + e;
+    v[e] = i < K ? buf[i] : 0x7fffffff;
+  }
   for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P; i += BS) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool up = (i & size) == 0;
-          const int a = buf[i], c = buf[j];
-          if ((a > c) == up) {
-            buf[i] = c;
-            buf[j] = a;
+    int stride = size >> 1;
+    if (stride >= 32 * E) {  // across warps, through shared memory
+      __syncthreads();       // every thread has read buf
+#pragma unroll
+      for (int e = 0; e < E; ++e) buf[tid * E + e] = v[e];
+      __syncthreads();
+      for (; stride >= 32 * E; stride >>= 1) {
+        for (int i = tid; i < P; i += BS) {
+          const int j = i ^ stride;
+          if (j > i) {
+            const bool up = (i & size) == 0;
+            const int a = buf[i], c = buf[j];
+            if ((a > c) == up) {
+              buf[i] = c;
+              buf[j] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = buf[tid * E + e];
+    }
+    for (; stride >= E; stride >>= 1) {  // between the lanes of a warp
+      const int lm = stride / E;
+      const bool lower = (lane & lm) == 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const bool up = ((tid * E + e) & size) == 0;
+        const int o = __shfl_xor_sync(0xffffffffu, v[e], lm);
+        v[e] = (lower == up) ? min(v[e], o) : max(v[e], o);
+      }
+    }
+#pragma unroll
+    for (int st = E / 2; st > 0; st >>= 1) {  // inside a thread
+      if (st < size) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int f = e ^ st;
+          if (f > e) {
+            const bool up = ((tid * E + e) & size) == 0;
+            const int a = v[e], c = v[f];
+            if ((a > c) == up) {
+              v[e] = c;
+              v[f] = a;
+            }
           }
         }
       }
-      __syncthreads();
     }
   }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = tid * E + e;
+    if (i < K) out[i] = v[e];
+  }
+  __syncthreads();
+}
+
+// The sort above for K <= 8*BS positions; buf holds max(BS, the next power
+// of two >= K) entries.
+template <int BS>
+__device__ void sort_positions(int32_t* buf, int K, int32_t* out) {
+  if (K <= BS)
+    sort_positions_e<BS, 1>(buf, K, out);
+  else if (K <= 2 * BS)
+    sort_positions_e<BS, 2>(buf, K, out);
+  else if (K <= 4 * BS)
+    sort_positions_e<BS, 4>(buf, K, out);
+  else
+    sort_positions_e<BS, 8>(buf, K, out);
 }
 
 // Write the positions marked in bits[0, nwords) to out[0, K) in ascending
@@ -758,8 +818,7 @@ __global__ void __launch_bounds__(kRowBS, 1) topk_rows_kernel(const float* __res
       bitmap_compact<kRowBS>(bits, nwords, K, out, warp_sums, status);
     } else {
       if (tid == 0 && s_ns != K) atomicOr(status, DSA_DEVERR_BATCH);
-      sort_positions<kRowBS>(sel, K);
-      for (int i = tid; i < K; i += kRowBS) out[i] = sel[i];
+      sort_positions<kRowBS>(sel, K, out);
     }
     __syncthreads();  // the next row reuses the shared buffers
   }
@@ -790,9 +849,23 @@ __global__ void __launch_bounds__(kLongBS) topk_cutoff_kernel(const float* __res
   constexpr int kRun = kPrefix / 16;
   const bool whole = len <= kPrefix;
   const int stride = (len / 16) & ~3;  // run starts stay float4-aligned
-  for (int v = tid * 4; v < P0; v += kLongBS * 4) {
-    const int s = whole ? v : (v / kRun) * stride + (v % kRun);
-    const float4 x = *reinterpret_cast<const float4*>(row + s);
+  auto at = [&](int v) { return whole ? v : (v / kRun) * stride + (v % kRun); };
+  // every sampled float4 of this thread is requested before any is counted
+  // (one round trip to L2 instead of one per float4)
+  constexpr int kCutLoads = kPrefix / (kLongBS * 4);
+  static_assert(kPrefix % (kLongBS * 4) == 0, "whole float4 loads per thread");
+  float4 xs[kCutLoads];
+#pragma unroll
+  for (int u = 0; u < kCutLoads; ++u) {
+    const int v = (tid + u * kLongBS) * 4;
+    xs[u] = v < P0 ? *reinterpret_cast<const float4*>(row + at(v)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int u = 0; u < kCutLoads; ++u) {
+    const int v = (tid + u * kLongBS) * 4;
+    if (v >= P0) break;
+    const int s = at(v);
+    const float4 x = xs[u];
     atomicAdd(&h[order_key(x.x) >> 20], 1u);
     if (s + 1 < len) atomicAdd(&h[order_key(x.y) >> 20], 1u);
     if (s + 2 < len) atomicAdd(&h[order_key(x.z) >> 20], 1u);
@@ -836,30 +909,25 @@ __global__ void __launch_bounds__(kLongBS) topk_capture_kernel(const float* __re
   const float* row = scores + static_cast<int64_t>(t) * b.max_len;
   const float cf = __int_as_float(ws.cnt[static_cast<int64_t>(t) * kCnt + 3]);
   // keys >= cf (float compare: NaN kept too, a superset is harmless), per
-  // warp in its own segment of the shared buffer, in warp-uniform tiles
+  // warp in its own segment of the shared buffer, in warp-uniform tiles; a
+  // slice of 8K positions is requested in one batch of float4 loads
   const uint32_t lt = lanemask_lt();
   int wcount = 0;  // warp-uniform
-  for (int base = lo + warp * 128; base < hi; base += kLongBS * 4) {
-    const int s = base + lane * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (s < hi) v = *reinterpret_cast<const float4*>(row + s);
-    const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const bool p = s + q < hi && !(x[q] < cf);
-      const uint32_t m = __ballot_sync(0xffffffffu, p);
-      if (m) {
-        if (p) {
-          const int i = wcount + __popc(m & lt);
-          if (i < kCapSeg) {
-            skey[warp * kCapSeg + i] = order_key(x[q]);
-            spos[warp * kCapSeg + i] = s + q;
-          }
+  auto capture = [&](int s, float x, bool valid) {
+    const bool p = valid && !(x < cf);
+    const uint32_t m = __ballot_sync(0xffffffffu, p);
+    if (m) {
+      if (p) {
+        const int i = wcount + __popc(m & lt);
+        if (i < kCapSeg) {
+          skey[warp * kCapSeg + i] = order_key(x);
+          spos[warp * kCapSeg + i] = lo + s;
         }
-        wcount += __popc(m);
       }
+      wcount += __popc(m);
     }
-  }
+  };
+  scan_row<kLongBS, 4>(row + lo, hi - lo, capture);  // lo is a multiple of 4
   if (lane == 0) s_wcnt[warp] = wcount;
   __syncthreads();
   int* cnt = ws.cnt + static_cast<int64_t>(t) * kCnt;
@@ -885,23 +953,80 @@ __global__ void __launch_bounds__(kLongBS) topk_capture_kernel(const float* __re
     }
 }
 
+// The taken entries of a capture list (key > T, or key == T at a position up
+// to pstar) appended to taken[0, K), one shared counter update per warp.
+// Ends with a CTA barrier.
+__device__ __forceinline__ void take_listed(int n, int K, uint32_t T, int pstar, const uint32_t* ckey,
+                                            const int32_t* cpos, int32_t* taken, int* s_taken) {
+  const int lane = threadIdx.x & 31;
+  for (int i0 = 0; i0 < n; i0 += blockDim.x) {  // n is the same in every thread
+    const int i = i0 + static_cast<int>(threadIdx.x);
+    bool tk = false;
+    int p = 0;
+    if (i < n) {
+      const uint32_t k = ckey[i];
+      p = cpos[i];
+      tk = k > T || (k == T && p <= pstar);
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, tk);
+    int base = 0;
+    if (lane == 0 && m) base = atomicAdd(s_taken, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (tk) {
+      const int j = base + __popc(m & lanemask_lt());
+      if (j < K) taken[j] = p;
+    }
+  }
+  __syncthreads();
+}
+
+// The K taken positions taken[0, K) of a row of len positions written to
+// out in ascending order: through a bitmap over the row in `area` (free
+// shared memory of kBitmapLen / 32 words) for rows up to kBitmapLen
+// positions, else by the sort.  Flags DSA_DEVERR_BATCH unless exactly K were
+// taken.  Ends with a CTA barrier.
+constexpr int kBitmapLen = 262144;  // measured: the sort's fixed cost wins beyond this
+template <int BS>
+__device__ void write_taken(int len, int K, int32_t* taken, int n_taken, uint32_t* area, int32_t* out,
+                            int* warp_sums, int* status) {
+  if (len <= kBitmapLen) {
+    const int nwords = (len + 31) >> 5;
+    for (int i = threadIdx.x; i < nwords; i += BS) area[i] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < min(n_taken, K); j += BS)
+      atomicOr(&area[taken[j] >> 5], 1u << (taken[j] & 31));
+    __syncthreads();
+    bitmap_compact<BS>(area, nwords, K, out, warp_sums, status);
+  } else {
+    if (threadIdx.x == 0 && n_taken != K) atomicOr(status, DSA_DEVERR_BATCH);
+    sort_positions<BS>(taken, K, out);
+  }
+}
+
 // Long path, launch 2: the threshold key and tie cut of a row from its
-// capture list, and each slice's first output slot (or the row marked for
-// the fallback).
-__global__ void __launch_bounds__(kFinBS, 1) topk_resolve_kernel(BatchArgs b, int K, int split,
-                                                                 LongScratch ws, int* status) {
+// capture list, then the taken positions (key > T, or key == T at a position
+// up to pstar: exactly K of them) in ascending order.  A row without the
+// guarantee (too few keys captured, or any dropped) is marked for the
+// fallback (word 6).
+__global__ void __launch_bounds__(kFinBS, 1) topk_resolve_write_kernel(BatchArgs b, int K,
+                                                                       LongScratch ws, int32_t* idx,
+                                                                       int* status) {
   __shared__ int hist2[2048];
   __shared__ uint32_t h[kHBins];
   __shared__ int warp_sums[32];
-  __shared__ int s_d, s_above, s_n, s_b1, s_nabove;
-  extern __shared__ uint32_t res_dyn[];  // captured keys and positions, then taken per slice
+  __shared__ int s_d, s_above, s_n, s_b1, s_nabove, s_taken;
+  extern __shared__ uint32_t res_dyn[];  // captured keys and positions, then the taken positions
   uint32_t* ckey = res_dyn;
   int32_t* cpos = reinterpret_cast<int32_t*>(res_dyn + kCandCap);
-  int* taken = reinterpret_cast<int*>(res_dyn + 2 * kCandCap);
+  int32_t* taken = reinterpret_cast<int32_t*>(res_dyn + 2 * kCandCap);
   const int t = blockIdx.x, tid = threadIdx.x;
   const int pos = query_pos(b, t, tid == 0 ? status : nullptr);
   const int len = pos + 1;
-  if (len <= K) return;
+  int32_t* out = idx + static_cast<int64_t>(t) * K;
+  if (len <= K) {  // every visible position, then -1 padding
+    for (int j = tid; j < K; j += kFinBS) out[j] = j < len ? j : -1;
+    return;
+  }
   int* cnt = ws.cnt + static_cast<int64_t>(t) * kCnt;
   const int n = cnt[1];
   if (cnt[2] != 0 || n < K || n > kCandCap) {  // no guarantee: the fallback takes the row
@@ -913,7 +1038,7 @@ __global__ void __launch_bounds__(kFinBS, 1) topk_resolve_kernel(BatchArgs b, in
     cpos[i] = ws.cpos[static_cast<int64_t>(t) * kCandCap + i];
   }
   for (int i = tid; i < kHBins; i += kFinBS) h[i] = 0;
-  for (int i = tid; i < split; i += kFinBS) taken[i] = 0;
+  if (tid == 0) s_taken = 0;
   __syncthreads();
   for (int i = tid; i < n; i += kFinBS) atomicAdd(&h[ckey[i] >> 20], 1u);
   __syncthreads();
@@ -927,84 +1052,8 @@ __global__ void __launch_bounds__(kFinBS, 1) topk_resolve_kernel(BatchArgs b, in
                           &need);
   const int pstar = tied_position_cut<kFinBS>(n, need, T, get_key, get_pos, hist2, warp_sums, &s_d,
                                               &s_above, &s_n);
-  // taken positions per slice (slice_of's cut: slices of `chunk` positions)
-  const int chunk = (((len + split - 1) / split) + 3) & ~3;
-  for (int i = tid; i < n; i += kFinBS) {
-    const uint32_t k = ckey[i];
-    if (k > T || (k == T && cpos[i] <= pstar)) atomicAdd(&taken[cpos[i] / chunk], 1);
-  }
-  __syncthreads();
-  const int per = (split + kFinBS - 1) / kFinBS;
-  int local = 0;
-  for (int k = 0; k < per; ++k) {
-    const int c = tid * per + k;
-    if (c < split) local += taken[c];
-  }
-  int total;
-  int run = block_excl_scan<kFinBS>(local, warp_sums, &total);
-  for (int k = 0; k < per; ++k) {
-    const int c = tid * per + k;
-    if (c >= split) break;
-    ws.slice_off[static_cast<int64_t>(t) * split + c] = run;
-    run += taken[c];
-  }
-  if (tid == 0) {
-    cnt[4] = static_cast<int>(T);
-    cnt[5] = pstar;
-    if (total != K) atomicOr(status, DSA_DEVERR_BATCH);
-  }
-}
-
-// Long path, launch 3: the slice's taken positions in ascending order.
-__global__ void __launch_bounds__(kLongBS) topk_write_kernel(const float* __restrict__ scores,
-                                                             BatchArgs b, int K, int split,
-                                                             LongScratch ws, int32_t* idx) {
-  __shared__ int warp_sums[32];
-  const int t = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
-  const int pos = query_pos(b, t, nullptr);
-  const int len = pos + 1;
-  int32_t* out = idx + static_cast<int64_t>(t) * K;
-  if (len <= K) {  // every visible position, then -1 padding
-    if (c == 0)
-      for (int j = tid; j < K; j += kLongBS) out[j] = j < len ? j : -1;
-    return;
-  }
-  const int* cnt = ws.cnt + static_cast<int64_t>(t) * kCnt;
-  if (cnt[6] != 0) return;  // the fallback writes this row
-  int lo, hi;
-  slice_of(len, split, c, lo, hi);
-  if (lo >= hi) return;
-  const uint32_t T = static_cast<uint32_t>(cnt[4]);
-  const int pstar = cnt[5];
-  int base = ws.slice_off[static_cast<int64_t>(t) * split + c];
-  const float* row = scores + static_cast<int64_t>(t) * b.max_len;
-  // in tiles of 4 * BS positions (lo is a multiple of 4, the row's capacity
-  // a multiple of 128, so a float4 read stays inside the row)
-#pragma unroll 1
-  for (int tile = lo; tile < hi; tile += 4 * kLongBS) {
-    const int s0 = tile + tid * 4;
-    bool take[4] = {false, false, false, false};
-    int n = 0;
-    if (s0 < hi) {
-      const float4 v = *reinterpret_cast<const float4*>(row + s0);
-      const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t k = order_key(x[q]);
-        take[q] = s0 + q < hi && (k > T || (k == T && s0 + q <= pstar));
-        n += take[q];
-      }
-    }
-    int tot;
-    int slot = base + block_excl_scan<kLongBS>(n, warp_sums, &tot);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (take[q]) {
-        if (slot < K) out[slot] = s0 + q;
-        ++slot;
-      }
-    base += tot;
-  }
+  take_listed(n, K, T, pstar, ckey, cpos, taken, &s_taken);
+  write_taken<kFinBS>(len, K, taken, s_taken, res_dyn, out, warp_sums, status);
 }
 
 // Rows beyond 16K positions: fewer than kRowsFew of them are spread over
@@ -1030,7 +1079,7 @@ size_t round256z(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Layout of the long path's scratch; *zeroed = bytes at its head to clear.
 LongScratch long_scratch(const dsa_batch_t& b, void* base_v, size_t* total, size_t* zeroed) {
-  const size_t q = static_cast<size_t>(b.num_q), sp = static_cast<size_t>(long_split(b));
+  const size_t q = static_cast<size_t>(b.num_q);
   uint8_t* base = static_cast<uint8_t*>(base_v);
   LongScratch ws;
   size_t off = 0;
@@ -1041,8 +1090,6 @@ LongScratch long_scratch(const dsa_batch_t& b, void* base_v, size_t* total, size
   off += round256z(q * kCandCap * 4);
   ws.cpos = reinterpret_cast<int32_t*>(base + off);
   off += round256z(q * kCandCap * 4);
-  ws.slice_off = reinterpret_cast<int*>(base + off);
-  off += round256z(q * sp * 4);
   if (total) *total = off;
   return ws;
 }
@@ -1178,11 +1225,13 @@ __global__ void __launch_bounds__(kLongBS) topk_sample_cutoff_kernel(BatchArgs b
 // One CTA per row: the row's capture list gathered from its key chunks'
 // segments, the threshold key T and tie cut pstar from it (as the long
 // path's resolve), then the taken positions (key > T, or key == T at a
-// position up to pstar: exactly K of them) sorted ascending into the output.
+// position up to pstar: exactly K of them) written in ascending order.
 // A row without the guarantee (too few keys captured, or a chunk with more
 // keys than its segment or the list more than kResCap) is marked for the
 // fallback (word 6).
 constexpr int kResCap = 8192;
+static_assert(kBitmapLen / 32 <= 2 * kResCap && kBitmapLen / 32 <= 2 * kCandCap,
+              "the bitmap fits in the lists' space of both resolve-and-write kernels");
 __global__ void __launch_bounds__(kFinBS) topk_list_resolve_write_kernel(BatchArgs b, int K,
                                                                          TopkLists ls,
                                                                          int32_t* idx,
@@ -1262,29 +1311,8 @@ __global__ void __launch_bounds__(kFinBS) topk_list_resolve_write_kernel(BatchAr
                           &need);
   const int pstar = tied_position_cut<kFinBS>(n, need, T, get_key, get_pos, hist2, warp_sums, &s_d,
                                               &s_above, &s_n);
-  for (int i = tid; i < n; i += kFinBS) {
-    const uint32_t k = ckey[i];
-    if (k > T || (k == T && cpos[i] <= pstar)) {
-      const int j = atomicAdd(&s_taken, 1);
-      if (j < K) taken[j] = cpos[i];
-    }
-  }
-  __syncthreads();
-  if (len <= kResCap * 32) {
-    // ascending order through a bitmap over the row (in the key area, free now)
-    uint32_t* bits = ckey;
-    const int nwords = (len + 31) >> 5;
-    for (int i = tid; i < nwords; i += kFinBS) bits[i] = 0;
-    __syncthreads();
-    for (int j = tid; j < min(s_taken, K); j += kFinBS)
-      atomicOr(&bits[taken[j] >> 5], 1u << (taken[j] & 31));
-    __syncthreads();
-    bitmap_compact<kFinBS>(bits, nwords, K, out, warp_sums, status);
-  } else {
-    if (tid == 0 && s_taken != K) atomicOr(status, DSA_DEVERR_BATCH);
-    sort_positions<kFinBS>(taken, K);
-    for (int j = tid; j < K; j += kFinBS) out[j] = taken[j];
-  }
+  take_listed(n, K, T, pstar, ckey, cpos, taken, &s_taken);
+  write_taken<kFinBS>(len, K, taken, s_taken, res_dyn, out, warp_sums, status);
 }
 
 }  // namespace
@@ -1358,7 +1386,7 @@ cudaError_t launch_indexer_topk_select(const void* q_idx, const float* q_scale, 
                           nullptr, ls, status, stream);
   if (e != cudaSuccess) return e;
   // 4. exact selection from the lists, written in ascending order
-  int pw = 1;
+  int pw = kFinBS;  // the sort's area: max(kFinBS, the next power of two >= k)
   while (pw < k) pw <<= 1;
   prof_begin(stream);
   topk_list_resolve_write_kernel<<<b.num_q, kFinBS, (2 * static_cast<size_t>(kResCap) + pw) * 4,
@@ -1392,17 +1420,20 @@ cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_
     cudaError_t e = cudaMemsetAsync(scratch, 0, zeroed, stream);
     if (e != cudaSuccess) return e;
     const int split = long_split(b);
-    if (split > 4096) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(split), static_cast<unsigned>(b.num_q));
     const BatchArgs a = to_args(b);
-    // resolve: the captured keys and positions, then one count per slice
-    const size_t res_bytes = (2 * static_cast<size_t>(kCandCap) + split) * 4;
+    // resolve and write: the captured keys and positions, then the taken
+    // positions (padded to a power of two for the sort)
+    int pw = kFinBS;
+    while (pw < k) pw <<= 1;
+    const size_t res_bytes = (2 * static_cast<size_t>(kCandCap) + pw) * 4;
     {
       static int configured_device = -1;
       int dev = 0;
       cudaGetDevice(&dev);
       if (configured_device != dev) {
-        e = cudaFuncSetAttribute(topk_resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(topk_resolve_write_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (2 * kCandCap + 4096) * 4);
         if (e != cudaSuccess) return e;
         configured_device = dev;
@@ -1422,11 +1453,10 @@ cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_
     prof_begin(stream);
     topk_cutoff_kernel<<<b.num_q, kLongBS, kCutDynBytes, stream>>>(scores, a, k, ws);
     topk_capture_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws);
-    topk_resolve_kernel<<<b.num_q, kFinBS, res_bytes, stream>>>(a, k, split, ws, status);
-    topk_write_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws, idx);
+    topk_resolve_write_kernel<<<b.num_q, kFinBS, res_bytes, stream>>>(a, k, ws, idx, status);
     e = launch_rows(scores, b, k, idx, status, stream, ws.cnt);  // marked rows only
     prof_end(kLaunchTopk, stream);
-    for (int i = 0; i < 4; ++i) count_launch(kLaunchTopk);
+    for (int i = 0; i < 3; ++i) count_launch(kLaunchTopk);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }

@@ -9,7 +9,8 @@ written once per group).
 Scores are made exact: every head of every query is the unit vector e0 and
 only head 0 has weight 1, so score(t, s) = ReLU(k[s, 0]) with k[s, 0] a
 small integer (exact in bf16 and in fp32).  The cases:
-  * random integers 0..255 (many ties: the position tie-break decides);
+  * random integers 0..255 (many ties: the position tie-break decides), on
+    rows of 30-40K positions and on rows of 300K;
   * a drift, k[s, 0] = s // 1000, so the selected keys all lie in the last
     key chunk and overflow its segments of the capture list (the fallback);
   * a misleading sample: a large value planted only inside the tiles the
@@ -77,11 +78,14 @@ def _per_seq(lay, f):
     return k0
 
 
-@pytest.mark.parametrize("case", ["random", "drift"])
+@pytest.mark.parametrize("case", ["random", "drift", "long"])
 def test_select_only_equals_oracle_topk(case):
-    lay = synth.make_layout([40000, 30000], [16, 8])
+    # "long": rows beyond 262,144 positions, whose taken positions are sorted
+    # into order rather than compacted from a bitmap over the row
+    lens, counts = ([300000, 20000], [8, 8]) if case == "long" else ([40000, 30000], [16, 8])
+    lay = synth.make_layout(lens, counts)
     rng = np.random.default_rng(5)
-    if case == "random":
+    if case in ("random", "long"):
         k0 = rng.integers(0, 256, lay.rows).astype(np.float32)
     else:
         k0 = _per_seq(lay, lambda s: (s // 1000).astype(np.float32))
