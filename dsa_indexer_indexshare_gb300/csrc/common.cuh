@@ -64,6 +64,46 @@ __device__ __forceinline__ int query_pos(const BatchArgs& b, int t, int* status)
   return p;
 }
 
+// Programmatic dependent launch.  The library's kernels on the indexer /
+// top-K / attention path are launched with programmatic stream
+// serialization (launch_chained): such a kernel may be scheduled while the
+// previous kernel of its stream is still running, so each of them calls
+// chain_wait() before its first access to global memory (it returns once
+// every earlier kernel of the stream has completed and its writes are
+// visible) and then chain_release(), which lets the next kernel be
+// scheduled.  Both are no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void chain_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// cudaLaunchKernelEx with programmatic stream serialization and, for
+// cluster > 1, that many CTAs per cluster along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, unsigned cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Order-preserving image of an fp32 score: a > b as floats iff key(a) >
 // key(b) as unsigned integers.  -0.0 is first replaced by +0.0 so that the
 // two zeros are one value (equal scores, ties to the lower position); a NaN

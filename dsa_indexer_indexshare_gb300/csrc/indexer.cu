@@ -86,6 +86,8 @@ template <int NTOK, bool FP8, int STAGES, int MODE>
 __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES, MODE>::NT, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap, const IndexerParams p) {
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
   using C = IdxCfg<NTOK, FP8, STAGES, MODE>;
   constexpr int W_PROD = C::NEPI, W_MMA = C::NEPI + 1, NEPT = C::NEPI * 32;
   extern __shared__ uint8_t smem_raw[];
@@ -428,10 +430,10 @@ cudaError_t launch_one(const CUtensorMap& qmap, const CUtensorMap& kmap, Indexer
   dim3 grid(static_cast<unsigned>(p.num_qb) * static_cast<unsigned>(p.num_kc),
             static_cast<unsigned>(p.b.num_seqs));
   prof_begin(stream);
-  kern<<<grid, C::NT, C::SMEM, stream>>>(qmap, kmap, p);
+  cudaError_t e = launch_chained(kern, grid, dim3(C::NT), C::SMEM, stream, 1, qmap, kmap, p);
   prof_end(kLaunchIndexer, stream);
   count_launch(kLaunchIndexer);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int MODE>

@@ -163,6 +163,8 @@ template <int H, int NSPLIT, bool PAGED, bool KV8>
 __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap qlat_map,
                       const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
   using C = MlaCfg<H>;
   constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
   // Two issuer warps: an mbarrier wait in the issuing thread stalls until its
@@ -743,20 +745,9 @@ cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaPa
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.b.max_q) * NSPLIT, static_cast<unsigned>(p.b.num_seqs));
-  cfg.blockDim = dim3(C::NT);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = NSPLIT;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  const dim3 grid(static_cast<unsigned>(p.b.max_q) * NSPLIT, static_cast<unsigned>(p.b.num_seqs));
   prof_begin(stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ql, qr, p);
+  cudaError_t e = launch_chained(kern, grid, dim3(C::NT), C::SMEM, stream, NSPLIT, ql, qr, p);
   prof_end(kLaunchMla, stream);
   count_launch(kLaunchMla);
   return e;

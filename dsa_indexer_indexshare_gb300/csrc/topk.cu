@@ -61,6 +61,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int* total
 template <int CL, int BS, bool STAGE>
 __global__ void __launch_bounds__(BS) topk_kernel(const float* __restrict__ scores, BatchArgs b,
                                                   int K, int32_t* __restrict__ idx, int* status) {
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
   extern __shared__ uint32_t skeys[];
   __shared__ int hist[2048];
   __shared__ int tot[CL > 1 ? 2048 : 1];
@@ -608,6 +610,8 @@ __device__ __forceinline__ void scan_row(const float* __restrict__ row, int hi, 
 __global__ void __launch_bounds__(kRowBS, 1) topk_rows_kernel(const float* __restrict__ scores,
                                                              BatchArgs b, int K, int32_t* idx,
                                                              int* status, const int* only) {
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
   extern __shared__ uint32_t row_dyn[];
   uint32_t* hcopies = row_dyn;                                  // [kHCopies][kHStride], pass 1
   uint32_t* hist = row_dyn;                                     // [kHBins], summed copies
@@ -833,10 +837,15 @@ constexpr int kCutCopies = 4;
 constexpr int kCutDynBytes = kCutCopies * kHBins * 4;
 __global__ void __launch_bounds__(kLongBS) topk_cutoff_kernel(const float* __restrict__ scores,
                                                               BatchArgs b, int K, LongScratch ws) {
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
   extern __shared__ uint32_t cut_dyn[];  // [kCutCopies][kHBins]
   __shared__ int warp_sums[32];
   __shared__ int s_cut, s_tmp;
   const int t = blockIdx.x, tid = threadIdx.x;
+  // the row's words start at zero: the later launches count into 1 and 2
+  // and mark 6 (every row, short ones included: the fallback reads word 6)
+  if (tid < kCnt) ws.cnt[static_cast<int64_t>(t) * kCnt + tid] = 0;
   const int pos = query_pos(b, t, nullptr);
   const int len = pos + 1;
   if (len <= K) return;
@@ -895,6 +904,8 @@ __global__ void __launch_bounds__(kLongBS) topk_cutoff_kernel(const float* __res
 __global__ void __launch_bounds__(kLongBS) topk_capture_kernel(const float* __restrict__ scores,
                                                                BatchArgs b, int K, int split,
                                                                LongScratch ws) {
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
   __shared__ uint32_t skey[(kLongBS / 32) * kCapSeg];
   __shared__ int32_t spos[(kLongBS / 32) * kCapSeg];
   __shared__ int s_wcnt[kLongBS / 32];
@@ -1011,6 +1022,8 @@ __device__ void write_taken(int len, int K, int32_t* taken, int n_taken, uint32_
 __global__ void __launch_bounds__(kFinBS, 1) topk_resolve_write_kernel(BatchArgs b, int K,
                                                                        LongScratch ws, int32_t* idx,
                                                                        int* status) {
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
   __shared__ int hist2[2048];
   __shared__ uint32_t h[kHBins];
   __shared__ int warp_sums[32];
@@ -1077,15 +1090,15 @@ int long_split(const dsa_batch_t& b) {
 
 size_t round256z(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Layout of the long path's scratch; *zeroed = bytes at its head to clear.
-LongScratch long_scratch(const dsa_batch_t& b, void* base_v, size_t* total, size_t* zeroed) {
+// Layout of the long path's scratch (its per-row words are cleared by the
+// cutoff launch).
+LongScratch long_scratch(const dsa_batch_t& b, void* base_v, size_t* total) {
   const size_t q = static_cast<size_t>(b.num_q);
   uint8_t* base = static_cast<uint8_t*>(base_v);
   LongScratch ws;
   size_t off = 0;
   ws.cnt = reinterpret_cast<int*>(base + off);
   off += round256z(q * kCnt * 4);
-  if (zeroed) *zeroed = off;
   ws.ckey = reinterpret_cast<uint32_t*>(base + off);
   off += round256z(q * kCandCap * 4);
   ws.cpos = reinterpret_cast<int32_t*>(base + off);
@@ -1109,20 +1122,10 @@ cudaError_t launch_cl(const float* scores, const dsa_batch_t& b, int k, int32_t*
       configured_device = dev;
     }
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(CL) * static_cast<unsigned>(b.num_q));
-  cfg.blockDim = dim3(BS);
-  cfg.dynamicSmemBytes = STAGE ? smem : 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   prof_begin(stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, scores, to_args(b), k, idx, status);
+  cudaError_t e = launch_chained(kern, dim3(static_cast<unsigned>(CL) * static_cast<unsigned>(b.num_q)),
+                                 dim3(BS), STAGE ? smem : 0, stream, CL, scores, to_args(b), k, idx,
+                                 status);
   prof_end(kLaunchTopk, stream);
   count_launch(kLaunchTopk);
   return e;
@@ -1143,10 +1146,11 @@ cudaError_t launch_rows(const float* scores, const dsa_batch_t& b, int k, int32_
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = static_cast<int>(std::min<int64_t>(b.num_q, sms));
   if (!only) prof_begin(stream);
-  topk_rows_kernel<<<grid, kRowBS, kRowDynBytes, stream>>>(scores, to_args(b), k, idx, status, only);
+  cudaError_t e = launch_chained(topk_rows_kernel, dim3(grid), dim3(kRowBS), kRowDynBytes, stream, 1,
+                                 scores, to_args(b), k, idx, status, only);
   if (!only) prof_end(kLaunchTopk, stream);
   count_launch(kLaunchTopk);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ select-only F layer
@@ -1160,6 +1164,8 @@ cudaError_t launch_rows(const float* scores, const dsa_batch_t& b, int k, int32_
 // when the sample holds fewer than need values.
 __global__ void __launch_bounds__(kLongBS) topk_sample_cutoff_kernel(BatchArgs b, int K,
                                                                      TopkLists ls) {
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
   extern __shared__ uint32_t cut_dyn[];  // [kCutCopies][kHBins]
   __shared__ int hist2[1024];
   __shared__ int warp_sums[32];
@@ -1236,6 +1242,8 @@ __global__ void __launch_bounds__(kFinBS) topk_list_resolve_write_kernel(BatchAr
                                                                          TopkLists ls,
                                                                          int32_t* idx,
                                                                          int* status) {
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
   __shared__ int hist2[2048];
   __shared__ uint32_t h[kHBins];
   __shared__ int warp_sums[32];
@@ -1377,7 +1385,9 @@ cudaError_t launch_indexer_topk_select(const void* q_idx, const float* q_scale, 
                           nullptr, ls, status, stream);
   if (e != cudaSuccess) return e;
   prof_begin(stream);
-  topk_sample_cutoff_kernel<<<b.num_q, kLongBS, kCutDynBytes, stream>>>(a, k, ls);
+  e = launch_chained(topk_sample_cutoff_kernel, dim3(b.num_q), dim3(kLongBS), kCutDynBytes, stream, 1, a,
+                     k, ls);
+  if (e != cudaSuccess) return e;
   prof_end(kLaunchTopk, stream);
   count_launch(kLaunchTopk);
   e = cudaMemsetAsync(ls.segcnt, 0, static_cast<size_t>(b.num_q) * kSegMax * 4 * 4, stream);
@@ -1389,8 +1399,9 @@ cudaError_t launch_indexer_topk_select(const void* q_idx, const float* q_scale, 
   int pw = kFinBS;  // the sort's area: max(kFinBS, the next power of two >= k)
   while (pw < k) pw <<= 1;
   prof_begin(stream);
-  topk_list_resolve_write_kernel<<<b.num_q, kFinBS, (2 * static_cast<size_t>(kResCap) + pw) * 4,
-                                   stream>>>(a, k, ls, idx, status);
+  e = launch_chained(topk_list_resolve_write_kernel, dim3(b.num_q), dim3(kFinBS),
+                     (2 * static_cast<size_t>(kResCap) + pw) * 4, stream, 1, a, k, ls, idx, status);
+  if (e != cudaSuccess) return e;
   prof_end(kLaunchTopk, stream);
   count_launch(kLaunchTopk);
   e = cudaGetLastError();
@@ -1406,7 +1417,7 @@ cudaError_t launch_indexer_topk_select(const void* q_idx, const float* q_scale, 
 size_t topk_scratch_bytes(const dsa_batch_t& b, int) {
   if (b.num_q == 0 || !use_long_path(b)) return 0;
   size_t total = 0;
-  long_scratch(b, nullptr, &total, nullptr);
+  long_scratch(b, nullptr, &total);
   return total;
 }
 
@@ -1415,10 +1426,8 @@ cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_
   if (b.num_q == 0) return cudaSuccess;
   if (use_long_path(b)) {
     if (!scratch || scratch_bytes < topk_scratch_bytes(b, k)) return cudaErrorInvalidValue;
-    size_t zeroed = 0;
-    const LongScratch ws = long_scratch(b, scratch, nullptr, &zeroed);
-    cudaError_t e = cudaMemsetAsync(scratch, 0, zeroed, stream);
-    if (e != cudaSuccess) return e;
+    const LongScratch ws = long_scratch(b, scratch, nullptr);
+    cudaError_t e = cudaSuccess;
     const int split = long_split(b);
     const dim3 grid(static_cast<unsigned>(split), static_cast<unsigned>(b.num_q));
     const BatchArgs a = to_args(b);
@@ -1451,10 +1460,14 @@ cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_
       }
     }
     prof_begin(stream);
-    topk_cutoff_kernel<<<b.num_q, kLongBS, kCutDynBytes, stream>>>(scores, a, k, ws);
-    topk_capture_kernel<<<grid, kLongBS, 0, stream>>>(scores, a, k, split, ws);
-    topk_resolve_write_kernel<<<b.num_q, kFinBS, res_bytes, stream>>>(a, k, ws, idx, status);
-    e = launch_rows(scores, b, k, idx, status, stream, ws.cnt);  // marked rows only
+    e = launch_chained(topk_cutoff_kernel, dim3(b.num_q), dim3(kLongBS), kCutDynBytes, stream, 1,
+                       scores, a, k, ws);
+    if (e == cudaSuccess)
+      e = launch_chained(topk_capture_kernel, grid, dim3(kLongBS), 0, stream, 1, scores, a, k, split, ws);
+    if (e == cudaSuccess)
+      e = launch_chained(topk_resolve_write_kernel, dim3(b.num_q), dim3(kFinBS), res_bytes, stream, 1, a,
+                         k, ws, idx, status);
+    if (e == cudaSuccess) e = launch_rows(scores, b, k, idx, status, stream, ws.cnt);  // marked rows only
     prof_end(kLaunchTopk, stream);
     for (int i = 0; i < 3; ++i) count_launch(kLaunchTopk);
     if (e != cudaSuccess) return e;
