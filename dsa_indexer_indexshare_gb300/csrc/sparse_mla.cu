@@ -97,6 +97,10 @@ struct MlaParams {
   float scale_log2;
   uint16_t* out;
   float* lse;
+  // tokens split over 4 or 8 CTAs: partial results of CTA r of token t at
+  // part + (t * NSPLIT + r) * (H * 512 + 2 * H): O^T as [h][512], then the
+  // running maxima and the row sums of the H heads
+  float* part;
   int* status;
   uint64_t timeout_ns;
 };
@@ -167,6 +171,10 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   chain_release();  // the next one may be scheduled
   using C = MlaCfg<H>;
   constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
+  // split tokens combine their partial results through L2 for 4 or 8 CTAs
+  // (each CTA would read 128 KB through the cluster, at ~35 GB/s per SM),
+  // through distributed shared memory for 2 (half of it local)
+  constexpr bool kMergeL2 = NSPLIT >= 4;
   // Two issuer warps: an mbarrier wait in the issuing thread stalls until its
   // own queued MMAs have drained, so the QK products (which wait for each
   // gathered group) and the P.V products (which wait for P) come from
@@ -640,10 +648,14 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     }
     named_bar_sync(1, NST);
     if (tid < H) lsum[tid] = (red[tid] + red[H + tid]) + (red[2 * H + tid] + red[3 * H + tid]);
-    // stage the unnormalised O^T of this CTA in shared memory as [h][512]
+    // the unnormalised O^T of this CTA as [h][512]: staged in shared memory,
+    // or for a token split over 4 or 8 CTAs written with the running maxima
+    // and the row sums to the token's partial results in global memory
+    // (zeros for a CTA without blocks), which the cluster combines through L2
     const bool have = j1 > j0 && mbar_wait(bar(B_O), 0, abort_flag, p.status, to);
     tc_fence_after();
-    float* Os = reinterpret_cast<float*>(sm + C::OFF_C);
+    float* Od = kMergeL2 ? p.part + (static_cast<int64_t>(t) * NSPLIT + rank) * (H * 512 + 2 * H)
+                         : reinterpret_cast<float*>(sm + C::OFF_C);
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       float o[HW];
@@ -654,7 +666,11 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         for (int h = 0; h < HW; ++h) o[h] = 0.f;
       }
 #pragma unroll
-      for (int h = 0; h < HW; ++h) Os[(h0 + h) * 512 + c * 128 + key] = o[h];
+      for (int h = 0; h < HW; ++h) Od[(h0 + h) * 512 + c * 128 + key] = o[h];
+    }
+    if (kMergeL2 && tid < H) {
+      Od[H * 512 + tid] = m_used[tid];
+      Od[H * 512 + H + tid] = lsum[tid];
     }
   }
   tc_fence_before();
@@ -667,14 +683,31 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   // ---- combine the NSPLIT partial results and write bf16 out (+ lse)
   float* Os = reinterpret_cast<float*>(sm + C::OFF_C);
   if constexpr (NSPLIT > 1) {
+    // every rank's partial results are complete before any is read: in
+    // global memory (L2, read at L2: the other SMs' writes are not in this
+    // L1), or in each rank's shared memory (read through the cluster)
+    if (kMergeL2) __threadfence();
     cluster_sync();
+    const float* part_t = p.part + static_cast<int64_t>(t) * NSPLIT * (H * 512 + 2 * H);
+    auto part4 = [&](int r, int h, int d) -> float4 {
+      if constexpr (kMergeL2)
+        return __ldcg(reinterpret_cast<const float4*>(part_t + r * (H * 512 + 2 * H) + h * 512 + d));
+      else
+        return ld_dsmem_f4(mapa_shared(smem_u32(&Os[h * 512 + d]), r));
+    };
     if (tid < H) {
       float mr[NSPLIT], lr[NSPLIT];
       float M = -INFINITY;
 #pragma unroll
       for (int r = 0; r < NSPLIT; ++r) {
-        mr[r] = __uint_as_float(ld_dsmem_u32(mapa_shared(smem_u32(&m_used[tid]), r)));
-        lr[r] = __uint_as_float(ld_dsmem_u32(mapa_shared(smem_u32(&lsum[tid]), r)));
+        if constexpr (kMergeL2) {
+          const float* pr = part_t + r * (H * 512 + 2 * H) + H * 512;
+          mr[r] = __ldcg(pr + tid);
+          lr[r] = __ldcg(pr + H + tid);
+        } else {
+          mr[r] = __uint_as_float(ld_dsmem_u32(mapa_shared(smem_u32(&m_used[tid]), r)));
+          lr[r] = __uint_as_float(ld_dsmem_u32(mapa_shared(smem_u32(&lsum[tid]), r)));
+        }
         M = fmaxf(M, mr[r]);
       }
       float L = 0.f;
@@ -687,28 +720,43 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         p.lse[static_cast<int64_t>(t) * H + tid] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
     __syncthreads();
-    constexpr int DS = 512 / NSPLIT;
-    for (int i = tid; i < H * DS / 4; i += NT) {
-      const int h = i / (DS / 4);
-      const int d = rank * DS + (i % (DS / 4)) * 4;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // this rank's DS dims of every head: each thread takes U float4 outputs
+    // per pass and requests all their U * NSPLIT vectors before summing any
+    constexpr int DS = 512 / NSPLIT, ITEMS = H * DS / 4, U = 16 / NSPLIT;
+    for (int i0 = tid; i0 < ITEMS; i0 += U * NT) {
+      float4 v[U][NSPLIT];
 #pragma unroll
-      for (int r = 0; r < NSPLIT; ++r) {
-        const float f = fac[r * H + h];
-        const float4 v = ld_dsmem_f4(mapa_shared(smem_u32(&Os[h * 512 + d]), r));
-        acc.x = fmaf(f, v.x, acc.x);
-        acc.y = fmaf(f, v.y, acc.y);
-        acc.z = fmaf(f, v.z, acc.z);
-        acc.w = fmaf(f, v.w, acc.w);
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * NT;
+        if (i < ITEMS) {
+          const int h = i / (DS / 4), d = rank * DS + (i % (DS / 4)) * 4;
+#pragma unroll
+          for (int r = 0; r < NSPLIT; ++r) v[u][r] = part4(r, h, d);
+        }
       }
-      __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
-      __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo2);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-      *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * H + h) * 512 + d) = pk;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * NT;
+        if (i >= ITEMS) break;
+        const int h = i / (DS / 4), d = rank * DS + (i % (DS / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < NSPLIT; ++r) {
+          const float f = fac[r * H + h];
+          acc.x = fmaf(f, v[u][r].x, acc.x);
+          acc.y = fmaf(f, v[u][r].y, acc.y);
+          acc.z = fmaf(f, v[u][r].z, acc.z);
+          acc.w = fmaf(f, v[u][r].w, acc.w);
+        }
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+        __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+        *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(t) * H + h) * 512 + d) = pk;
+      }
     }
-    cluster_sync();  // keep this CTA's shared memory alive until every rank has read it
+    if (!kMergeL2) cluster_sync();  // this CTA's shared memory stays until every rank has read it
   } else {
     if (tid < H) {
       const float L = lsum[tid];
@@ -770,11 +818,27 @@ cudaError_t launch_h(const CUtensorMap& ql, const CUtensorMap& qr, const MlaPara
 
 }  // namespace
 
-size_t mla_workspace_bytes(const dsa_batch_t&, int, int) { return 0; }
+// CTAs per token (one cluster): a token's key blocks are split over several
+// CTAs when there are too few tokens to cover the SMs (decode).
+int mla_nsplit(const dsa_batch_t& b, int k) {
+  const int nblk = (k + 127) / 128;
+  int nsplit = 1;
+  while (nsplit < 8 && nsplit * 2 <= nblk && static_cast<int64_t>(b.num_q) * nsplit * 2 <= 152)
+    nsplit *= 2;
+  return nsplit;
+}
+
+// The partial results of tokens split over 4 or 8 CTAs (pairs combine
+// through distributed shared memory).
+size_t mla_workspace_bytes(const dsa_batch_t& b, int heads, int k) {
+  const int nsplit = mla_nsplit(b, k);
+  if (nsplit < 4) return 0;
+  return static_cast<size_t>(b.num_q) * nsplit * (static_cast<size_t>(heads) * 512 + 2 * heads) * 4;
+}
 
 cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void* kv,
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
-                              const dsa_batch_t& b, void* out, float* lse, void*, size_t,
+                              const dsa_batch_t& b, void* out, float* lse, void* ws, size_t ws_bytes,
                               int* status, cudaStream_t stream, bool kv_fp8, bool direct_rows) {
   if (b.num_q == 0) return cudaSuccess;
   CUtensorMap ql, qr;
@@ -798,12 +862,11 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   p.lse = lse;
   p.status = status;
   p.timeout_ns = wait_timeout_ns();
-  // Split each token's blocks over a cluster when there are too few tokens
-  // to cover the SMs (decode).
-  const int nblk = (k + 127) / 128;
-  int nsplit = 1;
-  while (nsplit < 8 && nsplit * 2 <= nblk && static_cast<int64_t>(b.num_q) * nsplit * 2 <= 152)
-    nsplit *= 2;
+  const int nsplit = mla_nsplit(b, k);
+  if (nsplit >= 4) {  // the partial results go through the workspace
+    if (!ws || ws_bytes < mla_workspace_bytes(b, heads, k)) return cudaErrorInvalidValue;
+    p.part = static_cast<float*>(ws);
+  }
   const bool paged = b.block_table != nullptr && !direct_rows;
   if (kv_fp8) {  // FP8 KV rows: the model's 64 heads only
     if (heads != 64) return cudaErrorNotSupported;

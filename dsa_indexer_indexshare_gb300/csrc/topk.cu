@@ -1071,11 +1071,12 @@ __global__ void __launch_bounds__(kFinBS, 1) topk_resolve_write_kernel(BatchArgs
 
 // Rows beyond 16K positions: fewer than kRowsFew of them are spread over
 // several CTAs each (the launches above); more get a persistent CTA per SM,
-// a row at a time (measured on GB300: 64 decode rows of ~115K positions take
-// 47 us there against 64 us on the sliced path, whose five launches and
-// per-row resolve cost more than the idle SMs save; 4 rows of 1M take 50 us
-// sliced).
-constexpr int kRowsFew = 32;
+// a row at a time.  Measured on GB300 with K = 2048 (top-K alone, chained
+// launches): 64 rows of ~115K positions take 34 us sliced against 37 us in
+// the persistent kernel, 96 rows 39 against 38, 128 rows 44 against 38
+// (where one pass of the persistent kernel covers them); 4 rows of 1M take
+// 31 us sliced.
+constexpr int kRowsFew = 80;
 
 bool use_long_path(const dsa_batch_t& b) {
   return b.num_q < kRowsFew && b.max_len > 16384;

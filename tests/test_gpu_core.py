@@ -92,13 +92,14 @@ def test_topk_bit_exact_short_rows(values):
 
 @pytest.mark.parametrize("values", ["ties", "gauss", "const", "signed_zeros"])
 def test_topk_bit_exact_long_rows(values):
-    # fewer than 32 rows beyond 16K positions: cutoff / capture / resolve /
-    # write launches (constant and 7-valued rows overflow the capture list
-    # and go to the fallback)
+    # fewer than 80 rows beyond 16K positions: cutoff / capture /
+    # resolve-and-write launches (constant and 7-valued rows overflow the
+    # capture list and go to the fallback); rows beyond 262,144 positions
+    # are sorted into order rather than compacted from a bitmap
     _topk_case([40000, 70001, 131072], [1, 1, 1], 2048, values, 3)
     _topk_case([1 << 20, 300000], [1, 1], 2048, values, 4)
-    # 31 rows: the same path; 103 rows: one persistent CTA per SM
-    _topk_case([20000, 17000, 131072], [20, 8, 3], 2048, values, 7)
+    # 79 rows: the same path; 103 rows: one persistent CTA per SM
+    _topk_case([20000, 17000, 131072], [40, 36, 3], 2048, values, 7)
     _topk_case([20000, 17000, 131072], [60, 40, 3], 2048, values, 8)
 
 
@@ -162,7 +163,12 @@ def test_mla_h64_k2048_gaussian_prefill():
 
 
 def test_mla_h64_decode_split_clusters():
+    # 4 tokens: clusters of 8 CTAs (partial results combined through L2; the
+    # short rows leave some CTAs without blocks)
     _mla_case([100000, 3000, 2047, 4100], [1, 1, 1, 1], 64, 2048, False, 7)
+    # 24 tokens: clusters of 4 CTAs
+    lens = [2100 + 157 * i for i in range(24)]
+    _mla_case(lens, [1] * 24, 64, 2048, False, 9, sample=[0, 5, 11, 23])
 
 
 def test_mla_holes_and_bad_index():
