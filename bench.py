@@ -50,10 +50,10 @@ DESCR = {
 # ncu DRAM traffic of the dominant kernel (bytes per launch), with the hash of
 # the kernel sources it was measured on; ignored once the sources change.
 NCU_TRAFFIC = {
-    # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch (204.7 MB
+    # ncu dram read+write of sparse_mla_kernel<64,1> on the 2560-token prefill launch (204.5 MB
     # read + 124.8 MB written), scaled by tokens to the 8192-token launch (q/out traffic is per
     # token; the kv cache is a few MB)
-    "sparse_mla": {"bytes": 1.0543e+09, "workload": "prefill8k", "src": "2547eeaef5193321"},
+    "sparse_mla": {"bytes": 1.0536e+09, "workload": "prefill8k", "src": "d31f87c4c5d50817"},
 }
 
 def kernel_src_hash(files):
