@@ -103,6 +103,12 @@ struct MlaParams {
   float* part;
   int* status;
   uint64_t timeout_ns;
+  // launched right after another of the library's kernels of the group call
+  // (none of which writes the batch metadata or the queries): the token's
+  // metadata, the barrier and TMEM set-up and the query load run before the
+  // wait for that kernel, everything that reads the indices or the cache or
+  // writes memory after it
+  int early_inputs;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -167,8 +173,8 @@ template <int H, int NSPLIT, bool PAGED, bool KV8>
 __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap qlat_map,
                       const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
-  chain_wait();     // the previous kernel of the stream has completed
-  chain_release();  // the next one may be scheduled
+  if (!p.early_inputs) chain_wait();  // the previous kernel of the stream has completed
+  chain_release();                    // the next one may be scheduled
   using C = MlaCfg<H>;
   constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
   // split tokens combine their partial results through L2 for 4 or 8 CTAs
@@ -204,6 +210,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   const int64_t row0 = p.direct ? 0 : seq_base_row(p.b, seq);
   const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.K;
   if (nb == 0) {  // nothing visible: zero output, lse = -inf
+    if (p.early_inputs) chain_wait();
     constexpr int DS = 512 / NSPLIT;
     for (int i = tid; i < H * DS; i += NT) {
       const int h = i / DS, d = rank * DS + i % DS;
@@ -276,14 +283,16 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   const uint32_t tbase = *tslot;
   const uint64_t to = p.timeout_ns;
   volatile int no_abort = 0;
+  if (warp == W_QK && lane == 0) {  // Q of the token, once, by TMA
+    mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
+    for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, t * H, bar(B_Q));
+    tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, t * H, bar(B_Q));
+  }
+  if (p.early_inputs) chain_wait();  // before the indices, the cache rows and any write
 
   if (warp == W_QK) {
     // ------------------------------------------------ QK issuer: S^T = C . Q^T per block
     if (lane == 0) {
-      // Q of the token, once, by TMA
-      mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
-      for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, t * H, bar(B_Q));
-      tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, t * H, bar(B_Q));
       constexpr uint32_t id_qk = idesc_bf16(128, H, false, false);
       bool ok = mbar_wait(bar(B_Q), 0, abort_flag, p.status, to);
       for (int j = j0; ok && j < j1; ++j) {
@@ -839,7 +848,8 @@ size_t mla_workspace_bytes(const dsa_batch_t& b, int heads, int k) {
 cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void* kv,
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
                               const dsa_batch_t& b, void* out, float* lse, void* ws, size_t ws_bytes,
-                              int* status, cudaStream_t stream, bool kv_fp8, bool direct_rows) {
+                              int* status, cudaStream_t stream, bool kv_fp8, bool direct_rows,
+                              bool after_own_kernel) {
   if (b.num_q == 0) return cudaSuccess;
   CUtensorMap ql, qr;
   const uint64_t qrows = static_cast<uint64_t>(b.num_q) * heads;
@@ -862,6 +872,7 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   p.lse = lse;
   p.status = status;
   p.timeout_ns = wait_timeout_ns();
+  p.early_inputs = after_own_kernel ? 1 : 0;
   const int nsplit = mla_nsplit(b, k);
   if (nsplit >= 4) {  // the partial results go through the workspace
     if (!ws || ws_bytes < mla_workspace_bytes(b, heads, k)) return cudaErrorInvalidValue;

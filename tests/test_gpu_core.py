@@ -103,6 +103,18 @@ def test_topk_bit_exact_long_rows(values):
     _topk_case([20000, 17000, 131072], [60, 40, 3], 2048, values, 8)
 
 
+@pytest.mark.parametrize("values", ["ties", "gauss"])
+def test_topk_bit_exact_sort_widths(values):
+    # the ordered write's sort at each width: few long rows (512 threads)
+    # with K = 300 (one entry per thread) and 4096 (eight); the persistent
+    # kernel (1024 threads, 80 rows) on a row beyond its 917,504-position
+    # bitmap (two entries per thread at K = 2048).  Integer rows overflow
+    # the few-rows capture and take the persistent kernel's sort instead.
+    _topk_case([300000, 270000], [1, 1], 300, values, 11)
+    _topk_case([300000, 270000], [1, 1], 4096, values, 12)
+    _topk_case([1000000] + [20000] * 79, [1] * 80, 2048, values, 13)
+
+
 @pytest.mark.parametrize("values", ["ties", "gauss", "const", "signed_zeros"])
 def test_topk_bit_exact_many_long_rows(values):
     # hundreds of rows beyond 16K positions: one persistent CTA per SM, two
