@@ -60,8 +60,8 @@ struct MlaCfg {
   static constexpr int OFF_C = OFF_Q + Q_BYTES;
   static constexpr int OFF_P = OFF_C + 8 * CSUB;  // the RoPE sub-tile
   static constexpr int OFF_SCR = OFF_C + 9 * CSUB;
-  // scratch (floats): m_used[H], red[4][H], lsum[H], fac[8][H]; flags[NSW]
-  static constexpr int SCR_FLOATS = H + 4 * H + H + 8 * H;
+  // scratch (floats): m_used[H], red[4][H], lsum[H], fac[16][H]; flags[NSW]
+  static constexpr int SCR_FLOATS = H + 4 * H + H + 16 * H;
   static constexpr int OFF_FLAGS = OFF_SCR + SCR_FLOATS * 4;
   static constexpr int OFF_BAR = (OFF_FLAGS + 4 * 8 + 7) & ~7;
   static constexpr int NBAR = 1 + 4 + 4 + 4;
@@ -97,7 +97,7 @@ struct MlaParams {
   float scale_log2;
   uint16_t* out;
   float* lse;
-  // tokens split over 4 or 8 CTAs: partial results of CTA r of token t at
+  // tokens split over 4, 8 or 16 CTAs: partial results of CTA r of token t at
   // part + (t * NSPLIT + r) * (H * 512 + 2 * H): O^T as [h][512], then the
   // running maxima and the row sums of the H heads
   float* part;
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   chain_release();                    // the next one may be scheduled
   using C = MlaCfg<H>;
   constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
-  // split tokens combine their partial results through L2 for 4 or 8 CTAs
+  // split tokens combine their partial results through L2 for 4 to 16 CTAs
   // (each CTA would read 128 KB through the cluster, at ~35 GB/s per SM),
   // through distributed shared memory for 2 (half of it local)
   constexpr bool kMergeL2 = NSPLIT >= 4;
@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     named_bar_sync(1, NST);
     if (tid < H) lsum[tid] = (red[tid] + red[H + tid]) + (red[2 * H + tid] + red[3 * H + tid]);
     // the unnormalised O^T of this CTA as [h][512]: staged in shared memory,
-    // or for a token split over 4 or 8 CTAs written with the running maxima
+    // or for a token split over 4 to 16 CTAs written with the running maxima
     // and the row sums to the token's partial results in global memory
     // (zeros for a CTA without blocks), which the cluster combines through L2
     const bool have = j1 > j0 && mbar_wait(bar(B_O), 0, abort_flag, p.status, to);
@@ -799,6 +799,8 @@ cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaPa
   cudaGetDevice(&dev);
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess && NSPLIT > 8)  // 16 CTAs per cluster: beyond the portable size
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
@@ -820,8 +822,10 @@ cudaError_t launch_h(const CUtensorMap& ql, const CUtensorMap& qr, const MlaPara
                          : launch_mla<H, 2, false, KV8>(ql, qr, p, stream);
     case 4: return paged ? launch_mla<H, 4, true, KV8>(ql, qr, p, stream)
                          : launch_mla<H, 4, false, KV8>(ql, qr, p, stream);
-    default: return paged ? launch_mla<H, 8, true, KV8>(ql, qr, p, stream)
-                          : launch_mla<H, 8, false, KV8>(ql, qr, p, stream);
+    case 8: return paged ? launch_mla<H, 8, true, KV8>(ql, qr, p, stream)
+                         : launch_mla<H, 8, false, KV8>(ql, qr, p, stream);
+    default: return paged ? launch_mla<H, 16, true, KV8>(ql, qr, p, stream)
+                          : launch_mla<H, 16, false, KV8>(ql, qr, p, stream);
   }
 }
 
@@ -834,10 +838,14 @@ int mla_nsplit(const dsa_batch_t& b, int k) {
   int nsplit = 1;
   while (nsplit < 8 && nsplit * 2 <= nblk && static_cast<int64_t>(b.num_q) * nsplit * 2 <= 152)
     nsplit *= 2;
+  // 16 CTAs per token while the launch is at most four such clusters, all
+  // resident at once (measured, K = 2048: 4 tokens 23.0 -> 21.2 us per layer;
+  // 8 tokens' eight 16-CTA clusters did not fit together: 24.7 -> 37.0 us)
+  if (nsplit == 8 && 16 <= nblk && static_cast<int64_t>(b.num_q) * 16 <= 64) nsplit = 16;
   return nsplit;
 }
 
-// The partial results of tokens split over 4 or 8 CTAs (pairs combine
+// The partial results of tokens split over 4 to 16 CTAs (pairs combine
 // through distributed shared memory).
 size_t mla_workspace_bytes(const dsa_batch_t& b, int heads, int k) {
   const int nsplit = mla_nsplit(b, k);

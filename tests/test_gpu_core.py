@@ -175,9 +175,11 @@ def test_mla_h64_k2048_gaussian_prefill():
 
 
 def test_mla_h64_decode_split_clusters():
-    # 4 tokens: clusters of 8 CTAs (partial results combined through L2; the
-    # short rows leave some CTAs without blocks)
+    # 4 tokens: clusters of 16 CTAs (partial results combined through L2;
+    # the short rows leave some CTAs without blocks)
     _mla_case([100000, 3000, 2047, 4100], [1, 1, 1, 1], 64, 2048, False, 7)
+    # 6 tokens: clusters of 8 CTAs
+    _mla_case([3000 + 517 * i for i in range(6)], [1] * 6, 64, 2048, False, 10)
     # 24 tokens: clusters of 4 CTAs
     lens = [2100 + 157 * i for i in range(24)]
     _mla_case(lens, [1] * 24, 64, 2048, False, 9, sample=[0, 5, 11, 23])
