@@ -205,7 +205,7 @@ DSA_API dsa_status_t dsa_indexer_scores(const void* q_idx, const float* q_scale,
  * -0.0 equals +0.0 (a tie, so the lower position wins); a NaN whose sign bit
  * is clear ranks above +inf and one whose sign bit is set below -inf.
  * ws: dsa_topk_workspace_size (the status
- * block, plus about 128 KB of scratch per row for batches of fewer than 32
+ * block, plus about 128 KB of scratch per row for batches of fewer than 80
  * rows longer than 16K positions).
  */
 DSA_API size_t dsa_topk_workspace_size(const dsa_batch_t* b, int32_t k);
@@ -231,7 +231,10 @@ DSA_API dsa_status_t dsa_topk(const float* scores, const dsa_batch_t* b, int32_t
  *   heads in {16, 64}; 1 <= k <= 4096 (slots are processed in blocks of 128,
  *   the last one masked).  Softmax statistics are fp32; P is
  *   rounded to bf16 for the P.V product (fp32 accumulation).
- * ws: dsa_sparse_mla_workspace_size.
+ * ws: dsa_sparse_mla_workspace_size: the status block, plus, when there are
+ * few enough queries for each to be split over 4 or more CTAs (decode), their
+ * fp32 partial results (num_q * split * heads * 514 * 4 bytes: 4.2 MB for 4
+ * queries of 64 heads split 16 ways).
  */
 DSA_API size_t dsa_sparse_mla_workspace_size(const dsa_batch_t* b, int32_t heads, int32_t k);
 DSA_API dsa_status_t dsa_sparse_mla_attn(const void* q_lat, const void* q_rope, const void* kv,
@@ -253,7 +256,8 @@ DSA_API dsa_status_t dsa_sparse_mla_attn(const void* q_lat, const void* q_rope, 
  * layers are ignored (may be NULL).  lse[l] may be NULL.
  * idx_buf: int32 [num_q, k], caller-owned; after the call it holds the
  * indices of the last F layer.  The workspace holds the status block and the
- * fp32 score matrix; size from dsa_group_workspace_size.
+ * fp32 score matrix with the top-K scratch, whose space the attention's
+ * partial results reuse afterwards; size from dsa_group_workspace_size.
  * For a prefill (some sequence with more than one query) whose rows exceed
  * 16K positions (up to 2M), an F layer selects without writing the score
  * matrix ("GLM-5.2 架构深度拆解" CH 2.2, the top-2048, and CH 4.4; "GLM-5 ->
