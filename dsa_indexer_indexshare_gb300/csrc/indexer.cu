@@ -321,16 +321,18 @@ __global__ void __launch_bounds__(IdxCfg<NTOK, FP8, STAGES, MODE>::NT, 1)
         tmem_wait_ld_dep(v);
         if (n < nq) {
           const float4* wv = reinterpret_cast<const float4*>(sW + n * 32);
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          // four running sums (heads j = 0, 1, 2, 3 mod 4), two per packed
+          // f32x2 fma: each lane rounds exactly as a scalar fma would
+          float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
             const float4 ww = wv[j4];
-            a0 = fmaf(ww.x, fmaxf(v[4 * j4 + 0], 0.f), a0);
-            a1 = fmaf(ww.y, fmaxf(v[4 * j4 + 1], 0.f), a1);
-            a2 = fmaf(ww.z, fmaxf(v[4 * j4 + 2], 0.f), a2);
-            a3 = fmaf(ww.w, fmaxf(v[4 * j4 + 3], 0.f), a3);
+            a01 = __ffma2_rn(make_float2(ww.x, ww.y),
+                             make_float2(fmaxf(v[4 * j4 + 0], 0.f), fmaxf(v[4 * j4 + 1], 0.f)), a01);
+            a23 = __ffma2_rn(make_float2(ww.z, ww.w),
+                             make_float2(fmaxf(v[4 * j4 + 2], 0.f), fmaxf(v[4 * j4 + 3], 0.f)), a23);
           }
-          float sc = (a0 + a1) + (a2 + a3);
+          float sc = (a01.x + a01.y) + (a23.x + a23.y);
           if (FP8) sc *= kscale;
           if constexpr (MODE == kIdxScores) {
             if (s > pn) sc = -INFINITY;
