@@ -701,6 +701,8 @@ def main():
     ap.add_argument("--workload", default="prefill8k", choices=list(DESCR))
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-slots", type=int, default=3,
+                    help="buffer sets of the end-to-end leg (uploads / group call / read-back overlap)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0)
     ap.add_argument("--with-append", action="store_true",
@@ -934,7 +936,7 @@ def e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, worl
     rows_dev = torch.from_numpy(rows_new).to(dev)
     if phys is not None:  # paged caches: the physical rows of those positions
         rows_dev = phys.index_select(0, rows_dev)
-    NSLOT = 3
+    NSLOT = max(2, args.e2e_slots)
     slots = []
     for sl in range(NSLOT):
         if sl == 0:
@@ -1003,7 +1005,7 @@ def e2e_arm(dsa, group, batch, layers, idx_buf, ws, lay, args, dev, stream, worl
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms / steps, 3),
             "inputs": "per-query tensors + the cache rows of the step's tokens",
-            "pipelining": "three buffer sets; uploads, group call and read-back on three streams"}
+            "pipelining": f"{NSLOT} buffer sets; uploads, group call and read-back on three streams"}
 
 
 def reference_arm(args):
