@@ -1046,9 +1046,26 @@ __global__ void __launch_bounds__(kFinBS, 1) topk_resolve_write_kernel(BatchArgs
     if (tid == 0) cnt[6] = 1;
     return;
   }
-  for (int i = tid; i < n; i += kFinBS) {
-    ckey[i] = ws.ckey[static_cast<int64_t>(t) * kCandCap + i];
-    cpos[i] = ws.cpos[static_cast<int64_t>(t) * kCandCap + i];
+  // the list into shared memory, 8 entries per thread requested before any is stored
+  for (int i0 = tid; i0 < n; i0 += 8 * kFinBS) {
+    uint32_t kk[8];
+    int32_t pp[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kFinBS;
+      if (i < n) {
+        kk[u] = ws.ckey[static_cast<int64_t>(t) * kCandCap + i];
+        pp[u] = ws.cpos[static_cast<int64_t>(t) * kCandCap + i];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kFinBS;
+      if (i < n) {
+        ckey[i] = kk[u];
+        cpos[i] = pp[u];
+      }
+    }
   }
   for (int i = tid; i < kHBins; i += kFinBS) h[i] = 0;
   if (tid == 0) s_taken = 0;
@@ -1293,15 +1310,35 @@ __global__ void __launch_bounds__(kFinBS) topk_list_resolve_write_kernel(BatchAr
     if (tid == 0) cnt[6] = 1;
     return;
   }
-  // gather: warp w copies cells w, w + warps, ... (each cell's entries are contiguous)
-  {
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int c = warp; c < ncell; c += kFinBS / 32) {
-      const int m = min(segcnt[c], segq), o = s_segoff[c];
-      const int64_t src = static_cast<int64_t>(t) * kTopkCandCap + static_cast<int64_t>(c) * segq;
-      for (int j = lane; j < m; j += 32) {
-        ckey[o + j] = ls.ckey[src + j];
-        cpos[o + j] = ls.cpos[src + j];
+  // gather: entry o of the gathered list lies in the last cell c with
+  // s_segoff[c] <= o (a binary search; empty cells share their successor's
+  // offset), at position o - s_segoff[c] of that cell's segment; 8 entries
+  // per thread are requested before any is stored
+  for (int o0 = tid; o0 < n; o0 += 8 * kFinBS) {
+    uint32_t kk[8];
+    int32_t pp[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int o = o0 + u * kFinBS;
+      if (o < n) {
+        int lo = 0, hi = ncell - 1;  // s_segoff[lo] <= o
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_segoff[mid] <= o) lo = mid;
+          else hi = mid - 1;
+        }
+        const int64_t src = static_cast<int64_t>(t) * kTopkCandCap + static_cast<int64_t>(lo) * segq +
+                            (o - s_segoff[lo]);
+        kk[u] = ls.ckey[src];
+        pp[u] = ls.cpos[src];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int o = o0 + u * kFinBS;
+      if (o < n) {
+        ckey[o] = kk[u];
+        cpos[o] = pp[u];
       }
     }
   }
