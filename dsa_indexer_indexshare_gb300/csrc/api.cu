@@ -488,7 +488,8 @@ dsa_status_t indexshare_group_forward(const dsa_group_t* g, const dsa_batch_t* b
             launch_sparse_mla(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, idx_buf, g->k,
                               g->heads, g->scale, *b, g->out[l], g->lse ? g->lse[l] : nullptr,
                               w.mla_extra, w.mla_extra_bytes, w.status, stream, kv_fp8, false,
-                              true),  // after the group's own F-layer or attention kernels
+                              true,  // after the group's own F-layer or attention kernels
+                              g->layer_types[l] == 'S'),  // right after the previous layer's
             "sparse MLA launch"))
       return s;
   }
@@ -639,7 +640,7 @@ dsa_status_t indexshare_group_forward_hot(const dsa_group_t* g, const dsa_batch_
             launch_sparse_mla(g->q_lat[l], g->q_rope[l], g->kv[l], g->kv_rows, hot->rows, g->k,
                               g->heads, g->scale, *b, g->out[l], g->lse ? g->lse[l] : nullptr,
                               w.mla_extra, w.mla_extra_bytes, w.status, stream, kv_fp8, true,
-                              true),
+                              true, g->layer_types[l] == 'S'),
             "sparse MLA launch"))
       return s;
   }

@@ -190,7 +190,7 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
                               const dsa_batch_t& b, void* out, float* lse, void* ws_extra,
                               size_t ws_extra_bytes, int* status, cudaStream_t stream,
                               bool kv_fp8 = false, bool direct_rows = false,
-                              bool after_own_kernel = false);
+                              bool after_own_kernel = false, bool after_attention = false);
 // Hot / cold KV: the plan of one step (one CTA per sequence) and the swap-in
 // of its fetch lists for `layers` layers from host-resident cold caches.
 cudaError_t launch_hot_plan(const int32_t* idx, int k, const dsa_batch_t& b, const dsa_hot_t& h,

@@ -107,8 +107,14 @@ struct MlaParams {
   // (none of which writes the batch metadata or the queries): the token's
   // metadata, the barrier and TMEM set-up and the query load run before the
   // wait for that kernel, everything that reads the indices or the cache or
-  // writes memory after it
+  // writes memory after it.  This kernel lets the next one be scheduled only
+  // after its own wait, so a kernel launched after it finds every kernel two
+  // or more places back in the stream complete.
   int early_inputs;
+  // (with early_inputs) launched right after another attention launch, whose
+  // predecessor wrote the indices and the cache rows if anything did: the
+  // first block's indices and its gather are issued before the wait too
+  int early_gather;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -173,8 +179,10 @@ template <int H, int NSPLIT, bool PAGED, bool KV8>
 __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap qlat_map,
                       const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
-  if (!p.early_inputs) chain_wait();  // the previous kernel of the stream has completed
-  chain_release();                    // the next one may be scheduled
+  if (!p.early_inputs) {
+    chain_wait();     // the previous kernel of the stream has completed
+    chain_release();  // the next one may be scheduled
+  }
   using C = MlaCfg<H>;
   constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
   // split tokens combine their partial results through L2 for 4 to 16 CTAs
@@ -210,7 +218,10 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   const int64_t row0 = p.direct ? 0 : seq_base_row(p.b, seq);
   const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.K;
   if (nb == 0) {  // nothing visible: zero output, lse = -inf
-    if (p.early_inputs) chain_wait();
+    if (p.early_inputs) {
+      chain_wait();
+      chain_release();
+    }
     constexpr int DS = 512 / NSPLIT;
     for (int i = tid; i < H * DS; i += NT) {
       const int h = i / DS, d = rank * DS + i % DS;
@@ -288,7 +299,10 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, t * H, bar(B_Q));
     tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, t * H, bar(B_Q));
   }
-  if (p.early_inputs) chain_wait();  // before the indices, the cache rows and any write
+  if (p.early_inputs && !p.early_gather) {  // before the indices, the cache rows and any write
+    chain_wait();
+    chain_release();
+  }
 
   if (warp == W_QK) {
     // ------------------------------------------------ QK issuer: S^T = C . Q^T per block
@@ -505,6 +519,10 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
           signal(g);
         }
       }
+    }
+    if (p.early_gather) {  // the first block is under way; the rest follows the wait
+      chain_wait();
+      chain_release();
     }
 
     int e_next = (j0 * 128 + key < nvalid && j0 < j1) ? idx_row[j0 * 128 + key] : -1;
@@ -857,7 +875,7 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,
                               const dsa_batch_t& b, void* out, float* lse, void* ws, size_t ws_bytes,
                               int* status, cudaStream_t stream, bool kv_fp8, bool direct_rows,
-                              bool after_own_kernel) {
+                              bool after_own_kernel, bool after_attention) {
   if (b.num_q == 0) return cudaSuccess;
   CUtensorMap ql, qr;
   const uint64_t qrows = static_cast<uint64_t>(b.num_q) * heads;
@@ -881,6 +899,7 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   p.status = status;
   p.timeout_ns = wait_timeout_ns();
   p.early_inputs = after_own_kernel ? 1 : 0;
+  p.early_gather = after_own_kernel && after_attention ? 1 : 0;
   const int nsplit = mla_nsplit(b, k);
   if (nsplit >= 4) {  // the partial results go through the workspace
     if (!ws || ws_bytes < mla_workspace_bytes(b, heads, k)) return cudaErrorInvalidValue;
