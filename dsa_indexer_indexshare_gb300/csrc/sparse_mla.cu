@@ -104,12 +104,12 @@ struct MlaParams {
   int* status;
   uint64_t timeout_ns;
   // launched right after another of the library's kernels of the group call
-  // (none of which writes the batch metadata or the queries): the token's
-  // metadata, the barrier and TMEM set-up and the query load run before the
-  // wait for that kernel, everything that reads the indices or the cache or
-  // writes memory after it.  This kernel lets the next one be scheduled only
-  // after its own wait, so a kernel launched after it finds every kernel two
-  // or more places back in the stream complete.
+  // (none of which writes the batch metadata): the token's metadata and the
+  // barrier and TMEM set-up run before the wait for that kernel; the query
+  // load (in a model the kernel just before would produce the queries), the
+  // indices, the cache rows and every write after it.  This kernel lets the
+  // next one be scheduled only after its own wait, so a kernel launched after
+  // it finds every kernel two or more places back in the stream complete.
   int early_inputs;
   // (with early_inputs) launched right after another attention launch, whose
   // predecessor wrote the indices and the cache rows if anything did: the
@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   const uint64_t to = p.timeout_ns;
   volatile int no_abort = 0;
   if (warp == W_QK && lane == 0) {  // Q of the token, once, by TMA
+    if (p.early_inputs) chain_wait();
     mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
     for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, t * H, bar(B_Q));
     tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, t * H, bar(B_Q));
