@@ -111,9 +111,12 @@ struct MlaParams {
   // next one be scheduled only after its own wait, so a kernel launched after
   // it finds every kernel two or more places back in the stream complete.
   int early_inputs;
-  // (with early_inputs) launched right after another attention launch, whose
-  // predecessor wrote the indices and the cache rows if anything did: the
-  // first block's indices and its gather are issued before the wait too
+  // (with early_inputs, bf16 rows) launched right after another attention
+  // launch, whose predecessor wrote the indices and the cache rows if
+  // anything did: the first block's indices, and its rows of positions before
+  // the sequence's first query of the call, are gathered before the wait too
+  // (in a model those exist before the layer starts; the call's own new rows
+  // come from the layer's projection just before it and follow the wait)
   int early_gather;
 };
 
@@ -213,6 +216,8 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   if (t >= qe) return;  // uniform over the cluster
   const int pos = query_pos(p.b, t, (tid == 0 && rank == 0) ? p.status : nullptr);
   const int nvalid = pos < 0 ? 0 : min(p.K, pos + 1);
+  // first position this call adds to the sequence (its first query's)
+  const int first_new = p.early_gather ? (t == qs ? pos : query_pos(p.b, qs, nullptr)) : 0;
   const int nb = (nvalid + 127) / 128;
   const int j0 = rank * nb / NSPLIT, j1 = (rank + 1) * nb / NSPLIT;  // this CTA's blocks
   const int64_t row0 = p.direct ? 0 : seq_base_row(p.b, seq);
@@ -401,14 +406,17 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         grow[c] = ok ? static_cast<int>(rr) : 0;
       }
     };
-    auto issue = [&](int i) {
+    // rows rb + GROW * c of sub-tile i for the c set in `rows`
+    auto issue_rows = [&](int i, uint32_t rows) {
       const uint32_t dst = gdst0 + i * C::CSUB;
 #pragma unroll
       for (int c = 0; c < RPT; ++c)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + c * GROW * 128),
-                     "l"(kvk + static_cast<int64_t>(grow[c]) * 576 + 64 * i)
-                     : "memory");
+        if ((rows >> c) & 1u)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + c * GROW * 128),
+                       "l"(kvk + static_cast<int64_t>(grow[c]) * 576 + 64 * i)
+                       : "memory");
     };
+    auto issue = [&](int i) { issue_rows(i, (1u << RPT) - 1u); };
     // ---- FP8 KV rows: a group's codes (128 keys x 128 dims, 16 KB) are staged
     // unswizzled in its second sub-tile, its rows' scales in a 2 KB area,
     // then the threads that copied them expand them in place to the swizzled
@@ -512,16 +520,34 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
 #pragma unroll 1
         for (int g = 0; g < 4; ++g) convert8(g, 3 - g);
       } else {
+        // rows of this call's new positions (at or after the sequence's first
+        // query) wait for the previous kernel when gathering early
+        uint32_t late = 0;
+        if (p.early_gather)
+#pragma unroll
+          for (int c = 0; c < RPT; ++c)
+            if (gsel[c] >= first_new) late |= 1u << c;
+        const uint32_t early = ((1u << RPT) - 1u) & ~late;
 #pragma unroll 1
         for (int g = 0; g < 4; ++g) {
-          issue(2 * g);
-          issue(2 * g + 1);
-          if (g == 3) issue(8);
+          issue_rows(2 * g, early);
+          issue_rows(2 * g + 1, early);
+          if (g == 3) issue_rows(8, early);
+        }
+        if (p.early_gather) {
+          chain_wait();
+          chain_release();
+        }
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          issue_rows(2 * g, late);
+          issue_rows(2 * g + 1, late);
+          if (g == 3) issue_rows(8, late);
           signal(g);
         }
       }
     }
-    if (p.early_gather) {  // the first block is under way; the rest follows the wait
+    if (p.early_gather && j0 >= j1) {
       chain_wait();
       chain_release();
     }
@@ -900,7 +926,7 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
   p.status = status;
   p.timeout_ns = wait_timeout_ns();
   p.early_inputs = after_own_kernel ? 1 : 0;
-  p.early_gather = after_own_kernel && after_attention ? 1 : 0;
+  p.early_gather = after_own_kernel && after_attention && !kv_fp8 ? 1 : 0;
   const int nsplit = mla_nsplit(b, k);
   if (nsplit >= 4) {  // the partial results go through the workspace
     if (!ws || ws_bytes < mla_workspace_bytes(b, heads, k)) return cudaErrorInvalidValue;
