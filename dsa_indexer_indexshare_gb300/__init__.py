@@ -80,6 +80,7 @@ def _load():
         "dsa_launch_counts": (c_int, [POINTER(c_uint64), c_int]),
         "dsa_launch_counts_reset": (None, []),
         "dsa_set_wait_timeout_ns": (None, [c_uint64]),
+        "dsa_set_mla_persistent": (None, [c_int]),
         "dsa_profile_enable": (None, [c_int]),
         "dsa_profile_collect": (c_int, [POINTER(ctypes.c_double), POINTER(c_uint64), c_int]),
         "dsa_selftest_wait_timeout": (st, [c_void_p, c_size_t, c_void_p]),
@@ -236,6 +237,12 @@ def dsa_profile_collect() -> dict:
 
 def set_wait_timeout_ns(ns: int):
     lib.dsa_set_wait_timeout_ns(int(ns))
+
+
+def set_mla_persistent(on: bool):
+    """Sparse attention over many tokens on a persistent grid (default) or one
+    CTA per token; both give bit-identical results."""
+    lib.dsa_set_mla_persistent(1 if on else 0)
 
 
 def dsa_selftest_wait_timeout(ws: torch.Tensor, stream=None):

@@ -357,6 +357,8 @@ void dsa_launch_counts_reset(void) {
 
 void dsa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
 
+void dsa_set_mla_persistent(int on) { set_mla_persistent(on != 0); }
+
 void dsa_profile_enable(int on) { g_prof_on.store(on ? 1 : 0); }
 
 int dsa_profile_collect(double* ms, uint64_t* launches, int n) {

@@ -184,6 +184,8 @@ cudaError_t launch_indexer_topk_select(const void* q_idx, const float* q_scale, 
 size_t topk_scratch_bytes(const dsa_batch_t& b, int k);
 cudaError_t launch_topk(const float* scores, const dsa_batch_t& b, int k, int32_t* idx,
                         int* status, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+// Prefill-sized attention launches on a persistent grid (default on).
+void set_mla_persistent(bool on);
 size_t mla_workspace_bytes(const dsa_batch_t& b, int heads, int k);
 cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void* kv,
                               int64_t kv_rows, const int32_t* idx, int k, int heads, float scale,

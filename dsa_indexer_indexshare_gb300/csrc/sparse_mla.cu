@@ -36,6 +36,8 @@
 // queued MMAs have drained, so one issuer waiting for gathered data would
 // empty the tensor pipe every time.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -124,6 +126,35 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Per-head reduction over the 32 keys (lanes) of a warp, N heads per lane, as
+// a transposing butterfly: at distance 16 each lane keeps half of its heads
+// and trades the other half with its partner, then the same at distance 8 on
+// the half it kept, down to distance 1: 31 shuffles for 32 heads instead of
+// 5 per head.  Each level combines the same two partial results as the plain
+// xor butterfly, so sums come out bit for bit the same.  On return v[0] holds
+// the result for head lane (N = 32) or lane / 2 (N = 16).
+template <int N, int OFF, bool MAX>
+__device__ __forceinline__ void head_reduce(float* v, int lane) {
+  if constexpr (OFF >= 1) {
+    if constexpr (N > 1) {
+      constexpr int HF = N / 2;
+      const bool up = (lane & OFF) != 0;
+#pragma unroll
+      for (int i = 0; i < HF; ++i) {
+        const float keep = up ? v[i + HF] : v[i];
+        const float give = up ? v[i] : v[i + HF];
+        const float got = __shfl_xor_sync(0xffffffffu, give, OFF);
+        v[i] = MAX ? fmaxf(keep, got) : keep + got;
+      }
+      head_reduce<HF, OFF / 2, MAX>(v, lane);
+    } else {
+      const float got = __shfl_xor_sync(0xffffffffu, v[0], OFF);
+      v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+      head_reduce<1, OFF / 2, MAX>(v, lane);
+    }
+  }
 }
 
 template <int NV>
@@ -592,13 +623,9 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         // first block): exact per-head maximum over the valid keys
         tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);  // raw scores again
 #pragma unroll
-        for (int h = 0; h < HW; ++h) {
-          d[h] *= sl2;
-          float v = valid ? d[h] : -INFINITY;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-          if (lane == 0) red[quarter * H + h0 + h] = v;
-        }
+        for (int h = 0; h < HW; ++h) d[h] = valid ? d[h] * sl2 : -INFINITY;
+        head_reduce<HW, 16, true>(d, lane);
+        if (HW == 32 || (lane & 1) == 0) red[quarter * H + h0 + (HW == 32 ? lane : lane >> 1)] = d[0];
         named_bar_sync(1, NST);
         if (tid < H) {
           const float mo = m_used[tid];
@@ -608,11 +635,12 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
           m_used[tid] = mn;
         }
         named_bar_sync(1, NST);
+        tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);  // and once more for the exponents
 #pragma unroll
         for (int h = 0; h < HW; ++h) {
           mneg[h] = -m_used[h0 + h];
           lpart[h] *= fac[h0 + h];
-          d[h] += mneg[h];
+          d[h] = fmaf(d[h], sl2, mneg[h]);
         }
         if (u > 0) {  // O^T rows of this thread: dims 128c + key, 16 heads at a time
 #pragma unroll 1
@@ -693,13 +721,8 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     // row sums over the 128 keys
-#pragma unroll
-    for (int h = 0; h < HW; ++h) {
-      float v = lpart[h];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) red[quarter * H + h0 + h] = v;
-    }
+    head_reduce<HW, 16, false>(lpart, lane);
+    if (HW == 32 || (lane & 1) == 0) red[quarter * H + h0 + (HW == 32 ? lane : lane >> 1)] = lpart[0];
     named_bar_sync(1, NST);
     if (tid < H) lsum[tid] = (red[tid] + red[H + tid]) + (red[2 * H + tid] + red[3 * H + tid]);
     // the unnormalised O^T of this CTA as [h][512]: staged in shared memory,
@@ -834,6 +857,455 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Prefill-sized launches (many tokens, 64 heads, bf16 rows of per-sequence
+// contiguous caches that L2 holds, one CTA per token): a persistent grid,
+// one CTA per SM, each walking a list of tokens.  A CTA per token pays, besides its blocks,
+// about 9.5 us of start-up and tail on GB300 (barrier and TMEM set-up,
+// metadata, the query and first gather, the pipeline fill, the output
+// written after the last product): about a sixth of an 8K prefill's
+// attention.  Here the next token's first block is gathered in the refill
+// slot of the current token's last block, its query is loaded by TMA as soon
+// as the current token's last QK product is done, and the current token's
+// output goes from TMEM straight to global memory (the C tile already holds
+// the next token's rows) while that token's first QK product runs.  The next
+// token's first P.V product, which overwrites O^T, waits for that token's
+// P, which the softmax warps give only after reading the previous O^T.
+// Per block the work is that of the kernel above, operation for operation,
+// so both give bit-identical results.
+constexpr int kMlaPersistMaxTokens = 256;  // tokens per CTA (one per softmax thread)
+
+template <int H>
+__global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
+    sparse_mla_persistent_kernel(const __grid_constant__ CUtensorMap qlat_map,
+                                 const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
+  using C = MlaCfg<H>;
+  static_assert(H == 64, "the persistent variant covers the 64-head model");
+  constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
+  constexpr int W_QK = NSW, W_PV = NSW + 1;
+  constexpr int GROW = NST / 8, RPT = 128 / GROW;
+  static_assert(NST == kMlaPersistMaxTokens, "one list entry per softmax thread");
+  // the token list {t, pos, first cache row (lo, hi)} reuses the block-table
+  // and FP8-scale areas, which this variant does not use
+  static_assert(C::OFF_KSC + 128 * 16 - C::OFF_TAB >= kMlaPersistMaxTokens * 16, "token list");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sQ = smem_u32(sm + C::OFF_Q);
+  const uint32_t sC = smem_u32(sm + C::OFF_C);
+  float* m_used = reinterpret_cast<float*>(sm + C::OFF_SCR);
+  float* red = m_used + H;
+  float* fac = red + 4 * H + H;
+  int* flags = reinterpret_cast<int*>(sm + C::OFF_FLAGS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC + 8);
+  int* wcnt = reinterpret_cast<int*>(sm + C::OFF_MISC + 16);  // list entries per softmax warp
+  int4* toks = reinterpret_cast<int4*>(sm + C::OFF_TAB);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const int B_Q = 0, B_CFULL = 1, B_CFREE = 5, B_S = 9, B_P = 10, B_O = 11, B_QD = 12;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(B_Q), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(B_CFULL + i), NST);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(B_CFREE + i), 1);
+    mbar_init(bar(B_S), 1);
+    mbar_init(bar(B_P), NST);
+    mbar_init(bar(B_O), 1);
+    mbar_init(bar(B_QD), 1);
+    fence_mbar_init();
+  }
+  if (tid < H) m_used[tid] = -INFINITY;
+  if (warp == W_PV) {
+    tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == W_QK && lane == 0) {
+    tma_prefetch_desc(&qlat_map);
+    tma_prefetch_desc(&qrope_map);
+  }
+  chain_wait();     // the previous kernel of the stream has completed
+  chain_release();  // the next one may be scheduled
+
+  // ---- this CTA's tokens, heaviest first: work item w = blockIdx.x + i * gridDim.x
+  // is the (w / num_seqs)-th latest query of sequence w % num_seqs; items past
+  // a sequence's end are skipped, a query at an invalid position gets a zero
+  // output and lse = -inf (and DSA_DEVERR_BATCH)
+  if (tid < NST) {
+    bool mine = false;
+    int4 tk = make_int4(0, 0, 0, 0);
+    const int64_t w = blockIdx.x + static_cast<int64_t>(tid) * gridDim.x;
+    if (w < static_cast<int64_t>(p.b.max_q) * p.b.num_seqs) {
+      const int seq = static_cast<int>(w % p.b.num_seqs);
+      const int qi = p.b.max_q - 1 - static_cast<int>(w / p.b.num_seqs);
+      const int qs = p.b.q_start[seq], qe = p.b.q_start[seq + 1];
+      if (qs < 0 || qe < qs || qe > p.b.num_q) {
+        atomicOr(p.status, DSA_DEVERR_BATCH);
+      } else if (qs + qi < qe) {
+        const int t = qs + qi;
+        const int pos = query_pos(p.b, t, p.status);
+        if (pos >= 0) {
+          const int64_t r0 = seq_base_row(p.b, seq);
+          mine = true;
+          tk = make_int4(t, pos, static_cast<int>(static_cast<uint32_t>(r0)),
+                         static_cast<int>(static_cast<uint64_t>(r0) >> 32));
+        } else {
+          uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(t) * H * 512);
+          for (int i = 0; i < H * 512 / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+          if (p.lse)
+            for (int h = 0; h < H; ++h) p.lse[static_cast<int64_t>(t) * H + h] = -INFINITY;
+        }
+      }
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, mine);
+    if (lane == 0) wcnt[warp] = __popc(bal);
+    named_bar_sync(1, NST);
+    int off = 0;
+    for (int w2 = 0; w2 < warp; ++w2) off += wcnt[w2];
+    if (mine) toks[off + __popc(bal & ((1u << lane) - 1u))] = tk;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  int ntok = 0;
+#pragma unroll
+  for (int w2 = 0; w2 < NSW; ++w2) ntok += wcnt[w2];
+  const uint32_t tbase = *tslot;
+  const uint64_t to = p.timeout_ns;
+  volatile int no_abort = 0;
+  auto tok_nb = [&](const int4& tk) { return (min(p.K, tk.y + 1) + 127) / 128; };
+
+  if (warp == W_QK) {
+    // ------------------------------------------------ QK issuer, and the query of each token
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(128, H, false, false);
+      bool ok = true;
+      uint32_t gu = 0;   // blocks of this CTA so far (barrier phases)
+      int nqd = 0, nq = 0;  // commits to B_QD, query loads issued
+      for (int i = 0; ok && i < ntok; ++i) {
+        const int4 tk = toks[i];
+        const int nb = tok_nb(tk);
+        if (i > 0) {  // the previous token's products have read the query tile
+          umma_commit(bar(B_QD));
+          ok = mbar_wait(bar(B_QD), nqd & 1, abort_flag, p.status, to);
+          ++nqd;
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
+        for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, tk.x * H, bar(B_Q));
+        tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, tk.x * H, bar(B_Q));
+        ok = mbar_wait(bar(B_Q), nq & 1, abort_flag, p.status, to);
+        ++nq;
+        for (int j = 0; ok && j < nb; ++j, ++gu) {
+          for (int g = 0; g < 4 && ok; ++g) {
+            ok = mbar_wait(bar(B_CFULL + g), gu & 1, abort_flag, p.status, to);
+            if (!ok) break;
+            fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05.mma reads
+            tc_fence_after();
+            const int i_end = g == 3 ? 9 : 2 * g + 2;
+            for (int s = 2 * g; s < i_end; ++s) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tbase + C::TM_S, sdesc_sw128(sC + s * C::CSUB + kk * 32, 0, 1024),
+                          sdesc_sw128(sQ + s * C::QSUB + kk * 32, 0, 1024), id_qk, (s | kk) != 0);
+            }
+          }
+          if (!ok) break;
+          umma_commit(bar(B_S));
+        }
+      }
+      umma_commit(bar(B_QD));  // drain this warp's products before exit
+      mbar_wait(bar(B_QD), nqd & 1, &no_abort, nullptr, to);
+      if (nq > 0) mbar_wait(bar(B_Q), (nq - 1) & 1, &no_abort, nullptr, to);  // the last copy landed
+    }
+    __syncwarp();
+  } else if (warp == W_PV) {
+    // ------------------------------------------------ P.V issuer: O^T (+)= C^T . P per block
+    if (lane == 0) {
+      constexpr uint32_t id_pv = idesc_bf16(128, H, true, C::P_MN);
+      bool ok = true;
+      uint32_t gu = 0;
+      int no = 0;  // commits to B_O (one per token)
+      for (int i = 0; ok && i < ntok; ++i) {
+        const int nb = tok_nb(toks[i]);
+        // the first product of a token overwrites O^T: its P arrives only
+        // after the softmax warps have read the previous token's O^T
+        for (int u = 0; u < nb; ++u, ++gu) {
+          ok = mbar_wait(bar(B_P), gu & 1, abort_flag, p.status, to);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16(tbase + C::TM_O + c * H,
+                        sdesc_sw128(sC + 2 * c * C::CSUB + kk * 2048, C::CSUB, 1024),
+                        sdesc_sw128(smem_u32(sm + C::OFF_P) + kk * 2048, 8192, 1024), id_pv,
+                        (u > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(bar(B_CFREE + c));
+          }
+        }
+        if (!ok) break;
+        umma_commit(bar(B_O));
+        ++no;
+      }
+      // drain: the last token's commit, or one more when none completed
+      // (after an abort nothing waits for B_O's phases any more)
+      if (no == 0 || !ok) {
+        umma_commit(bar(B_O));
+        ++no;
+      }
+      mbar_wait(bar(B_O), (no - 1) & 1, &no_abort, nullptr, to);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax / gather / output warps
+    const int quarter = warp & 3;
+    const int h0 = (warp >> 2) * HW;
+    const int key = quarter * 32 + lane;
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = p.scale_log2;
+    float lpart[HW];
+    float mneg[HW];
+    const int kch = tid & 7, rb = tid >> 3;
+    const uint32_t gdst0 = sC + rb * 128 + ((kch ^ (rb & 7)) << 4);
+    const uint16_t* kvk = p.kv + kch * 8;
+    // a token's row base, positions visible to it and index row
+    auto tok_row0 = [](const int4& tk) {
+      return static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(tk.w)) << 32) |
+                                  static_cast<uint32_t>(tk.z));
+    };
+    int gsel[RPT];
+    auto fetch_sel = [&](const int32_t* irow, int nv, int jj) {
+#pragma unroll
+      for (int c = 0; c < RPT; ++c) {
+        const int sl = jj * 128 + rb + GROW * c;
+        gsel[c] = sl < nv ? irow[sl] : -1;
+      }
+    };
+    int grow[RPT];
+    auto resolve_rows = [&](int gpos, int64_t grow0) {
+#pragma unroll
+      for (int c = 0; c < RPT; ++c) {
+        const int e = gsel[c];
+        const int64_t rr = grow0 + e;
+        const bool ok = e >= 0 && e <= gpos && rr >= 0 && rr < p.kv_rows;
+        if (!ok && e != -1 && kch == 0) atomicOr(p.status, DSA_DEVERR_INDEX);
+        grow[c] = ok ? static_cast<int>(rr) : 0;
+      }
+    };
+    auto issue = [&](int i) {
+      const uint32_t dst = gdst0 + i * C::CSUB;
+#pragma unroll
+      for (int c = 0; c < RPT; ++c)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + c * GROW * 128),
+                     "l"(kvk + static_cast<int64_t>(grow[c]) * 576 + 64 * i)
+                     : "memory");
+    };
+    auto signal = [&](int g) {
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(B_CFULL + g))
+                   : "memory");
+    };
+    uint32_t gu = 0;  // blocks of this CTA so far (barrier phases)
+    int e_next = -1;  // this thread's key in the next block
+    if (ntok > 0) {   // the first token's first block
+      const int4 tk = toks[0];
+      const int nv = min(p.K, tk.y + 1);
+      const int32_t* irow = p.idx + static_cast<int64_t>(tk.x) * p.K;
+      fetch_sel(irow, nv, 0);
+      resolve_rows(tk.y, tok_row0(tk));
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        issue(2 * g);
+        issue(2 * g + 1);
+        if (g == 3) issue(8);
+        signal(g);
+      }
+      e_next = key < nv ? irow[key] : -1;
+    }
+    bool alive = true;
+#pragma unroll 1
+    for (int i = 0; alive && i < ntok; ++i) {
+      const int4 tk = toks[i];
+      const int t = tk.x, pos = tk.y;
+      const int64_t row0 = tok_row0(tk);
+      const int nvalid = min(p.K, pos + 1), nb = (nvalid + 127) / 128;
+      const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.K;
+      const bool has_next = i + 1 < ntok;
+      const int4 tn = has_next ? toks[i + 1] : make_int4(0, -1, 0, 0);
+      const int nvalid_n = min(p.K, tn.y + 1);
+      const int32_t* idx_row_n = p.idx + static_cast<int64_t>(tn.x) * p.K;
+#pragma unroll
+      for (int h = 0; h < HW; ++h) {
+        lpart[h] = 0.f;
+        mneg[h] = INFINITY;
+      }
+#pragma unroll 1
+      for (int j = 0; j < nb; ++j, ++gu) {
+        const int u = j;
+        const bool more = j + 1 < nb;
+        const int e = e_next;
+        if (more) {
+          const int sn = (j + 1) * 128 + key;
+          e_next = sn < nvalid ? idx_row[sn] : -1;
+          fetch_sel(idx_row, nvalid, j + 1);
+        } else if (has_next) {  // the next token's first block
+          e_next = key < nvalid_n ? idx_row_n[key] : -1;
+          fetch_sel(idx_row_n, nvalid_n, 0);
+        }
+        if (!mbar_wait(bar(B_S), gu & 1, abort_flag, p.status, to)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        bool valid = e >= 0 && e <= pos;
+        if (valid) {
+          const int64_t rr = row0 + e;
+          valid = rr >= 0 && rr < p.kv_rows;
+        }
+        float d[HW];
+        tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
+        float dmax = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < HW; ++h) {
+          d[h] = fmaf(d[h], sl2, mneg[h]);
+          dmax = fmaxf(dmax, d[h]);
+        }
+        const bool exceed = valid && dmax > kRescaleThreshold;
+        const unsigned any = __any_sync(0xffffffffu, exceed);
+        if (lane == 0) flags[warp] = any ? 1 : 0;
+        named_bar_sync(1, NST);
+        int resc = 0;
+#pragma unroll
+        for (int w = 0; w < NSW; ++w) resc |= flags[w];
+        if (resc) {
+          tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
+#pragma unroll
+          for (int h = 0; h < HW; ++h) d[h] = valid ? d[h] * sl2 : -INFINITY;
+          head_reduce<HW, 16, true>(d, lane);
+          red[quarter * H + h0 + lane] = d[0];
+          named_bar_sync(1, NST);
+          if (tid < H) {
+            const float mo = m_used[tid];
+            const float mb = fmaxf(fmaxf(red[tid], red[H + tid]), fmaxf(red[2 * H + tid], red[3 * H + tid]));
+            const float mn = fmaxf(mo, mb);
+            fac[tid] = (mn == -INFINITY) ? 1.f : ex2(mo - mn);
+            m_used[tid] = mn;
+          }
+          named_bar_sync(1, NST);
+          tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
+#pragma unroll
+          for (int h = 0; h < HW; ++h) {
+            mneg[h] = -m_used[h0 + h];
+            lpart[h] *= fac[h0 + h];
+            d[h] = fmaf(d[h], sl2, mneg[h]);
+          }
+          if (u > 0) {
+#pragma unroll 1
+            for (int c = 0; c < 4 * (HW / 16); ++c) {
+              const int hh = (c % (HW / 16)) * 16;
+              const uint32_t col = C::TM_O + (c / (HW / 16)) * H + h0 + hh;
+              float o[16];
+              tmem_cols_load<16>(lane_base + col, o);
+#pragma unroll
+              for (int h = 0; h < 16; ++h) o[h] *= fac[h0 + hh + h];
+              tmem_cols_store<16>(lane_base + col, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        {  // P[key][h] = bf16(2^d), one 128-byte swizzled row per key
+          uint8_t* prow = sm + C::OFF_P + key * 128;
+#pragma unroll
+          for (int q = 0; q < HW / 8; ++q) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const int h = q * 8 + k2 * 2;
+              const float p0 = valid ? ex2(d[h]) : 0.f;
+              const float p1 = valid ? ex2(d[h + 1]) : 0.f;
+              lpart[h] += p0;
+              lpart[h + 1] += p1;
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              wv[k2] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            const int chunk = ((h0 >> 3) + q) ^ (key & 7);
+            *reinterpret_cast<uint4*>(prow + (chunk << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(B_P));
+        if (more || has_next) {
+          // refill: block j+1, or the next token's first block
+          if (more)
+            resolve_rows(pos, row0);
+          else
+            resolve_rows(tn.y, tok_row0(tn));
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            if (!mbar_wait(bar(B_CFREE + c), gu & 1, abort_flag, p.status, to)) {
+              alive = false;
+              break;
+            }
+            issue(2 * c);
+            issue(2 * c + 1);
+            if (c == 3) issue(8);
+            signal(c);
+          }
+          if (!alive) break;
+        }
+      }
+      if (!alive) break;
+      // ---- the token's output: row sums, then O^T / L from TMEM to global memory
+      head_reduce<HW, 16, false>(lpart, lane);
+      red[quarter * H + h0 + lane] = lpart[0];
+      named_bar_sync(1, NST);
+      if (tid < H) {
+        const float L = (red[tid] + red[H + tid]) + (red[2 * H + tid] + red[3 * H + tid]);
+        fac[tid] = L > 0.f ? 1.f / L : 0.f;
+        if (p.lse)
+          p.lse[static_cast<int64_t>(t) * H + tid] = L > 0.f ? (m_used[tid] + log2f(L)) * kLn2 : -INFINITY;
+        m_used[tid] = -INFINITY;  // the next token's running maximum
+      }
+      named_bar_sync(1, NST);
+      if (!mbar_wait(bar(B_O), i & 1, abort_flag, p.status, to)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      // dims 128c + key of this thread's 32 heads: lanes 2m and 2m+1 swap one
+      // value of each head pair, so that each writes one head's two dims
+      const bool odd = lane & 1;
+      uint16_t* orow = p.out + static_cast<int64_t>(t) * H * 512 + (key & ~1);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float o[HW];
+        tmem_cols_load<HW>(lane_base + C::TM_O + c * H + h0, o);
+#pragma unroll
+        for (int hp = 0; hp < HW / 2; ++hp) {
+          const float mine = odd ? o[2 * hp + 1] : o[2 * hp];
+          const float other = __shfl_xor_sync(0xffffffffu, odd ? o[2 * hp] : o[2 * hp + 1], 1);
+          const int h = h0 + 2 * hp + (odd ? 1 : 0);
+          const float f = fac[h];
+          const __nv_bfloat162 b2 = odd ? __floats2bfloat162_rn(other * f, mine * f)
+                                        : __floats2bfloat162_rn(mine * f, other * f);
+          *reinterpret_cast<uint32_t*>(orow + h * 512 + c * 128) = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == W_PV) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
 template <int H, int NSPLIT, bool PAGED, bool KV8>
 cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p,
                        cudaStream_t stream) {
@@ -857,6 +1329,29 @@ cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaPa
   return e;
 }
 
+template <int H>
+cudaError_t launch_mla_persistent(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p,
+                                  int grid, cudaStream_t stream) {
+  using C = MlaCfg<H>;
+  auto* kern = sparse_mla_persistent_kernel<H>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  prof_begin(stream);
+  cudaError_t e = launch_chained(kern, dim3(static_cast<unsigned>(grid)), dim3(C::NT), C::SMEM, stream, 1,
+                                 ql, qr, p);
+  prof_end(kLaunchMla, stream);
+  count_launch(kLaunchMla);
+  return e;
+}
+
+int g_mla_persistent = 1;
+
 template <int H, bool KV8>
 cudaError_t launch_h(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p, int nsplit,
                      bool paged, cudaStream_t stream) {
@@ -875,6 +1370,8 @@ cudaError_t launch_h(const CUtensorMap& ql, const CUtensorMap& qr, const MlaPara
 }
 
 }  // namespace
+
+void set_mla_persistent(bool on) { g_mla_persistent = on ? 1 : 0; }
 
 // CTAs per token (one cluster): a token's key blocks are split over several
 // CTAs when there are too few tokens to cover the SMs (decode).
@@ -933,6 +1430,24 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
     p.part = static_cast<float*>(ws);
   }
   const bool paged = b.block_table != nullptr && !direct_rows;
+  // prefill-sized launches of the 64-head model over bf16 rows of contiguous
+  // caches that L2 holds: a persistent grid of one CTA per SM (at most 256
+  // tokens each)
+  // (HBM-resident caches keep the CTA-per-token kernel, whose CTAs the
+  // hardware hands out as SMs free up: with rows from HBM the time per token
+  // varies, and the static token lists measured 4 % slower)
+  if (g_mla_persistent && nsplit == 1 && heads == 64 && !kv_fp8 && !paged && !direct_rows &&
+      !p.l2_prefetch) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms > 0 && b.num_q >= 2 * static_cast<int64_t>(sms)) {
+      const int64_t items = static_cast<int64_t>(b.max_q) * b.num_seqs;
+      const int64_t grid =
+          std::max<int64_t>(sms, (items + kMlaPersistMaxTokens - 1) / kMlaPersistMaxTokens);
+      return launch_mla_persistent<64>(ql, qr, p, static_cast<int>(grid), stream);
+    }
+  }
   if (kv_fp8) {  // FP8 KV rows: the model's 64 heads only
     if (heads != 64) return cudaErrorNotSupported;
     return launch_h<64, true>(ql, qr, p, nsplit, paged, stream);

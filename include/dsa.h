@@ -163,6 +163,17 @@ DSA_API int dsa_profile_collect(double* ms, uint64_t* launches, int n);
  * after this call (default 2e9).  Exposed so that tests can shorten it. */
 DSA_API void dsa_set_wait_timeout_ns(uint64_t ns);
 
+/* Kernel choice for sparse attention over many tokens (at least twice as many
+ * as the GPU has SMs) with 64 heads on bf16 rows of contiguous caches
+ * (dsa_sparse_mla_attn and the group calls): with `on` (the default) one
+ * persistent CTA per SM walks a list of tokens, overlapping each token's
+ * output and the next token's query and first gather with the current
+ * token's products; with 0, one CTA per token.  Both compute the same
+ * results bit for bit; the switch exists for tests and measurements.  Takes
+ * effect for launches after the call; not synchronised with launches on
+ * other host threads. */
+DSA_API void dsa_set_mla_persistent(int on);
+
 /* Test aid for the failure path: launch one CTA that waits on an mbarrier
  * nothing ever arrives on, bounded by the current wait limit, records
  * DSA_ERR_TIMEOUT in the status block of `d_ws` and exits cleanly. */

@@ -193,6 +193,73 @@ def test_mla_h16_ragged_batch():
     _mla_case([300, 77, 1000], [300, 5, 129], 16, 128, False, 9)
 
 
+def _mla_both_kernels(lens, qcounts, K, seed, holes=False, bad_pos=None, sample=()):
+    """64 heads, bf16 rows, at least twice as many tokens as SMs: the
+    persistent grid and the CTA-per-token kernel give bit-identical outputs
+    and lse; sampled rows match the oracle; a query at an invalid position
+    gets zeros and lse = -inf from both (and the batch error)."""
+    lay = synth.make_layout(lens, qcounts)
+    assert lay.num_q >= 2 * torch.cuda.get_device_properties(DEV).multi_processor_count
+    H = 64
+    host = synth.host_layers(lay, "S", H, ints=False, seed=seed)[0]
+    rng = np.random.default_rng(seed)
+    idx = np.full((lay.num_q, K), -1, np.int32)
+    for t in range(lay.num_q):
+        n = int(lay.q_pos[t]) + 1
+        take = min(n, K)
+        sel = np.sort(rng.choice(n, take, replace=False))
+        if holes and t % 3 == 0 and take > 10:
+            sel = sel[: take // 2]
+        idx[t, : len(sel)] = sel
+    q_pos = lay.q_pos.copy()
+    if bad_pos is not None:
+        q_pos[bad_pos] = lay.max_len  # outside [0, max_len)
+    d = device_layers([host], DEV)[0]
+    batch = dsa.Batch(lay.q_start, q_pos, lay.seq_row0, lay.max_len, device=DEV)
+    idx_d = torch.from_numpy(idx).to(DEV)
+    got = []
+    for persistent in (True, False):
+        out = torch.full((lay.num_q, H, 512), 3.0, dtype=torch.bfloat16, device=DEV)
+        lse = torch.full((lay.num_q, H), 5.0, dtype=torch.float32, device=DEV)
+        ws = dsa.workspace(dsa.lib.dsa_sparse_mla_workspace_size(batch.c, H, K), DEV)
+        dsa.set_mla_persistent(persistent)
+        try:
+            dsa.dsa_sparse_mla_attn(d["q_lat"], d["q_rope"], d["kv"], idx_d, batch, scale=1 / 16,
+                                    out=out, lse=lse, ws=ws)
+        finally:
+            dsa.set_mla_persistent(True)
+        if bad_pos is None:
+            dsa.status_fetch(ws)
+        else:
+            with pytest.raises(dsa.DsaError) as e:
+                dsa.status_fetch(ws)
+            assert e.value.status == dsa.DSA_ERR_DEVICE_INDEX
+        got.append((bits(out), lse.cpu().numpy()))
+    (op, lp), (ot, lt) = got
+    assert np.array_equal(op, ot), "outputs differ between the two kernels"
+    assert np.array_equal(lp.view(np.uint32), lt.view(np.uint32)), "lse differs between the two kernels"
+    if bad_pos is not None:
+        assert not op[bad_pos].any() and np.all(lp[bad_pos] == -np.inf)
+    rows = np.asarray([r for r in sample if r != bad_pos], np.int32)
+    pos, key0 = rows_meta(lay, rows)
+    ref_o, ref_l = oracle.sparse_mla(host["q_lat"][rows], host["q_rope"][rows], host["kv"],
+                                     np.arange(len(rows), dtype=np.int32), key0, idx[rows], 1 / 16)
+    o = op[rows].view(np.uint16).astype(np.uint32) << 16
+    assert_close(o.view(np.float32), ref_o, 2e-2, "out")
+    assert np.allclose(lp[rows], ref_l, rtol=0, atol=1e-3 * max(1.0, np.abs(ref_l).max()))
+
+
+def test_mla_persistent_grid_matches_per_token_kernel():
+    # three sequences of unequal query counts, short index rows and holes
+    _mla_both_kernels([3000, 700, 1500], [400, 300, 1000], 512, 21, holes=True,
+                      sample=[0, 1, 399, 400, 699, 700, 1100, 1699])
+    # 200 sequences (one of 200 queries, 199 of one): 40000 work items, more
+    # than 256 per SM, so the grid outgrows the SM count; most items are past
+    # their sequence's end; one query at an invalid position
+    _mla_both_kernels([300] + [50] * 199, [200] + [1] * 199, 128, 22, bad_pos=5,
+                      sample=[0, 4, 6, 199, 200, 398])
+
+
 @pytest.mark.parametrize("types", ["FSSS", "FFFF", "FSSSFSSS"])
 def test_group_tiny_bit_exact_indices(types):
     lay = synth.workload_layout("tiny")
