@@ -107,6 +107,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int32
       : "memory");
 }
 
+// 2-D tiled prefetch of one box into L2 (no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation is warp-wide: the whole warp executes these.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

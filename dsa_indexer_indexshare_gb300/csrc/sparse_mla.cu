@@ -605,23 +605,28 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       // d = scale*log2(e)*s - m: the exponent of P and the rescale test in one FFMA
       float d[HW];
       tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
-      float dmax = -INFINITY;
+      // the first block sets the running maximum; a later one raises it only
+      // when one of its scores exceeds it by more than the threshold
+      int resc = 1;
+      if (u > 0) {
+        float dmax = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < HW; ++h) {
-        d[h] = fmaf(d[h], sl2, mneg[h]);
-        dmax = fmaxf(dmax, d[h]);
+        for (int h = 0; h < HW; ++h) {
+          d[h] = fmaf(d[h], sl2, mneg[h]);
+          dmax = fmaxf(dmax, d[h]);
+        }
+        const bool exceed = valid && dmax > kRescaleThreshold;
+        const unsigned any = __any_sync(0xffffffffu, exceed);
+        if (lane == 0) flags[warp] = any ? 1 : 0;
+        named_bar_sync(1, NST);
+        resc = 0;
+#pragma unroll
+        for (int w = 0; w < NSW; ++w) resc |= flags[w];
+        if (resc) tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);  // raw scores again
       }
-      const bool exceed = valid && dmax > kRescaleThreshold;
-      const unsigned any = __any_sync(0xffffffffu, exceed);
-      if (lane == 0) flags[warp] = any ? 1 : 0;
-      named_bar_sync(1, NST);
-      int resc = 0;
-#pragma unroll
-      for (int w = 0; w < NSW; ++w) resc |= flags[w];
       if (resc) {
         // raise the running maximum to this block's maximum (rare after the
         // first block): exact per-head maximum over the valid keys
-        tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);  // raw scores again
 #pragma unroll
         for (int h = 0; h < HW; ++h) d[h] = valid ? d[h] * sl2 : -INFINITY;
         head_reduce<HW, 16, true>(d, lane);
@@ -996,6 +1001,11 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
         for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, tk.x * H, bar(B_Q));
         tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, tk.x * H, bar(B_Q));
+        if (i + 1 < ntok) {  // the next token's query into L2 (read from HBM it takes ~2.5 us)
+          const int tn = toks[i + 1].x;
+          for (int c = 0; c < 8; ++c) tma_prefetch_l2_2d(&qlat_map, 64 * c, tn * H);
+          tma_prefetch_l2_2d(&qrope_map, 0, tn * H);
+        }
         ok = mbar_wait(bar(B_Q), nq & 1, abort_flag, p.status, to);
         ++nq;
         for (int j = 0; ok && j < nb; ++j, ++gu) {
@@ -1167,21 +1177,26 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         }
         float d[HW];
         tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
-        float dmax = -INFINITY;
+        // the first block sets the running maximum; a later one raises it only
+        // when one of its scores exceeds it by more than the threshold
+        int resc = 1;
+        if (u > 0) {
+          float dmax = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < HW; ++h) {
-          d[h] = fmaf(d[h], sl2, mneg[h]);
-          dmax = fmaxf(dmax, d[h]);
+          for (int h = 0; h < HW; ++h) {
+            d[h] = fmaf(d[h], sl2, mneg[h]);
+            dmax = fmaxf(dmax, d[h]);
+          }
+          const bool exceed = valid && dmax > kRescaleThreshold;
+          const unsigned any = __any_sync(0xffffffffu, exceed);
+          if (lane == 0) flags[warp] = any ? 1 : 0;
+          named_bar_sync(1, NST);
+          resc = 0;
+#pragma unroll
+          for (int w = 0; w < NSW; ++w) resc |= flags[w];
+          if (resc) tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);  // raw scores again
         }
-        const bool exceed = valid && dmax > kRescaleThreshold;
-        const unsigned any = __any_sync(0xffffffffu, exceed);
-        if (lane == 0) flags[warp] = any ? 1 : 0;
-        named_bar_sync(1, NST);
-        int resc = 0;
-#pragma unroll
-        for (int w = 0; w < NSW; ++w) resc |= flags[w];
         if (resc) {
-          tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
 #pragma unroll
           for (int h = 0; h < HW; ++h) d[h] = valid ? d[h] * sl2 : -INFINITY;
           head_reduce<HW, 16, true>(d, lane);
