@@ -863,9 +863,9 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Prefill-sized launches (many tokens, 64 heads, bf16 rows of per-sequence
-// contiguous caches that L2 holds, one CTA per token): a persistent grid,
-// one CTA per SM, each walking a list of tokens.  A CTA per token pays, besides its blocks,
+// Prefill-sized launches (many tokens, 64 heads, bf16 rows of contiguous or
+// paged caches that L2 holds, one CTA per token): a persistent grid, one CTA
+// per SM, each walking a list of tokens.  A CTA per token pays, besides its blocks,
 // about 9.5 us of start-up and tail on GB300 (barrier and TMEM set-up,
 // metadata, the query and first gather, the pipeline fill, the output
 // written after the last product): about a sixth of an 8K prefill's
@@ -880,7 +880,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
 // so both give bit-identical results.
 constexpr int kMlaPersistMaxTokens = 256;  // tokens per CTA (one per softmax thread)
 
-template <int H>
+template <int H, bool PAGED>
 __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     sparse_mla_persistent_kernel(const __grid_constant__ CUtensorMap qlat_map,
                                  const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
@@ -890,8 +890,10 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   constexpr int W_QK = NSW, W_PV = NSW + 1;
   constexpr int GROW = NST / 8, RPT = 128 / GROW;
   static_assert(NST == kMlaPersistMaxTokens, "one list entry per softmax thread");
-  // the token list {t, pos, first cache row (lo, hi)} reuses the block-table
-  // and FP8-scale areas, which this variant does not use
+  // the token list {t, pos, first cache row (lo, hi)} -- {t, pos, sequence, 0}
+  // for paged caches -- reuses the block-table and FP8-scale areas, which
+  // this variant does not use (it reads a paged cache's block table through
+  // L1)
   static_assert(C::OFF_KSC + 128 * 16 - C::OFF_TAB >= kMlaPersistMaxTokens * 16, "token list");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -957,7 +959,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         const int t = qs + qi;
         const int pos = query_pos(p.b, t, p.status);
         if (pos >= 0) {
-          const int64_t r0 = seq_base_row(p.b, seq);
+          const int64_t r0 = PAGED ? seq : seq_base_row(p.b, seq);
           mine = true;
           tk = make_int4(t, pos, static_cast<int>(static_cast<uint32_t>(r0)),
                          static_cast<int>(static_cast<uint64_t>(r0) >> 32));
@@ -1087,10 +1089,19 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     const int kch = tid & 7, rb = tid >> 3;
     const uint32_t gdst0 = sC + rb * 128 + ((kch ^ (rb & 7)) << 4);
     const uint16_t* kvk = p.kv + kch * 8;
-    // a token's row base, positions visible to it and index row
-    auto tok_row0 = [](const int4& tk) {
-      return static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(tk.w)) << 32) |
-                                  static_cast<uint32_t>(tk.z));
+    // cache row of position e >= 0 of a listed token's sequence, -1 if unmapped
+    const int bps = p.b.blocks_per_seq;
+    const int rshift = PAGED ? __ffs(p.b.block_rows) - 1 : 0;  // block_rows is a power of two
+    auto row_of = [&](const int4& tk, int e) -> int64_t {
+      if constexpr (!PAGED) {
+        return static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(tk.w)) << 32) |
+                                    static_cast<uint32_t>(tk.z)) + e;
+      } else {
+        const int blk = e >> rshift;
+        if (blk >= bps) return -1;
+        const int32_t id = __ldg(p.b.block_table + static_cast<int64_t>(tk.z) * bps + blk);
+        return id < 0 ? -1 : (static_cast<int64_t>(id) << rshift) + (e & (p.b.block_rows - 1));
+      }
     };
     int gsel[RPT];
     auto fetch_sel = [&](const int32_t* irow, int nv, int jj) {
@@ -1101,12 +1112,12 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       }
     };
     int grow[RPT];
-    auto resolve_rows = [&](int gpos, int64_t grow0) {
+    auto resolve_rows = [&](const int4& gtk) {
 #pragma unroll
       for (int c = 0; c < RPT; ++c) {
         const int e = gsel[c];
-        const int64_t rr = grow0 + e;
-        const bool ok = e >= 0 && e <= gpos && rr >= 0 && rr < p.kv_rows;
+        const int64_t rr = e >= 0 ? row_of(gtk, e) : -1;
+        const bool ok = e >= 0 && e <= gtk.y && rr >= 0 && rr < p.kv_rows;
         if (!ok && e != -1 && kch == 0) atomicOr(p.status, DSA_DEVERR_INDEX);
         grow[c] = ok ? static_cast<int>(rr) : 0;
       }
@@ -1130,7 +1141,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       const int nv = min(p.K, tk.y + 1);
       const int32_t* irow = p.idx + static_cast<int64_t>(tk.x) * p.K;
       fetch_sel(irow, nv, 0);
-      resolve_rows(tk.y, tok_row0(tk));
+      resolve_rows(tk);
 #pragma unroll 1
       for (int g = 0; g < 4; ++g) {
         issue(2 * g);
@@ -1145,7 +1156,6 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     for (int i = 0; alive && i < ntok; ++i) {
       const int4 tk = toks[i];
       const int t = tk.x, pos = tk.y;
-      const int64_t row0 = tok_row0(tk);
       const int nvalid = min(p.K, pos + 1), nb = (nvalid + 127) / 128;
       const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.K;
       const bool has_next = i + 1 < ntok;
@@ -1177,7 +1187,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         tc_fence_after();
         bool valid = e >= 0 && e <= pos;
         if (valid) {
-          const int64_t rr = row0 + e;
+          const int64_t rr = row_of(tk, e);
           valid = rr >= 0 && rr < p.kv_rows;
         }
         float d[HW];
@@ -1261,9 +1271,9 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         if (more || has_next) {
           // refill: block j+1, or the next token's first block
           if (more)
-            resolve_rows(pos, row0);
+            resolve_rows(tk);
           else
-            resolve_rows(tn.y, tok_row0(tn));
+            resolve_rows(tn);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             if (!mbar_wait(bar(B_CFREE + c), gu & 1, abort_flag, p.status, to)) {
@@ -1349,11 +1359,11 @@ cudaError_t launch_mla(const CUtensorMap& ql, const CUtensorMap& qr, const MlaPa
   return e;
 }
 
-template <int H>
+template <int H, bool PAGED>
 cudaError_t launch_mla_persistent(const CUtensorMap& ql, const CUtensorMap& qr, const MlaParams& p,
                                   int grid, cudaStream_t stream) {
   using C = MlaCfg<H>;
-  auto* kern = sparse_mla_persistent_kernel<H>;
+  auto* kern = sparse_mla_persistent_kernel<H, PAGED>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1450,13 +1460,13 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
     p.part = static_cast<float*>(ws);
   }
   const bool paged = b.block_table != nullptr && !direct_rows;
-  // prefill-sized launches of the 64-head model over bf16 rows of contiguous
-  // caches that L2 holds: a persistent grid of one CTA per SM (at most 256
-  // tokens each)
+  // prefill-sized launches of the 64-head model over bf16 rows of caches
+  // that L2 holds (contiguous or paged): a persistent grid of one CTA per SM
+  // (at most 256 tokens each)
   // (HBM-resident caches keep the CTA-per-token kernel, whose CTAs the
   // hardware hands out as SMs free up: with rows from HBM the time per token
   // varies, and the static token lists measured 4 % slower)
-  if (g_mla_persistent && nsplit == 1 && heads == 64 && !kv_fp8 && !paged && !direct_rows &&
+  if (g_mla_persistent && nsplit == 1 && heads == 64 && !kv_fp8 && !direct_rows &&
       !p.l2_prefetch) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -1465,7 +1475,8 @@ cudaError_t launch_sparse_mla(const void* q_lat, const void* q_rope, const void*
       const int64_t items = static_cast<int64_t>(b.max_q) * b.num_seqs;
       const int64_t grid =
           std::max<int64_t>(sms, (items + kMlaPersistMaxTokens - 1) / kMlaPersistMaxTokens);
-      return launch_mla_persistent<64>(ql, qr, p, static_cast<int>(grid), stream);
+      return paged ? launch_mla_persistent<64, true>(ql, qr, p, static_cast<int>(grid), stream)
+                   : launch_mla_persistent<64, false>(ql, qr, p, static_cast<int>(grid), stream);
     }
   }
   if (kv_fp8) {  // FP8 KV rows: the model's 64 heads only

@@ -193,11 +193,12 @@ def test_mla_h16_ragged_batch():
     _mla_case([300, 77, 1000], [300, 5, 129], 16, 128, False, 9)
 
 
-def _mla_both_kernels(lens, qcounts, K, seed, holes=False, bad_pos=None, sample=()):
+def _mla_both_kernels(lens, qcounts, K, seed, holes=False, bad_pos=None, sample=(), page_rows=0):
     """64 heads, bf16 rows, at least twice as many tokens as SMs: the
     persistent grid and the CTA-per-token kernel give bit-identical outputs
-    and lse; sampled rows match the oracle; a query at an invalid position
-    gets zeros and lse = -inf from both (and the batch error)."""
+    and lse (on paged caches also equal to the contiguous cache's); sampled
+    rows match the oracle; a query at an invalid position gets zeros and
+    lse = -inf from both (and the batch error)."""
     lay = synth.make_layout(lens, qcounts)
     assert lay.num_q >= 2 * torch.cuda.get_device_properties(DEV).multi_processor_count
     H = 64
@@ -215,16 +216,16 @@ def _mla_both_kernels(lens, qcounts, K, seed, holes=False, bad_pos=None, sample=
     if bad_pos is not None:
         q_pos[bad_pos] = lay.max_len  # outside [0, max_len)
     d = device_layers([host], DEV)[0]
-    batch = dsa.Batch(lay.q_start, q_pos, lay.seq_row0, lay.max_len, device=DEV)
     idx_d = torch.from_numpy(idx).to(DEV)
-    got = []
-    for persistent in (True, False):
+    contiguous = dsa.Batch(lay.q_start, q_pos, lay.seq_row0, lay.max_len, device=DEV)
+
+    def run(batch, kv, persistent):
         out = torch.full((lay.num_q, H, 512), 3.0, dtype=torch.bfloat16, device=DEV)
         lse = torch.full((lay.num_q, H), 5.0, dtype=torch.float32, device=DEV)
         ws = dsa.workspace(dsa.lib.dsa_sparse_mla_workspace_size(batch.c, H, K), DEV)
         dsa.set_mla_persistent(persistent)
         try:
-            dsa.dsa_sparse_mla_attn(d["q_lat"], d["q_rope"], d["kv"], idx_d, batch, scale=1 / 16,
+            dsa.dsa_sparse_mla_attn(d["q_lat"], d["q_rope"], kv, idx_d, batch, scale=1 / 16,
                                     out=out, lse=lse, ws=ws)
         finally:
             dsa.set_mla_persistent(True)
@@ -234,10 +235,22 @@ def _mla_both_kernels(lens, qcounts, K, seed, holes=False, bad_pos=None, sample=
             with pytest.raises(dsa.DsaError) as e:
                 dsa.status_fetch(ws)
             assert e.value.status == dsa.DSA_ERR_DEVICE_INDEX
-        got.append((bits(out), lse.cpu().numpy()))
-    (op, lp), (ot, lt) = got
+        return bits(out), lse.cpu().numpy()
+
+    if page_rows:
+        table, (kv_paged,) = _page(lay, [host["kv"]], page_rows, seed=seed + 1)
+        batch = dsa.Batch(lay.q_start, q_pos, None, lay.max_len, device=DEV, block_table=table,
+                          block_rows=page_rows)
+        kv = bf16_dev(kv_paged, DEV)
+    else:
+        batch, kv = contiguous, d["kv"]
+    (op, lp), (ot, lt) = run(batch, kv, True), run(batch, kv, False)
     assert np.array_equal(op, ot), "outputs differ between the two kernels"
     assert np.array_equal(lp.view(np.uint32), lt.view(np.uint32)), "lse differs between the two kernels"
+    if page_rows:
+        oc, lc = run(contiguous, d["kv"], True)
+        assert np.array_equal(op, oc) and np.array_equal(lp.view(np.uint32), lc.view(np.uint32)), \
+            "paged and contiguous caches give different results"
     if bad_pos is not None:
         assert not op[bad_pos].any() and np.all(lp[bad_pos] == -np.inf)
     rows = np.asarray([r for r in sample if r != bad_pos], np.int32)
@@ -258,6 +271,9 @@ def test_mla_persistent_grid_matches_per_token_kernel():
     # their sequence's end; one query at an invalid position
     _mla_both_kernels([300] + [50] * 199, [200] + [1] * 199, 128, 22, bad_pos=5,
                       sample=[0, 4, 6, 199, 200, 398])
+    # paged caches (blocks of 128 positions over a permuted pool): two sequences
+    _mla_both_kernels([2500, 1300], [700, 400], 1024, 23, holes=True, page_rows=128,
+                      sample=[0, 1, 699, 700, 1099])
 
 
 @pytest.mark.parametrize("types", ["FSSS", "FFFF", "FSSSFSSS"])
