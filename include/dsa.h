@@ -164,8 +164,9 @@ DSA_API int dsa_profile_collect(double* ms, uint64_t* launches, int n);
 DSA_API void dsa_set_wait_timeout_ns(uint64_t ns);
 
 /* Kernel choice for sparse attention over many tokens (at least twice as many
- * as the GPU has SMs) with 64 heads on bf16 rows of contiguous caches
- * (dsa_sparse_mla_attn and the group calls): with `on` (the default) one
+ * as the GPU has SMs) with 64 heads on bf16 rows of contiguous or paged
+ * caches of at most 96 MB, which L2 holds (dsa_sparse_mla_attn and the group
+ * calls): with `on` (the default) one
  * persistent CTA per SM walks a list of tokens, overlapping each token's
  * output and the next token's query and first gather with the current
  * token's products; with 0, one CTA per token.  Both compute the same
