@@ -107,6 +107,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int32
       : "memory");
 }
 
+// Read-only global loads with an L1 eviction policy: a stream read once
+// (allocates no L1 line) and a small table read over and over (kept in L1
+// ahead of other lines).  Only for data no thread writes during the kernel.
+__device__ __forceinline__ int32_t ld_stream_i32(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int32_t ld_keep_i32(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.L1::evict_last.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 // 2-D tiled prefetch of one box into L2 (no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -1099,7 +1099,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       } else {
         const int blk = e >> rshift;
         if (blk >= bps) return -1;
-        const int32_t id = __ldg(p.b.block_table + static_cast<int64_t>(tk.z) * bps + blk);
+        const int32_t id = ld_keep_i32(p.b.block_table + static_cast<int64_t>(tk.z) * bps + blk);
         return id < 0 ? -1 : (static_cast<int64_t>(id) << rshift) + (e & (p.b.block_rows - 1));
       }
     };
@@ -1108,7 +1108,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
 #pragma unroll
       for (int c = 0; c < RPT; ++c) {
         const int sl = jj * 128 + rb + GROW * c;
-        gsel[c] = sl < nv ? irow[sl] : -1;
+        gsel[c] = sl < nv ? ld_stream_i32(irow + sl) : -1;
       }
     };
     int grow[RPT];
@@ -1149,7 +1149,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         if (g == 3) issue(8);
         signal(g);
       }
-      e_next = key < nv ? irow[key] : -1;
+      e_next = key < nv ? ld_stream_i32(irow + key) : -1;
     }
     bool alive = true;
 #pragma unroll 1
@@ -1174,22 +1174,31 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         const int e = e_next;
         if (more) {
           const int sn = (j + 1) * 128 + key;
-          e_next = sn < nvalid ? idx_row[sn] : -1;
+          e_next = sn < nvalid ? ld_stream_i32(idx_row + sn) : -1;
           fetch_sel(idx_row, nvalid, j + 1);
         } else if (has_next) {  // the next token's first block
-          e_next = key < nvalid_n ? idx_row_n[key] : -1;
+          e_next = key < nvalid_n ? ld_stream_i32(idx_row_n + key) : -1;
           fetch_sel(idx_row_n, nvalid_n, 0);
+        }
+        // this thread's key (a mapped row of a visible position?) and, for a
+        // paged cache, the refill's rows: their block-table lookups come
+        // before the wait, which hides their latency
+        bool valid = e >= 0 && e <= pos;
+        if (valid) {
+          const int64_t rr = row_of(tk, e);
+          valid = rr >= 0 && rr < p.kv_rows;
+        }
+        if constexpr (PAGED) {
+          if (more)
+            resolve_rows(tk);
+          else if (has_next)
+            resolve_rows(tn);
         }
         if (!mbar_wait(bar(B_S), gu & 1, abort_flag, p.status, to)) {
           alive = false;
           break;
         }
         tc_fence_after();
-        bool valid = e >= 0 && e <= pos;
-        if (valid) {
-          const int64_t rr = row_of(tk, e);
-          valid = rr >= 0 && rr < p.kv_rows;
-        }
         float d[HW];
         tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
         // the first block sets the running maximum; a later one raises it only
@@ -1270,10 +1279,12 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         mbar_arrive(bar(B_P));
         if (more || has_next) {
           // refill: block j+1, or the next token's first block
-          if (more)
-            resolve_rows(tk);
-          else
-            resolve_rows(tn);
+          if constexpr (!PAGED) {
+            if (more)
+              resolve_rows(tk);
+            else
+              resolve_rows(tn);
+          }
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             if (!mbar_wait(bar(B_CFREE + c), gu & 1, abort_flag, p.status, to)) {
