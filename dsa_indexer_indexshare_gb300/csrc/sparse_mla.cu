@@ -595,13 +595,15 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       if (more) fetch_sel(j + 1);  // consumed after P of this block
       if (j == j0) prefetch_rows();  // block j0 + 1
       if (j + 2 < j1) fetch_pf(j + 2);  // prefetched after this block's refill
-      if (!mbar_wait(bar(B_S), u & 1, abort_flag, p.status, to)) break;
-      tc_fence_after();
-      bool valid = e >= 0 && (p.direct || e <= pos);  // the gather's test, on this thread's key
+      // the gather's test on this thread's key, before the wait (which hides a
+      // paged cache's table lookup)
+      bool valid = e >= 0 && (p.direct || e <= pos);
       if (valid) {
         const int64_t rr = row_of(e);
         valid = rr >= 0 && rr < p.kv_rows;
       }
+      if (!mbar_wait(bar(B_S), u & 1, abort_flag, p.status, to)) break;
+      tc_fence_after();
       // d = scale*log2(e)*s - m: the exponent of P and the rescale test in one FFMA
       float d[HW];
       tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
