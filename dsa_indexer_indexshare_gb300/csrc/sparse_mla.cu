@@ -1160,10 +1160,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       const int t = tk.x, pos = tk.y;
       const int nvalid = min(p.K, pos + 1), nb = (nvalid + 127) / 128;
       const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.K;
-      const bool has_next = i + 1 < ntok;
-      const int4 tn = has_next ? toks[i + 1] : make_int4(0, -1, 0, 0);
-      const int nvalid_n = min(p.K, tn.y + 1);
-      const int32_t* idx_row_n = p.idx + static_cast<int64_t>(tn.x) * p.K;
+      const bool has_next = i + 1 < ntok;  // the next token's entry is read where it is used
 #pragma unroll
       for (int h = 0; h < HW; ++h) {
         lpart[h] = 0.f;
@@ -1179,6 +1176,9 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
           e_next = sn < nvalid ? ld_stream_i32(idx_row + sn) : -1;
           fetch_sel(idx_row, nvalid, j + 1);
         } else if (has_next) {  // the next token's first block
+          const int4 tn = toks[i + 1];
+          const int nvalid_n = min(p.K, tn.y + 1);
+          const int32_t* idx_row_n = p.idx + static_cast<int64_t>(tn.x) * p.K;
           e_next = key < nvalid_n ? ld_stream_i32(idx_row_n + key) : -1;
           fetch_sel(idx_row_n, nvalid_n, 0);
         }
@@ -1194,7 +1194,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
           if (more)
             resolve_rows(tk);
           else if (has_next)
-            resolve_rows(tn);
+            resolve_rows(toks[i + 1]);
         }
         if (!mbar_wait(bar(B_S), gu & 1, abort_flag, p.status, to)) {
           alive = false;
@@ -1285,7 +1285,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
             if (more)
               resolve_rows(tk);
             else
-              resolve_rows(tn);
+              resolve_rows(toks[i + 1]);
           }
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
