@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         asm volatile("cp.async.wait_group 2;" ::: "memory");
       else
         asm volatile("cp.async.wait_group 3;" ::: "memory");
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < RPT; ++c) {
         const int r = rb + GROW * c;
         // every code of row r is read (by its 8 threads, one warp) before any
