@@ -1086,8 +1086,9 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     const int key = quarter * 32 + lane;
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
-    float lpart[HW];
-    float mneg[HW];
+    float lpart[HW];  // this thread's share of the softmax denominators
+    // (the running maxima are read from shared memory where they are used:
+    // registers for them made this kernel spill)
     const int kch = tid & 7, rb = tid >> 3;
     const uint32_t gdst0 = sC + rb * 128 + ((kch ^ (rb & 7)) << 4);
     const uint16_t* kvk = p.kv + kch * 8;
@@ -1156,22 +1157,19 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     bool alive = true;
 #pragma unroll 1
     for (int i = 0; alive && i < ntok; ++i) {
-      const int4 tk = toks[i];
-      const int t = tk.x, pos = tk.y;
+      const int4 tk = toks[i];  // (its token index is read again where it is used)
+      const int pos = tk.y;
       const int nvalid = min(p.K, pos + 1), nb = (nvalid + 127) / 128;
-      const int32_t* idx_row = p.idx + static_cast<int64_t>(t) * p.K;
       const bool has_next = i + 1 < ntok;  // the next token's entry is read where it is used
 #pragma unroll
-      for (int h = 0; h < HW; ++h) {
-        lpart[h] = 0.f;
-        mneg[h] = INFINITY;
-      }
+      for (int h = 0; h < HW; ++h) lpart[h] = 0.f;
 #pragma unroll 1
       for (int j = 0; j < nb; ++j, ++gu) {
         const int u = j;
         const bool more = j + 1 < nb;
         const int e = e_next;
         if (more) {
+          const int32_t* idx_row = p.idx + static_cast<int64_t>(toks[i].x) * p.K;
           const int sn = (j + 1) * 128 + key;
           e_next = sn < nvalid ? ld_stream_i32(idx_row + sn) : -1;
           fetch_sel(idx_row, nvalid, j + 1);
@@ -1210,7 +1208,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
           float dmax = -INFINITY;
 #pragma unroll
           for (int h = 0; h < HW; ++h) {
-            d[h] = fmaf(d[h], sl2, mneg[h]);
+            d[h] = fmaf(d[h], sl2, -m_used[h0 + h]);
             dmax = fmaxf(dmax, d[h]);
           }
           const bool exceed = valid && dmax > kRescaleThreshold;
@@ -1239,9 +1237,8 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
           tmem_cols_load<HW>(lane_base + C::TM_S + h0, d);
 #pragma unroll
           for (int h = 0; h < HW; ++h) {
-            mneg[h] = -m_used[h0 + h];
             lpart[h] *= fac[h0 + h];
-            d[h] = fmaf(d[h], sl2, mneg[h]);
+            d[h] = fmaf(d[h], sl2, -m_used[h0 + h]);
           }
           if (u > 0) {
 #pragma unroll 1
@@ -1310,7 +1307,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         const float L = (red[tid] + red[H + tid]) + (red[2 * H + tid] + red[3 * H + tid]);
         fac[tid] = L > 0.f ? 1.f / L : 0.f;
         if (p.lse)
-          p.lse[static_cast<int64_t>(t) * H + tid] = L > 0.f ? (m_used[tid] + log2f(L)) * kLn2 : -INFINITY;
+          p.lse[static_cast<int64_t>(toks[i].x) * H + tid] = L > 0.f ? (m_used[tid] + log2f(L)) * kLn2 : -INFINITY;
         m_used[tid] = -INFINITY;  // the next token's running maximum
       }
       named_bar_sync(1, NST);
@@ -1322,7 +1319,7 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
       // dims 128c + key of this thread's 32 heads: lanes 2m and 2m+1 swap one
       // value of each head pair, so that each writes one head's two dims
       const bool odd = lane & 1;
-      uint16_t* orow = p.out + static_cast<int64_t>(t) * H * 512 + (key & ~1);
+      uint16_t* orow = p.out + static_cast<int64_t>(toks[i].x) * H * 512 + (key & ~1);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float o[HW];
