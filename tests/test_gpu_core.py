@@ -271,6 +271,10 @@ def test_mla_persistent_grid_matches_per_token_kernel():
     # their sequence's end; one query at an invalid position
     _mla_both_kernels([300] + [50] * 199, [200] + [1] * 199, 128, 22, bad_pos=5,
                       sample=[0, 4, 6, 199, 200, 398])
+    # 304 sequences, one of 400 queries and 303 of one: 121,600 work items over
+    # 475 CTAs for 703 tokens, so some CTAs get an empty list
+    _mla_both_kernels([500] + [30] * 303, [400] + [1] * 303, 64, 27,
+                      sample=[0, 1, 399, 400, 702])
     # paged caches (blocks of 128 positions over a permuted pool): two sequences
     _mla_both_kernels([2500, 1300], [700, 400], 1024, 23, holes=True, page_rows=128,
                       sample=[0, 1, 699, 700, 1099])
