@@ -197,6 +197,45 @@ __device__ __forceinline__ void tmem_cols_store(uint32_t taddr, const float (&v)
     tmem_st32(taddr, v);
 }
 
+// MMA issue.  One thread issues every product of a block, and the tensor
+// pipe takes an M128 N64 K16 bf16 MMA every ~49 cycles; computing each
+// operand descriptor from a run-time sub-tile or chunk index cost the issuing
+// thread more than that (measured: ~72 cycles per QK and ~66 per P.V MMA with
+// those loops, ~49 fully unrolled).  So the issuers take a descriptor of each
+// tile's base once and step through the tile with compile-time offsets: the
+// start-address field holds (address >> 4) in its low 14 bits and every tile
+// ends below 256 KB of shared memory, so adding offset >> 4 to the 64-bit
+// descriptor never carries out of the field.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t base, uint32_t byte_off) {
+  return base + (byte_off >> 4);
+}
+
+// S^T (+)= C_s . Q_s^T for the sub-tiles s of dims group G (0-2: two latent
+// sub-tiles; 3: the last two latent sub-tiles and the RoPE sub-tile).
+template <int G, class C>
+__device__ __forceinline__ void issue_qk_group(uint32_t d_s, uint64_t dc, uint64_t dq,
+                                               uint32_t idesc) {
+  constexpr int s_end = G == 3 ? 9 : 2 * G + 2;
+#pragma unroll
+  for (int s = 2 * G; s < s_end; ++s)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      umma_bf16(d_s, sdesc_at(dc, s * C::CSUB + kk * 32), sdesc_at(dq, s * C::QSUB + kk * 32),
+                idesc, (s | kk) != 0);
+}
+
+// O^T chunk c (+)= C^T . P over the block's 128 keys (K = 16 per MMA); the
+// first MMA of a token's first block overwrites the accumulator.
+template <int c, class C>
+__device__ __forceinline__ void issue_pv_chunk(uint32_t d_o, uint64_t dcv, uint64_t dp,
+                                               uint32_t idesc, bool first) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    umma_bf16(d_o, sdesc_at(dcv, 2 * c * C::CSUB + kk * 2048),
+              sdesc_at(dp, C::P_MN ? kk * 2048 : (kk >> 2) * C::PSUB + (kk & 3) * 32), idesc,
+              (kk > 0 || !first) ? 1u : 0u);
+}
+
 // bf16 bits of four E4M3 codes (one 32-bit word, lowest byte first) times
 // their group scale: the codes widen exactly to fp16 then fp32, the fp32
 // products round to nearest even (two lanes per packed multiply), and each
@@ -345,21 +384,25 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     // ------------------------------------------------ QK issuer: S^T = C . Q^T per block
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, H, false, false);
+      const uint64_t dc = sdesc_sw128(sC, 0, 1024), dq = sdesc_sw128(sQ, 0, 1024);
+      const uint32_t d_s = tbase + C::TM_S;
       bool ok = mbar_wait(bar(B_Q), 0, abort_flag, p.status, to);
       for (int j = j0; ok && j < j1; ++j) {
         const int u = j - j0;
-        for (int g = 0; g < 4 && ok; ++g) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
           ok = mbar_wait(bar(B_CFULL + g), u & 1, abort_flag, p.status, to);
           if (!ok) break;
           fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05.mma reads
           tc_fence_after();
-          const int i_end = g == 3 ? 9 : 2 * g + 2;
-          for (int i = 2 * g; i < i_end; ++i) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tbase + C::TM_S, sdesc_sw128(sC + i * C::CSUB + kk * 32, 0, 1024),
-                        sdesc_sw128(sQ + i * C::QSUB + kk * 32, 0, 1024), id_qk, (i | kk) != 0);
-          }
+          if (g == 0)
+            issue_qk_group<0, C>(d_s, dc, dq, id_qk);
+          else if (g == 1)
+            issue_qk_group<1, C>(d_s, dc, dq, id_qk);
+          else if (g == 2)
+            issue_qk_group<2, C>(d_s, dc, dq, id_qk);
+          else
+            issue_qk_group<3, C>(d_s, dc, dq, id_qk);
         }
         if (!ok) break;
         umma_commit(bar(B_S));
@@ -373,24 +416,23 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     // ------------------------------------------------ P.V issuer: O^T += C^T . P per block
     if (lane == 0) {
       constexpr uint32_t id_pv = idesc_bf16(128, H, true, C::P_MN);
+      const uint64_t dcv = sdesc_sw128(sC, C::CSUB, 1024);
+      const uint64_t dp = C::P_MN ? sdesc_sw128(sP, 8192, 1024) : sdesc_sw128(sP, 0, 1024);
+      const uint32_t d_o = tbase + C::TM_O;
       bool ok = true;
       for (int j = j0; ok && j < j1; ++j) {
         const int u = j - j0;
         ok = mbar_wait(bar(B_P), u & 1, abort_flag, p.status, to);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16(tbase + C::TM_O + c * H,
-                      sdesc_sw128(sC + 2 * c * C::CSUB + kk * 2048, C::CSUB, 1024),
-                      C::P_MN ? sdesc_sw128(sP + kk * 2048, 8192, 1024)
-                              : sdesc_sw128(sP + (kk >> 2) * C::PSUB + (kk & 3) * 32, 0, 1024),
-                      id_pv,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar(B_CFREE + c));
-        }
+        issue_pv_chunk<0, C>(d_o, dcv, dp, id_pv, u == 0);
+        umma_commit(bar(B_CFREE + 0));
+        issue_pv_chunk<1, C>(d_o + H, dcv, dp, id_pv, u == 0);
+        umma_commit(bar(B_CFREE + 1));
+        issue_pv_chunk<2, C>(d_o + 2 * H, dcv, dp, id_pv, u == 0);
+        umma_commit(bar(B_CFREE + 2));
+        issue_pv_chunk<3, C>(d_o + 3 * H, dcv, dp, id_pv, u == 0);
+        umma_commit(bar(B_CFREE + 3));
       }
       umma_commit(bar(B_O));
       mbar_wait(bar(B_O), 0, &no_abort, nullptr, to);
@@ -1007,6 +1049,8 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     // ------------------------------------------------ QK issuer, and the query of each token
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, H, false, false);
+      const uint64_t dc = sdesc_sw128(sC, 0, 1024), dq = sdesc_sw128(sQ, 0, 1024);
+      const uint32_t d_s = tbase + C::TM_S;
       bool ok = true;
       uint32_t gu = 0;   // blocks of this CTA so far (barrier phases)
       int nqd = 0, nq = 0;  // commits to B_QD, query loads issued
@@ -1030,18 +1074,20 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
         ok = mbar_wait(bar(B_Q), nq & 1, abort_flag, p.status, to);
         ++nq;
         for (int j = 0; ok && j < nb; ++j, ++gu) {
-          for (int g = 0; g < 4 && ok; ++g) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
             ok = mbar_wait(bar(B_CFULL + g), gu & 1, abort_flag, p.status, to);
             if (!ok) break;
             fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05.mma reads
             tc_fence_after();
-            const int i_end = g == 3 ? 9 : 2 * g + 2;
-            for (int s = 2 * g; s < i_end; ++s) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_bf16(tbase + C::TM_S, sdesc_sw128(sC + s * C::CSUB + kk * 32, 0, 1024),
-                          sdesc_sw128(sQ + s * C::QSUB + kk * 32, 0, 1024), id_qk, (s | kk) != 0);
-            }
+            if (g == 0)
+              issue_qk_group<0, C>(d_s, dc, dq, id_qk);
+            else if (g == 1)
+              issue_qk_group<1, C>(d_s, dc, dq, id_qk);
+            else if (g == 2)
+              issue_qk_group<2, C>(d_s, dc, dq, id_qk);
+            else
+              issue_qk_group<3, C>(d_s, dc, dq, id_qk);
           }
           if (!ok) break;
           umma_commit(bar(B_S));
@@ -1056,6 +1102,10 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
     // ------------------------------------------------ P.V issuer: O^T (+)= C^T . P per block
     if (lane == 0) {
       constexpr uint32_t id_pv = idesc_bf16(128, H, true, C::P_MN);
+      static_assert(C::P_MN, "the persistent grid keeps P MN-major");
+      const uint64_t dcv = sdesc_sw128(sC, C::CSUB, 1024);
+      const uint64_t dp = sdesc_sw128(smem_u32(sm + C::OFF_P), 8192, 1024);
+      const uint32_t d_o = tbase + C::TM_O;
       bool ok = true;
       uint32_t gu = 0;
       int no = 0;  // commits to B_O (one per token)
@@ -1067,16 +1117,14 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
           ok = mbar_wait(bar(B_P), gu & 1, abort_flag, p.status, to);
           if (!ok) break;
           tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_bf16(tbase + C::TM_O + c * H,
-                        sdesc_sw128(sC + 2 * c * C::CSUB + kk * 2048, C::CSUB, 1024),
-                        sdesc_sw128(smem_u32(sm + C::OFF_P) + kk * 2048, 8192, 1024), id_pv,
-                        (u > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(bar(B_CFREE + c));
-          }
+          issue_pv_chunk<0, C>(d_o, dcv, dp, id_pv, u == 0);
+          umma_commit(bar(B_CFREE + 0));
+          issue_pv_chunk<1, C>(d_o + H, dcv, dp, id_pv, u == 0);
+          umma_commit(bar(B_CFREE + 1));
+          issue_pv_chunk<2, C>(d_o + 2 * H, dcv, dp, id_pv, u == 0);
+          umma_commit(bar(B_CFREE + 2));
+          issue_pv_chunk<3, C>(d_o + 3 * H, dcv, dp, id_pv, u == 0);
+          umma_commit(bar(B_CFREE + 3));
         }
         if (!ok) break;
         umma_commit(bar(B_O));
