@@ -207,7 +207,8 @@ __device__ __forceinline__ void tmem_cols_store(uint32_t taddr, const float (&v)
 // ends below 256 KB of shared memory, so adding offset >> 4 to the 64-bit
 // descriptor never carries out of the field.
 __device__ __forceinline__ uint64_t sdesc_at(uint64_t base, uint32_t byte_off) {
-  return base + (byte_off >> 4);
+  // only the low word changes: one add per descriptor
+  return (base & 0xFFFFFFFF00000000ull) | (static_cast<uint32_t>(base) + (byte_off >> 4));
 }
 
 // S^T (+)= C_s . Q_s^T for the sub-tiles s of dims group G (0-2: two latent
@@ -215,6 +216,9 @@ __device__ __forceinline__ uint64_t sdesc_at(uint64_t base, uint32_t byte_off) {
 template <int G, class C>
 __device__ __forceinline__ void issue_qk_group(uint32_t d_s, uint64_t dc, uint64_t dq,
                                                uint32_t idesc) {
+  // the bases are opaque here, so the descriptors are formed as they are
+  // issued rather than all kept in registers across the block loop
+  asm volatile("" : "+l"(dc), "+l"(dq));
   constexpr int s_end = G == 3 ? 9 : 2 * G + 2;
 #pragma unroll
   for (int s = 2 * G; s < s_end; ++s)
@@ -229,6 +233,7 @@ __device__ __forceinline__ void issue_qk_group(uint32_t d_s, uint64_t dc, uint64
 template <int c, class C>
 __device__ __forceinline__ void issue_pv_chunk(uint32_t d_o, uint64_t dcv, uint64_t dp,
                                                uint32_t idesc, bool first) {
+  asm volatile("" : "+l"(dcv), "+l"(dp));
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
     umma_bf16(d_o, sdesc_at(dcv, 2 * c * C::CSUB + kk * 2048),
@@ -937,12 +942,12 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
 constexpr int kMlaPersistMaxTokens = 256;  // tokens per CTA (one per softmax thread)
 
 template <int H, bool PAGED>
-__global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
+__global__ void __launch_bounds__(MlaCfg<H>::NT + 64, 1)
     sparse_mla_persistent_kernel(const __grid_constant__ CUtensorMap qlat_map,
                                  const __grid_constant__ CUtensorMap qrope_map, const MlaParams p) {
   using C = MlaCfg<H>;
   static_assert(H == 64, "the persistent variant covers the 64-head model");
-  constexpr int HW = C::HW, NSW = C::NSW, NT = C::NT, NST = NSW * 32;
+  constexpr int HW = C::HW, NSW = C::NSW, NST = NSW * 32;
   constexpr int W_QK = NSW, W_PV = NSW + 1;
   constexpr int GROW = NST / 8, RPT = 128 / GROW;
   static_assert(NST == kMlaPersistMaxTokens, "one list entry per softmax thread");
@@ -1045,101 +1050,110 @@ __global__ void __launch_bounds__(MlaCfg<H>::NT, 1)
   volatile int no_abort = 0;
   auto tok_nb = [&](const int4& tk) { return (min(p.K, tk.y + 1) + 127) / 128; };
 
-  if (warp == W_QK) {
-    // ------------------------------------------------ QK issuer, and the query of each token
-    if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16(128, H, false, false);
-      const uint64_t dc = sdesc_sw128(sC, 0, 1024), dq = sdesc_sw128(sQ, 0, 1024);
-      const uint32_t d_s = tbase + C::TM_S;
-      bool ok = true;
-      uint32_t gu = 0;   // blocks of this CTA so far (barrier phases)
-      int nqd = 0, nq = 0;  // commits to B_QD, query loads issued
-      for (int i = 0; ok && i < ntok; ++i) {
-        const int4 tk = toks[i];
-        const int nb = tok_nb(tk);
-        if (i > 0) {  // the previous token's products have read the query tile
-          umma_commit(bar(B_QD));
-          ok = mbar_wait(bar(B_QD), nqd & 1, abort_flag, p.status, to);
-          ++nqd;
-          if (!ok) break;
-        }
-        mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
-        for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, tk.x * H, bar(B_Q));
-        tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, tk.x * H, bar(B_Q));
-        if (i + 1 < ntok) {  // the next token's query into L2 (read from HBM it takes ~2.5 us)
-          const int tn = toks[i + 1].x;
-          for (int c = 0; c < 8; ++c) tma_prefetch_l2_2d(&qlat_map, 64 * c, tn * H);
-          tma_prefetch_l2_2d(&qrope_map, 0, tn * H);
-        }
-        ok = mbar_wait(bar(B_Q), nq & 1, abort_flag, p.status, to);
-        ++nq;
-        for (int j = 0; ok && j < nb; ++j, ++gu) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            ok = mbar_wait(bar(B_CFULL + g), gu & 1, abort_flag, p.status, to);
+  // Register split: the QK and P.V issuer warps and two idle ones form the
+  // third warpgroup and give up registers to the eight softmax warps.  At
+  // launch every thread has 168 (three warps share a sub-partition's 16K);
+  // 128 x 88 + 256 x 208 = 384 x 168, so the increase always completes.
+  // Each branch runs under its own limit up to the common tail.
+  if (warp >= NSW) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+    if (warp == W_QK) {
+      // ------------------------------------------------ QK issuer, and the query of each token
+      if (lane == 0) {
+        constexpr uint32_t id_qk = idesc_bf16(128, H, false, false);
+        const uint64_t dc = sdesc_sw128(sC, 0, 1024), dq = sdesc_sw128(sQ, 0, 1024);
+        const uint32_t d_s = tbase + C::TM_S;
+        bool ok = true;
+        uint32_t gu = 0;   // blocks of this CTA so far (barrier phases)
+        int nqd = 0, nq = 0;  // commits to B_QD, query loads issued
+        for (int i = 0; ok && i < ntok; ++i) {
+          const int4 tk = toks[i];
+          const int nb = tok_nb(tk);
+          if (i > 0) {  // the previous token's products have read the query tile
+            umma_commit(bar(B_QD));
+            ok = mbar_wait(bar(B_QD), nqd & 1, abort_flag, p.status, to);
+            ++nqd;
             if (!ok) break;
-            fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05.mma reads
+          }
+          mbar_arrive_expect_tx(bar(B_Q), C::Q_BYTES);
+          for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * C::QSUB, &qlat_map, 64 * c, tk.x * H, bar(B_Q));
+          tma_load_2d(sQ + 8 * C::QSUB, &qrope_map, 0, tk.x * H, bar(B_Q));
+          if (i + 1 < ntok) {  // the next token's query into L2 (read from HBM it takes ~2.5 us)
+            const int tn = toks[i + 1].x;
+            for (int c = 0; c < 8; ++c) tma_prefetch_l2_2d(&qlat_map, 64 * c, tn * H);
+            tma_prefetch_l2_2d(&qrope_map, 0, tn * H);
+          }
+          ok = mbar_wait(bar(B_Q), nq & 1, abort_flag, p.status, to);
+          ++nq;
+          for (int j = 0; ok && j < nb; ++j, ++gu) {
+  #pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              ok = mbar_wait(bar(B_CFULL + g), gu & 1, abort_flag, p.status, to);
+              if (!ok) break;
+              fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05.mma reads
+              tc_fence_after();
+              if (g == 0)
+                issue_qk_group<0, C>(d_s, dc, dq, id_qk);
+              else if (g == 1)
+                issue_qk_group<1, C>(d_s, dc, dq, id_qk);
+              else if (g == 2)
+                issue_qk_group<2, C>(d_s, dc, dq, id_qk);
+              else
+                issue_qk_group<3, C>(d_s, dc, dq, id_qk);
+            }
+            if (!ok) break;
+            umma_commit(bar(B_S));
+          }
+        }
+        umma_commit(bar(B_QD));  // drain this warp's products before exit
+        mbar_wait(bar(B_QD), nqd & 1, &no_abort, nullptr, to);
+        if (nq > 0) mbar_wait(bar(B_Q), (nq - 1) & 1, &no_abort, nullptr, to);  // the last copy landed
+      }
+      __syncwarp();
+    } else if (warp == W_PV) {
+      // ------------------------------------------------ P.V issuer: O^T (+)= C^T . P per block
+      if (lane == 0) {
+        constexpr uint32_t id_pv = idesc_bf16(128, H, true, C::P_MN);
+        static_assert(C::P_MN, "the persistent grid keeps P MN-major");
+        const uint64_t dcv = sdesc_sw128(sC, C::CSUB, 1024);
+        const uint64_t dp = sdesc_sw128(smem_u32(sm + C::OFF_P), 8192, 1024);
+        const uint32_t d_o = tbase + C::TM_O;
+        bool ok = true;
+        uint32_t gu = 0;
+        int no = 0;  // commits to B_O (one per token)
+        for (int i = 0; ok && i < ntok; ++i) {
+          const int nb = tok_nb(toks[i]);
+          // the first product of a token overwrites O^T: its P arrives only
+          // after the softmax warps have read the previous token's O^T
+          for (int u = 0; u < nb; ++u, ++gu) {
+            ok = mbar_wait(bar(B_P), gu & 1, abort_flag, p.status, to);
+            if (!ok) break;
             tc_fence_after();
-            if (g == 0)
-              issue_qk_group<0, C>(d_s, dc, dq, id_qk);
-            else if (g == 1)
-              issue_qk_group<1, C>(d_s, dc, dq, id_qk);
-            else if (g == 2)
-              issue_qk_group<2, C>(d_s, dc, dq, id_qk);
-            else
-              issue_qk_group<3, C>(d_s, dc, dq, id_qk);
+            issue_pv_chunk<0, C>(d_o, dcv, dp, id_pv, u == 0);
+            umma_commit(bar(B_CFREE + 0));
+            issue_pv_chunk<1, C>(d_o + H, dcv, dp, id_pv, u == 0);
+            umma_commit(bar(B_CFREE + 1));
+            issue_pv_chunk<2, C>(d_o + 2 * H, dcv, dp, id_pv, u == 0);
+            umma_commit(bar(B_CFREE + 2));
+            issue_pv_chunk<3, C>(d_o + 3 * H, dcv, dp, id_pv, u == 0);
+            umma_commit(bar(B_CFREE + 3));
           }
           if (!ok) break;
-          umma_commit(bar(B_S));
+          umma_commit(bar(B_O));
+          ++no;
         }
-      }
-      umma_commit(bar(B_QD));  // drain this warp's products before exit
-      mbar_wait(bar(B_QD), nqd & 1, &no_abort, nullptr, to);
-      if (nq > 0) mbar_wait(bar(B_Q), (nq - 1) & 1, &no_abort, nullptr, to);  // the last copy landed
-    }
-    __syncwarp();
-  } else if (warp == W_PV) {
-    // ------------------------------------------------ P.V issuer: O^T (+)= C^T . P per block
-    if (lane == 0) {
-      constexpr uint32_t id_pv = idesc_bf16(128, H, true, C::P_MN);
-      static_assert(C::P_MN, "the persistent grid keeps P MN-major");
-      const uint64_t dcv = sdesc_sw128(sC, C::CSUB, 1024);
-      const uint64_t dp = sdesc_sw128(smem_u32(sm + C::OFF_P), 8192, 1024);
-      const uint32_t d_o = tbase + C::TM_O;
-      bool ok = true;
-      uint32_t gu = 0;
-      int no = 0;  // commits to B_O (one per token)
-      for (int i = 0; ok && i < ntok; ++i) {
-        const int nb = tok_nb(toks[i]);
-        // the first product of a token overwrites O^T: its P arrives only
-        // after the softmax warps have read the previous token's O^T
-        for (int u = 0; u < nb; ++u, ++gu) {
-          ok = mbar_wait(bar(B_P), gu & 1, abort_flag, p.status, to);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv_chunk<0, C>(d_o, dcv, dp, id_pv, u == 0);
-          umma_commit(bar(B_CFREE + 0));
-          issue_pv_chunk<1, C>(d_o + H, dcv, dp, id_pv, u == 0);
-          umma_commit(bar(B_CFREE + 1));
-          issue_pv_chunk<2, C>(d_o + 2 * H, dcv, dp, id_pv, u == 0);
-          umma_commit(bar(B_CFREE + 2));
-          issue_pv_chunk<3, C>(d_o + 3 * H, dcv, dp, id_pv, u == 0);
-          umma_commit(bar(B_CFREE + 3));
+        // drain: the last token's commit, or one more when none completed
+        // (after an abort nothing waits for B_O's phases any more)
+        if (no == 0 || !ok) {
+          umma_commit(bar(B_O));
+          ++no;
         }
-        if (!ok) break;
-        umma_commit(bar(B_O));
-        ++no;
+        mbar_wait(bar(B_O), (no - 1) & 1, &no_abort, nullptr, to);
       }
-      // drain: the last token's commit, or one more when none completed
-      // (after an abort nothing waits for B_O's phases any more)
-      if (no == 0 || !ok) {
-        umma_commit(bar(B_O));
-        ++no;
-      }
-      mbar_wait(bar(B_O), (no - 1) & 1, &no_abort, nullptr, to);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
     // ------------------------------------------------ softmax / gather / output warps
     const int quarter = warp & 3;
     const int h0 = (warp >> 2) * HW;
@@ -1443,8 +1457,9 @@ cudaError_t launch_mla_persistent(const CUtensorMap& ql, const CUtensorMap& qr, 
     configured_device = dev;
   }
   prof_begin(stream);
-  cudaError_t e = launch_chained(kern, dim3(static_cast<unsigned>(grid)), dim3(C::NT), C::SMEM, stream, 1,
-                                 ql, qr, p);
+  // the softmax warps, the QK and P.V issuers and two idle warps (the issuers' warpgroup)
+  cudaError_t e = launch_chained(kern, dim3(static_cast<unsigned>(grid)), dim3(C::NT + 64), C::SMEM,
+                                 stream, 1, ql, qr, p);
   prof_end(kLaunchMla, stream);
   count_launch(kLaunchMla);
   return e;
